@@ -1,0 +1,212 @@
+/*
+ * poetx.h -- C ABI of the POET-X orthogonal-equivalence linear layer on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The layer.  W = R W0 P with W0 (m x n) frozen and R (m x m), P (n x n)
+ * orthogonal ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+ * Transformation", gist.science summary, Methodologie §1: the update
+ * W <- R_i W P_i rewritten as linear maps on the input).  R and P are
+ * block-diagonal in a permuted basis (Methodologie §2: permutations as index
+ * maps, two of the four folded into the weight ahead of time; §3: blocks
+ * handled as independent matrices).  Each block B is the Cayley image of a
+ * skew matrix Q, B = (I+Q)(I-Q)^-1 ("POET-X：基于正交变换缩放的内存高效LLM训练方法",
+ * ai-stack.site, 实践 2), or its truncated Neumann form (Methodologie §4);
+ * only the strict upper triangle of Q is stored (Methodologie §4).
+ *
+ * Conventions fixed by this library (the pages leave them open):
+ *   - Activations are row-major: X is T x n, Y is T x m, Y = X W^T.
+ *   - A permutation is an int32 array pi with (Pi x)_j = x_{pi(j)}.
+ *     R = Pi_R^T blockdiag(B_R) Pi_R and P = Pi_P^T blockdiag(B_P) Pi_P.
+ *   - pi is splitmix64(seed) driving a Fisher-Yates shuffle (i from d-1 down
+ *     to 1, j uniform in [0, i] by rejection of the top partial bucket).
+ *   - Blocks are contiguous in the permuted basis; if b does not divide d the
+ *     last block has size d mod b and its own generator.
+ *   - Packed generator: blocks concatenated; in a block of size s entry
+ *     (i, j), i < j, sits at i*s - i*(i+1)/2 + (j-i-1); Q = U - U^T.
+ *   - Neumann mode of order k: B = (I+Q)(I + Q + ... + Q^k).
+ *   - W0' = Pi_R W0 Pi_P^T (W0'[i][j] = W0[pi_R(i)][pi_P(j)]) is the weight
+ *     the forward and backward passes consume.
+ *
+ * Memory.  Every pointer argument is DEVICE memory owned by the caller
+ * unless its comment says HOST.  The library allocates no device memory on
+ * any path; per-call scratch comes from the caller's `workspace`, sized by
+ * the matching *_workspace_size function, 256-byte aligned.  Layer state
+ * (block matrices, permutations) lives in the caller's `params` buffer of
+ * poetx_params_size() bytes, 256-byte aligned.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ * default stream.  Every call is asynchronous on that stream unless stated;
+ * no call synchronises the host except poetx_device_status and the *_host
+ * entry point.
+ *
+ * Errors.  Argument errors return a status before any launch and leave all
+ * outputs untouched.  A failed launch returns POETX_ERR_CUDA.  Kernels that
+ * wait on a barrier give up after a bounded time, record the fact in a
+ * device status word and return; poetx_device_status() reports it as
+ * POETX_ERR_TIMEOUT.  No function throws across this boundary.
+ *
+ * Precision.  dtype FP32: every step in fp32 on CUDA cores.  dtype BF16:
+ * X, Y, dX, dY, W0' and the saved h are bf16; block matrices are built in
+ * fp32 and rounded to bf16 for the tensor-core contractions, which
+ * accumulate in fp32; generator gradients are reduced and returned in fp32.
+ * Generators are always fp32.
+ */
+#ifndef POETX_H
+#define POETX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum poetx_status {
+  POETX_OK = 0,
+  POETX_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum value      */
+  POETX_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dims % 8)   */
+  POETX_ERR_MISALIGNED = 3,   /* a pointer is not 256-byte (buffers) or
+                                 16-byte (tensors) aligned                    */
+  POETX_ERR_CUDA = 4,         /* a CUDA call or launch failed                */
+  POETX_ERR_TIMEOUT = 5       /* a device-side bounded wait ran out          */
+} poetx_status;
+
+enum { POETX_MODE_CAYLEY = 0, POETX_MODE_NEUMANN = 1 };
+enum { POETX_DTYPE_FP32 = 0, POETX_DTYPE_BF16 = 1 };
+
+/* Geometry and options of one layer.  m, n >= 1; 1 <= b_R <= m and
+ * 1 <= b_P <= n.  BF16 additionally needs m and n multiples of 8 (16-byte
+ * rows for the tensor-memory-accelerator copies) and b_R, b_P in
+ * {32, 64, 128, 256, 512}.  neumann_k >= 1 is read in Neumann mode only.
+ * reserved must be 0. */
+typedef struct poetx_layer_desc {
+  int32_t m, n;
+  int32_t b_R, b_P;
+  uint64_t seed_R, seed_P;
+  int32_t mode;
+  int32_t neumann_k;
+  int32_t dtype;
+  int32_t reserved;
+} poetx_layer_desc;
+
+/* Human-readable name of a status code (static storage). */
+const char* poetx_status_string(int32_t status);
+
+/* Library ABI version (major*1000 + minor). */
+int32_t poetx_version(void);
+
+/* HOST.  Writes the permutation of 0..d-1 generated from `seed` (the
+ * Fisher-Yates/splitmix64 recipe above) into host_out[0..d-1].
+ * Source: Methodologie §2 (permutations realised as index maps).
+ * Errors: INVALID_ARG if d < 1 or host_out is NULL. */
+poetx_status poetx_perm_generate(uint64_t seed, int32_t d, int32_t* host_out);
+
+/* Number of fp32 entries in the packed generator of a d-dimensional side
+ * with block size b (sum over blocks of s(s-1)/2).  Methodologie §4.
+ * Returns -1 on invalid arguments. */
+int64_t poetx_gen_length(int32_t d, int32_t b);
+
+/* Bytes of the params buffer for `desc`; 0 if desc is invalid. */
+size_t poetx_params_size(const poetx_layer_desc* desc);
+
+/* Builds the layer state into `params` (caller-owned device memory of
+ * poetx_params_size bytes, 256-byte aligned): the permutations pi_R, pi_P
+ * and their inverses (generated on the host and copied on `stream`), and
+ * per block B = (I+Q)(I-Q)^-1 (exact Cayley, fp32 Gauss-Jordan) or the
+ * Neumann polynomial, plus the backward's auxiliaries.
+ * genR: device fp32[poetx_gen_length(m, b_R)]; genP: [poetx_gen_length(n, b_P)].
+ * Source: Methodologie §2 and §4; 实践 2.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA. */
+poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR,
+                                const float* genP, void* params, void* stream);
+
+/* Pre-merges the two permutations adjacent to W0 into it:
+ * W0p[i][j] = W0[pi_R(i)][pi_P(j)] (row-major m x n, dtype of desc).
+ * W0 and W0p must not overlap.  params must come from poetx_params_build
+ * with the same desc.  Source: Methodologie §2 (two of the four forward
+ * permutations merged into the weight ahead of time). */
+poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* params,
+                                   const void* W0, void* W0p, void* stream);
+
+/* Scratch bytes that poetx_linear_fwd / poetx_linear_bwd need for T tokens. */
+size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T);
+
+/* Forward, input-centric: Y = R(W0(P x)) for each of the T rows of X,
+ * never forming R W0 P (Methodologie §1, §2, §3):
+ *   u = X[:, pi_P];  v_k = u_k B_P,k^T;  h = v W0'^T;  z_k = h_k B_R,k^T;
+ *   Y[:, pi_R] = z.
+ * X: T x n, Y: T x m (dtype).  saved_h: T x m (dtype) receives h, or NULL
+ * for activation recompute in the backward (Methodologie §5, POET-Xmem).
+ * T = 0 is a no-op.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
+poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params,
+                              const void* W0p, const void* X, int64_t T, void* Y,
+                              void* saved_h, void* workspace, void* stream);
+
+/* Backward of L with upstream gradient dY (T x m):
+ *   dz = dY[:, pi_R];  G_R,k = dz_k^T h_k;  dh_k = dz_k B_R,k;
+ *   dv = dh W0';       G_P,k = dv_k^T u_k;  du_k = dv_k B_P,k;
+ *   dX[:, pi_P] = du;
+ * then per block the Cayley backward dL/dQ = 2 M^T G M^T with
+ * M = (I-Q)^-1 (or the Neumann chain rule) and the packed gradient
+ * g_ij = dL/dQ[i][j] - dL/dQ[j][i] for i < j.
+ * saved_h: the h written by poetx_linear_fwd, or NULL to recompute v and h
+ * from X.  dX: T x n or NULL to skip it.  dGenR/dGenP: fp32 packed
+ * gradients (lengths as for the generators); accumulate != 0 adds into them.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params,
+                              const void* W0p, const void* X, const void* dY,
+                              const void* saved_h, int64_t T, void* dX, float* dGenR,
+                              float* dGenP, int32_t accumulate, void* workspace,
+                              void* stream);
+
+/* Scratch bytes that poetx_merge needs. */
+size_t poetx_merge_workspace_size(const poetx_layer_desc* desc);
+
+/* Merge (Methodologie §1, W <- R W P): folds the current R and P into the
+ * base weight and re-expresses it under the permutations of
+ * (new_seed_R, new_seed_P): with K = blockdiag(B_R) W0p blockdiag(B_P),
+ * W0p_new[i][j] = K[pi_R^-1(pi'_R(i))][pi_P^-1(pi'_P(j))], accumulated in fp32
+ * and rounded once to dtype.  W0p is updated in place.  The caller then
+ * resets the generators to zero and rebuilds params with the new seeds;
+ * the layer then computes the same map as before the merge.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void* W0p,
+                         uint64_t new_seed_R, uint64_t new_seed_P, void* workspace,
+                         void* stream);
+
+/* One forward+backward step from HOST buffers: copies X_host (T x n) and
+ * dY_host (T x m) into the device buffers X_dev / dY_dev, runs
+ * poetx_linear_fwd (into Y_dev, saved_h_dev) and poetx_linear_bwd (into
+ * dX_dev, dGenR_dev, dGenP_dev, overwriting), and copies the generator
+ * gradients back into dGenR_host / dGenP_host.  Host buffers should be
+ * pinned for asynchronous copies.  Synchronises `stream` before returning.
+ * saved_h_dev may be NULL (recompute). */
+poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params,
+                                    const void* W0p, const void* X_host,
+                                    const void* dY_host, int64_t T, void* X_dev,
+                                    void* dY_dev, void* Y_dev, void* saved_h_dev,
+                                    void* dX_dev, float* dGenR_dev, float* dGenP_dev,
+                                    float* dGenR_host, float* dGenP_host,
+                                    void* workspace, void* stream);
+
+/* Reads (and with reset != 0 clears) the device status word that bounded
+ * waits write.  Synchronises the device.  Returns POETX_OK, POETX_ERR_TIMEOUT
+ * if any kernel gave up on a wait since the last reset, or POETX_ERR_CUDA. */
+poetx_status poetx_device_status(int32_t reset);
+
+/* Self-test of the bounded-wait machinery: launches one kernel that waits
+ * on a shared-memory barrier nothing will ever complete, with a deadline of
+ * timeout_ns nanoseconds (1 us .. 10 s); the kernel must record the timeout
+ * and return.  Returns the kernel's status (POETX_ERR_TIMEOUT when the
+ * machinery works).  Synchronises `stream`. */
+poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/* Sets the deadline (nanoseconds) of every bounded device wait in later
+ * launches; 0 restores the default (2 s). */
+void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POETX_H */

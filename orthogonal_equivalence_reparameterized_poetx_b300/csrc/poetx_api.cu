@@ -1,0 +1,1103 @@
+// C ABI of the POET-X layer (declared in include/poetx.h): argument checks,
+// buffer layouts, host-side permutation generation, and the launch sequence
+// of the forward, backward, build and merge passes.
+//
+// Passages followed ("POET-X: Memory-efficient LLM Training by Scaling
+// Orthogonal Transformation", gist.science summary, Methodologie):
+//   §1 input-centric evaluation: Y = R(W0(P x)) as maps on the input;
+//   §2 permutations as index maps, two of four merged into the weight;
+//   §3 block-diagonal factors as independent small matrices;
+//   §4 Cayley-Neumann parameterisation from packed upper triangles;
+//   §5 gradient checkpointing (recompute v and h in the backward).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "poetx.h"
+#include "ptx.cuh"
+#include "simt.cuh"
+#include "tc_gemm.cuh"
+
+using namespace poetx;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+uint64_t g_timeout_ns = kDefaultTimeoutNs;
+
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ permutations
+// splitmix64 (Steele, Lea & Flood, OOPSLA 2014) drives a Fisher-Yates shuffle;
+// a draw in [0, bound) rejects values at or above the largest multiple of
+// bound representable in 2^64 and reduces the rest modulo bound.
+struct SplitMix64 {
+  uint64_t state;
+  uint64_t next() {
+    state += 0x9E3779B97F4A7C15ull;
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  }
+};
+
+uint64_t draw_below(SplitMix64& g, uint64_t bound) {
+  // 2^64 mod bound, computed without 128-bit arithmetic
+  const uint64_t rem = (0 - bound) % bound;           // (2^64 - bound) mod bound
+  const uint64_t limit = 0 - rem;                      // 2^64 - rem (wraps to 0 if rem == 0)
+  for (;;) {
+    const uint64_t r = g.next();
+    if (rem == 0 || r < limit) return r % bound;
+  }
+}
+
+void make_permutation(uint64_t seed, int d, int32_t* out) {
+  for (int i = 0; i < d; ++i) out[i] = i;
+  SplitMix64 g{seed};
+  for (int i = d - 1; i >= 1; --i) {
+    const int j = static_cast<int>(draw_below(g, static_cast<uint64_t>(i) + 1));
+    std::swap(out[i], out[j]);
+  }
+}
+
+// ------------------------------------------------------------------ layouts
+
+struct SideLayout {
+  SideGeom g;
+  int sb, nsb;          // tensor-core super-block size and count
+  size_t off_B, off_M, off_Q;
+  size_t off_Bsb, off_BsbT;
+  size_t off_s1, off_s2, off_s3;  // build scratch
+  size_t bb() const { return static_cast<size_t>(g.b) * g.b; }
+};
+
+struct ParamsLayout {
+  size_t off_piR, off_piRinv, off_piP, off_piPinv;
+  SideLayout R, P;
+  size_t total;
+};
+
+SideGeom side_geom(int d, int b) {
+  SideGeom s;
+  s.d = d;
+  s.b = b;
+  s.nblk = (d + b - 1) / b;
+  s.last = d - (s.nblk - 1) * b;
+  return s;
+}
+
+void layout_side(SideLayout& L, int d, int b, const poetx_layer_desc& desc, size_t& off) {
+  L.g = side_geom(d, b);
+  L.sb = std::max(b, 128);
+  L.nsb = (d + L.sb - 1) / L.sb;
+  const size_t mat = static_cast<size_t>(L.g.nblk) * b * b * sizeof(float);
+  L.off_B = off; off = align_up(off + mat);
+  L.off_M = off; off = align_up(off + mat);
+  L.off_Q = off; off = align_up(off + mat);
+  if (desc.dtype == POETX_DTYPE_BF16) {
+    const size_t sbm = static_cast<size_t>(L.nsb) * L.sb * L.sb * sizeof(__nv_bfloat16);
+    L.off_Bsb = off; off = align_up(off + sbm);
+    L.off_BsbT = off; off = align_up(off + sbm);
+  } else {
+    L.off_Bsb = L.off_BsbT = 0;
+  }
+  // scratch: exact b > 128 needs column panel (b x 128), pivot inverse
+  // (128 x 128) and row panel (128 x b) per block; Neumann needs two b x b.
+  size_t s1 = 0, s2 = 0, s3 = 0;
+  if (desc.mode == POETX_MODE_NEUMANN) {
+    s1 = s2 = mat;
+  } else if (b > 128) {
+    s1 = static_cast<size_t>(L.g.nblk) * b * 128 * sizeof(float);
+    s2 = static_cast<size_t>(L.g.nblk) * 128 * 128 * sizeof(float);
+    s3 = s1;
+  }
+  L.off_s1 = off; off = align_up(off + s1);
+  L.off_s2 = off; off = align_up(off + s2);
+  L.off_s3 = off; off = align_up(off + s3);
+}
+
+ParamsLayout params_layout(const poetx_layer_desc& d) {
+  ParamsLayout L{};
+  size_t off = 0;
+  L.off_piR = off; off = align_up(off + sizeof(int32_t) * d.m);
+  L.off_piRinv = off; off = align_up(off + sizeof(int32_t) * d.m);
+  L.off_piP = off; off = align_up(off + sizeof(int32_t) * d.n);
+  L.off_piPinv = off; off = align_up(off + sizeof(int32_t) * d.n);
+  layout_side(L.R, d.m, d.b_R, d, off);
+  layout_side(L.P, d.n, d.b_P, d, off);
+  L.total = off;
+  return L;
+}
+
+// GradRed token splits: about four waves of tiles over the SMs, each split a
+// multiple of 64 tokens; the split count is recomputed from the rounded chunk
+// so that every split holds at least one token.
+struct Splits {
+  int splits, chunk;
+};
+
+Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
+  const int tps = S.sb / 128;
+  const int per_split = S.nsb * tps * tps;
+  const int64_t Tc = std::max<int64_t>(T, 1);
+  int64_t target = (4 * nsm + per_split - 1) / per_split;
+  target = std::max<int64_t>(1, std::min<int64_t>(target, (Tc + 63) / 64));
+  const int64_t per = (Tc + target - 1) / target;
+  const int64_t chunk = (per + 63) / 64 * 64;
+  const int64_t splits = (Tc + chunk - 1) / chunk;
+  return Splits{static_cast<int>(splits), static_cast<int>(chunk)};
+}
+
+struct WorkLayout {
+  size_t off_n1, off_n2, off_m1, off_m2, off_m3;
+  size_t off_partR, off_partP, off_GR, off_GP, off_t1, off_t2, off_nsc;
+  int splitsR, splitsP;
+  size_t total;
+};
+
+int device_sm_count() {
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      nsm = 148;
+  }
+  return nsm;
+}
+
+WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t T, int nsm) {
+  WorkLayout W{};
+  const size_t e = d.dtype == POETX_DTYPE_BF16 ? 2 : 4;
+  const size_t tn = static_cast<size_t>(T) * d.n * e, tm = static_cast<size_t>(T) * d.m * e;
+  size_t off = 0;
+  W.off_n1 = off; off = align_up(off + tn);
+  W.off_n2 = off; off = align_up(off + tn);
+  W.off_m1 = off; off = align_up(off + tm);
+  W.off_m2 = off; off = align_up(off + tm);
+  W.off_m3 = off; off = align_up(off + tm);
+  W.splitsR = W.splitsP = 0;
+  if (d.dtype == POETX_DTYPE_BF16) {
+    W.splitsR = gradred_splits(P.R, T, nsm).splits;
+    W.splitsP = gradred_splits(P.P, T, nsm).splits;
+    W.off_partR = off;
+    off = align_up(off + static_cast<size_t>(W.splitsR) * P.R.nsb * P.R.sb * P.R.sb * 4);
+    W.off_partP = off;
+    off = align_up(off + static_cast<size_t>(W.splitsP) * P.P.nsb * P.P.sb * P.P.sb * 4);
+  } else {
+    W.off_partR = W.off_partP = off;
+  }
+  const size_t gR = static_cast<size_t>(P.R.g.nblk) * P.R.bb() * 4;
+  const size_t gP = static_cast<size_t>(P.P.g.nblk) * P.P.bb() * 4;
+  const size_t gmax = std::max(gR, gP);
+  W.off_GR = off; off = align_up(off + gR);
+  W.off_GP = off; off = align_up(off + gP);
+  W.off_t1 = off; off = align_up(off + gmax);
+  W.off_t2 = off; off = align_up(off + gmax);
+  W.off_nsc = off;
+  if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * (d.neumann_k + 3));
+  W.total = off;
+  return W;
+}
+
+// ------------------------------------------------------------------ checks
+
+poetx_status check_desc(const poetx_layer_desc* d) {
+  if (!d) return POETX_ERR_INVALID_ARG;
+  if (d->m < 1 || d->n < 1 || d->b_R < 1 || d->b_P < 1 || d->b_R > d->m || d->b_P > d->n)
+    return POETX_ERR_INVALID_ARG;
+  if (d->mode != POETX_MODE_CAYLEY && d->mode != POETX_MODE_NEUMANN) return POETX_ERR_INVALID_ARG;
+  if (d->mode == POETX_MODE_NEUMANN && (d->neumann_k < 1 || d->neumann_k > 6))
+    return POETX_ERR_INVALID_ARG;
+  if (d->dtype != POETX_DTYPE_FP32 && d->dtype != POETX_DTYPE_BF16) return POETX_ERR_INVALID_ARG;
+  if (d->reserved != 0) return POETX_ERR_INVALID_ARG;
+  auto b_ok_fp32 = [](int b) { return b <= 128 || (b % 128 == 0 && b <= 1024); };
+  auto b_ok_bf16 = [](int b) { return b == 32 || b == 64 || b == 128 || b == 256 || b == 512; };
+  if (d->dtype == POETX_DTYPE_FP32) {
+    if (!b_ok_fp32(d->b_R) || !b_ok_fp32(d->b_P)) return POETX_ERR_UNSUPPORTED;
+  } else {
+    if (d->m % 8 || d->n % 8) return POETX_ERR_UNSUPPORTED;
+    if (!b_ok_bf16(d->b_R) || !b_ok_bf16(d->b_P)) return POETX_ERR_UNSUPPORTED;
+  }
+  return POETX_OK;
+}
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+#define POETX_CUDA(...)                          \
+  do {                                           \
+    if ((__VA_ARGS__) != cudaSuccess) {          \
+      (void)cudaGetLastError();                  \
+      return POETX_ERR_CUDA;                     \
+    }                                            \
+  } while (0)
+
+#define POETX_LAUNCHED()                         \
+  do {                                           \
+    if (cudaGetLastError() != cudaSuccess) return POETX_ERR_CUDA; \
+  } while (0)
+
+#define POETX_TRY(...)                           \
+  do {                                           \
+    poetx_status _s = (__VA_ARGS__);             \
+    if (_s != POETX_OK) return _s;               \
+  } while (0)
+
+// ------------------------------------------------------------------ launch helpers
+
+int grid_for(int64_t work, int per_block = 256, int max_blocks = 148 * 16) {
+  const int64_t g = (work + per_block - 1) / per_block;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, max_blocks)));
+}
+
+template <typename TA, typename TB, typename TC>
+poetx_status simt_gemm(cudaStream_t st, int M, int N, int K, int batch, const TA* A, int64_t sAm,
+                       int64_t sAk, int64_t bsA, const TB* B, int64_t sBk, int64_t sBn, int64_t bsB,
+                       TC* C, int64_t sCm, int64_t sCn, int64_t bsC, float alpha, float beta) {
+  if (M <= 0 || N <= 0 || batch <= 0) return POETX_OK;
+  SimtGemmArgs g{M, N, K, batch, A, sAm, sAk, bsA, B, sBk, sBn, bsB, C, sCm, sCn, bsC, alpha, beta};
+  dim3 grid((N + 63) / 64, (M + 63) / 64, batch);
+  simt_gemm_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+template <typename T>
+poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* idx, int64_t rows,
+                         int d) {
+  if (rows <= 0) return POETX_OK;
+  const size_t smem = static_cast<size_t>(d) * sizeof(T);
+  if (smem > 48 * 1024) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(gather_cols_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           200 * 1024);
+    });
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(rows, device_sm_count() * 8));
+  gather_cols_kernel<T><<<grid, 256, smem, st>>>(in, out, idx, rows, d);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled get_encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] with leading dimension ld (elements);
+// box = box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
+poetx_status tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t ld, uint32_t box_rows) {
+  PFN_encodeTiled enc = get_encode_fn();
+  if (!enc) return POETX_ERR_CUDA;
+  if (!aligned(base, 16) || (ld * 2) % 16 != 0) return POETX_ERR_MISALIGNED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? POETX_OK : POETX_ERR_CUDA;
+}
+
+template <int BN, bool A_MN, bool B_MN, TileMode MODE, typename OutT>
+poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
+                       TcGemmArgs args) {
+  if (args.num_tiles <= 0) return POETX_OK;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, MODE, OutT>;
+  constexpr int smem = TcGemmCfg<BN>::SMEM_BYTES;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  args.timeout_ns = g_timeout_ns;
+  const int grid = std::min(args.num_tiles, device_sm_count());
+  kern<<<grid, 192, smem, st>>>(ta, tb, args);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+// h (T x N) = A (T x K) * W^T, W row-major N x K (both K-major).
+poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
+                         int K) {
+  if (T <= 0) return POETX_OK;
+  const bool wide = N >= 1024;
+  const int BN = wide ? 256 : 128;
+  CUtensorMap ta, tb;
+  POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
+  POETX_TRY(tmap_bf16(&tb, W, N, K, K, BN));
+  TcGemmArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.C = C;
+  a.ldc = N;
+  a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
+  if (wide) return launch_tc<256, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+  return launch_tc<128, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+}
+
+// dv (T x N) = A (T x K) * W, W row-major K x N (B operand MN-major).
+poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
+                         int K) {
+  if (T <= 0) return POETX_OK;
+  const bool wide = N >= 1024;
+  const int BN = wide ? 256 : 128;
+  CUtensorMap ta, tb;
+  POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
+  POETX_TRY(tmap_bf16(&tb, W, K, N, N, 64));
+  TcGemmArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.C = C;
+  a.ldc = N;
+  a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
+  if (wide) return launch_tc<256, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+  return launch_tc<128, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+}
+
+// out[:, s] = in[:, s] * S_s^T over super-blocks: in/out T x d, Ssb (nsb*sb) x sb.
+poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void* out, int64_t T,
+                          int d, int sb, int nsb) {
+  if (T <= 0) return POETX_OK;
+  const int BN = sb >= 256 ? 256 : 128;
+  CUtensorMap ta, tb;
+  POETX_TRY(tmap_bf16(&ta, in, T, d, d, 128));
+  POETX_TRY(tmap_bf16(&tb, Ssb, static_cast<uint64_t>(nsb) * sb, sb, sb, BN));
+  TcGemmArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = d;
+  a.sb = sb;
+  a.C = out;
+  a.ldc = d;
+  a.num_tiles = static_cast<int>((T + 127) / 128) * ((d + BN - 1) / BN);
+  if (BN == 256) return launch_tc<256, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, a);
+  return launch_tc<128, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, a);
+}
+
+// partial[p][s] = sum_{t in split p} A[t, s]^T B[t, s] (fp32, sb x sb per super-block).
+poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, const void* B,
+                        float* partial, int64_t T, int expected_splits) {
+  const Splits sp = gradred_splits(S, T, device_sm_count());
+  if (sp.splits != expected_splits) return POETX_ERR_INVALID_ARG;
+  const int d = S.g.d, sb = S.sb, nsb = S.nsb;
+  CUtensorMap ta, tb;
+  POETX_TRY(tmap_bf16(&ta, A, T, d, d, 64));
+  POETX_TRY(tmap_bf16(&tb, B, T, d, d, 64));
+  TcGemmArgs a{};
+  a.sb = sb;
+  a.nsb = nsb;
+  a.tokens = static_cast<int>(T);
+  a.chunk = sp.chunk;
+  a.C = partial;
+  a.split_stride = static_cast<int64_t>(nsb) * sb * sb;
+  const int tps = sb / 128;
+  a.num_tiles = sp.splits * nsb * tps * tps;
+  return launch_tc<128, true, true, TileMode::GradRed, float>(st, ta, tb, a);
+}
+
+// ------------------------------------------------------------------ builder
+
+poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
+                        const float* gen, uint8_t* params) {
+  float* B = reinterpret_cast<float*>(params + S.off_B);
+  float* M = reinterpret_cast<float*>(params + S.off_M);
+  float* Q = reinterpret_cast<float*>(params + S.off_Q);
+  const int b = S.g.b, nb = S.g.nblk;
+  const int64_t bb = static_cast<int64_t>(b) * b;
+  unpack_kernel<<<nb, 256, 0, st>>>(gen, S.g, Q, M);
+  POETX_LAUNCHED();
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(gj_invert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         128 * 128 * 4 + 2 * 128 * 4);
+  });
+  if (d.mode == POETX_MODE_CAYLEY) {
+    if (b <= 128) {
+      const size_t smem = static_cast<size_t>(b) * b * 4 + 2 * b * 4;
+      gj_invert_kernel<<<nb, 1024, smem, st>>>(M, bb, b, M, bb, b, b);
+      POETX_LAUNCHED();
+    } else {
+      // Block Gauss-Jordan with 128-wide panels: for panel k,
+      // C = A[:, k], D = A_kk^-1, R = D A[k, :], A -= C R, A[k, :] = R,
+      // A[:, k] = -C D, A_kk = D.
+      float* Cc = reinterpret_cast<float*>(params + S.off_s1);
+      float* D = reinterpret_cast<float*>(params + S.off_s2);
+      float* Rr = reinterpret_cast<float*>(params + S.off_s3);
+      const int P = 128;
+      const size_t smem = static_cast<size_t>(P) * P * 4 + 2 * P * 4;
+      for (int k = 0; k < b / P; ++k) {
+        const int o = k * P;
+        copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(b) * P), nb), 256, 0, st>>>(
+            M + o, bb, b, Cc, static_cast<int64_t>(b) * P, P, b, P, 1.f, 0.f);
+        POETX_LAUNCHED();
+        gj_invert_kernel<<<nb, 1024, smem, st>>>(M + static_cast<int64_t>(o) * b + o, bb, b, D,
+                                                 static_cast<int64_t>(P) * P, P, P);
+        POETX_LAUNCHED();
+        POETX_TRY(simt_gemm<float, float, float>(st, P, b, P, nb, D, P, 1, static_cast<int64_t>(P) * P,
+                                                 M + static_cast<int64_t>(o) * b, b, 1, bb, Rr, b, 1,
+                                                 static_cast<int64_t>(P) * b, 1.f, 0.f));
+        POETX_TRY(simt_gemm<float, float, float>(st, b, b, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
+                                                 Rr, b, 1, static_cast<int64_t>(P) * b, M, b, 1, bb,
+                                                 -1.f, 1.f));
+        copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(b) * P), nb), 256, 0, st>>>(
+            Rr, static_cast<int64_t>(P) * b, b, M + static_cast<int64_t>(o) * b, bb, b, P, b, 1.f, 0.f);
+        POETX_LAUNCHED();
+        POETX_TRY(simt_gemm<float, float, float>(st, b, P, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
+                                                 D, P, 1, static_cast<int64_t>(P) * P, M + o, b, 1, bb,
+                                                 -1.f, 0.f));
+        copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(P) * P), nb), 256, 0, st>>>(
+            D, static_cast<int64_t>(P) * P, P, M + static_cast<int64_t>(o) * b + o, bb, b, P, P, 1.f,
+            0.f);
+        POETX_LAUNCHED();
+      }
+    }
+    // B = 2M - I
+    copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(M, bb, b, B, bb, b, b, b, 2.f, -1.f);
+    POETX_LAUNCHED();
+  } else {
+    // Neumann: S_0 = I, S_i = I + Q S_{i-1} (i = 1..k), B = S_k + Q S_k.
+    float* Sa = reinterpret_cast<float*>(params + S.off_s1);
+    float* Sb = reinterpret_cast<float*>(params + S.off_s2);
+    copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(Q, bb, b, Sa, bb, b, b, b, 0.f, 1.f);
+    POETX_LAUNCHED();
+    for (int i = 1; i <= d.neumann_k; ++i) {
+      copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(Q, bb, b, Sb, bb, b, b, b, 0.f, 1.f);
+      POETX_LAUNCHED();
+      POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, Sb, b, 1,
+                                               bb, 1.f, 1.f));
+      std::swap(Sa, Sb);
+    }
+    copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(Sa, bb, b, B, bb, b, b, b, 1.f, 0.f);
+    POETX_LAUNCHED();
+    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, B, b, 1, bb,
+                                             1.f, 1.f));
+  }
+  if (d.dtype == POETX_DTYPE_BF16) {
+    auto* Bsb = reinterpret_cast<__nv_bfloat16*>(params + S.off_Bsb);
+    auto* BsbT = reinterpret_cast<__nv_bfloat16*>(params + S.off_BsbT);
+    superblock_kernel<<<grid_for(static_cast<int64_t>(S.nsb) * S.sb * S.sb), 256, 0, st>>>(
+        B, S.g, S.sb, S.nsb, Bsb, BsbT);
+    POETX_LAUNCHED();
+  }
+  return POETX_OK;
+}
+
+// dL/dQ from dL/dB per block (fp32), then packed into dGen.
+poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
+                                const uint8_t* params, const float* G, float* t1, float* t2,
+                                float* nsc, float* dGen, int accumulate) {
+  const int b = S.g.b, nb = S.g.nblk;
+  const int64_t bb = static_cast<int64_t>(b) * b;
+  const float* M = reinterpret_cast<const float*>(params + S.off_M);
+  const float* Q = reinterpret_cast<const float*>(params + S.off_Q);
+  float* GQ = t2;
+  if (d.mode == POETX_MODE_CAYLEY) {
+    // dL/dQ = 2 M^T G M^T
+    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, M, 1, b, bb, G, b, 1, bb, t1, b, 1, bb,
+                                             1.f, 0.f));
+    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, t1, b, 1, bb, M, 1, b, bb, GQ, b, 1,
+                                             bb, 2.f, 0.f));
+  } else {
+    // B = sum_p c_p Q^p (c_0 = 1, c_1..c_k = 2, c_{k+1} = 1), so
+    // dL/dQ = sum_{a+c <= k} c_{a+c+1} Qt^a G Qt^c with Qt = Q^T.
+    // R_c = G Qt^c; T_a = sum_c c_{a+c+1} R_c; dL/dQ = T_0 + Qt(T_1 + Qt(... T_k)).
+    const int k = d.neumann_k;
+    const int64_t tstride = static_cast<int64_t>(nb) * bb;
+    float* R = nsc;                          // R_0 .. R_k
+    float* cur = nsc + (k + 1) * tstride;    // Horner accumulator
+    float* nxt = t1;
+    copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(G, bb, b, R, bb, b, b, b, 1.f, 0.f);
+    POETX_LAUNCHED();
+    for (int c = 1; c <= k; ++c)  // R_c = R_{c-1} Qt
+      POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, R + (c - 1) * tstride, b, 1, bb, Q,
+                                               1, b, bb, R + c * tstride, b, 1, bb, 1.f, 0.f));
+    auto coef = [&](int p) { return (p == 0 || p == k + 1) ? 1.f : 2.f; };
+    for (int a = k; a >= 0; --a) {
+      float* dst = (a == k) ? cur : nxt;  // T_a
+      copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(R, bb, b, dst, bb, b, b, b,
+                                                            coef(a + 1), 0.f);
+      POETX_LAUNCHED();
+      for (int c = 1; c <= k - a; ++c) {
+        axpy_kernel<<<grid_for(tstride), 256, 0, st>>>(dst, R + c * tstride, coef(a + c + 1), tstride);
+        POETX_LAUNCHED();
+      }
+      if (a != k) {  // nxt = T_a + Qt cur
+        POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, 1, b, bb, cur, b, 1, bb, nxt, b,
+                                                 1, bb, 1.f, 1.f));
+        std::swap(cur, nxt);
+      }
+    }
+    GQ = cur;
+  }
+  pack_grad_kernel<<<nb, 256, 0, st>>>(GQ, S.g, dGen, accumulate);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// ------------------------------------------------------------------ pinned staging
+// Host-generated permutations reach the device through a small ring of
+// pinned host slots, so the copies stay asynchronous.  A slot is reused only
+// after the copy that last read it has executed (an event wait that only
+// blocks if the ring wraps before the stream reaches that copy).
+struct PinnedRing {
+  std::mutex mu;
+  uint8_t* buf = nullptr;
+  size_t slot_bytes = 0;
+  static constexpr int kSlots = 8;
+  cudaEvent_t ev[kSlots] = {};
+  bool pending[kSlots] = {};
+  int next = 0;
+};
+PinnedRing g_ring;
+
+poetx_status ring_upload(cudaStream_t st, const std::vector<std::pair<const int32_t*, size_t>>& parts,
+                         const std::vector<void*>& dsts) {
+  std::lock_guard<std::mutex> lock(g_ring.mu);
+  size_t need = 0;
+  for (auto& p : parts) need += align_up(p.second * sizeof(int32_t), 16);
+  if (need > g_ring.slot_bytes) {
+    for (int s = 0; s < PinnedRing::kSlots; ++s)
+      if (g_ring.pending[s]) POETX_CUDA(cudaEventSynchronize(g_ring.ev[s]));
+    if (g_ring.buf) POETX_CUDA(cudaFreeHost(g_ring.buf));
+    g_ring.buf = nullptr;
+    const size_t slot = align_up(std::max<size_t>(need, 1 << 16), 4096);
+    POETX_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&g_ring.buf), slot * PinnedRing::kSlots,
+                             cudaHostAllocDefault));
+    g_ring.slot_bytes = slot;
+    for (int s = 0; s < PinnedRing::kSlots; ++s) {
+      if (!g_ring.ev[s]) POETX_CUDA(cudaEventCreateWithFlags(&g_ring.ev[s], cudaEventDisableTiming));
+      g_ring.pending[s] = false;
+    }
+  }
+  const int s = g_ring.next;
+  g_ring.next = (s + 1) % PinnedRing::kSlots;
+  if (g_ring.pending[s]) POETX_CUDA(cudaEventSynchronize(g_ring.ev[s]));
+  uint8_t* base = g_ring.buf + static_cast<size_t>(s) * g_ring.slot_bytes;
+  size_t off = 0;
+  for (size_t i = 0; i < parts.size(); ++i) {
+    const size_t bytes = parts[i].second * sizeof(int32_t);
+    std::memcpy(base + off, parts[i].first, bytes);
+    POETX_CUDA(cudaMemcpyAsync(dsts[i], base + off, bytes, cudaMemcpyHostToDevice, st));
+    off += align_up(bytes, 16);
+  }
+  POETX_CUDA(cudaEventRecord(g_ring.ev[s], st));
+  g_ring.pending[s] = true;
+  return POETX_OK;
+}
+
+void perm_and_inverse(uint64_t seed, int d, std::vector<int32_t>& p, std::vector<int32_t>& inv) {
+  p.resize(d);
+  inv.resize(d);
+  make_permutation(seed, d, p.data());
+  for (int i = 0; i < d; ++i) inv[p[i]] = i;
+}
+
+// ------------------------------------------------------------------ fp32 path helpers
+
+// out[:, blk] = in[:, blk] * B_blk^T (transpose) or * B_blk, per block, T rows,
+// leading dimension ld; the ragged last block uses its top-left corner.
+template <typename TI, typename TO>
+poetx_status simt_blocks(cudaStream_t st, const SideLayout& S, const uint8_t* params, const TI* in,
+                         TO* out, int64_t T, int64_t ld, bool transpose) {
+  const float* B = reinterpret_cast<const float*>(params + S.off_B);
+  const int b = S.g.b;
+  const int64_t bb = static_cast<int64_t>(b) * b;
+  const int full = S.g.nblk - (S.g.last < b ? 1 : 0);
+  const int64_t sBk = transpose ? 1 : b, sBn = transpose ? b : 1;
+  POETX_TRY(simt_gemm<TI, float, TO>(st, static_cast<int>(T), b, b, full, in, ld, 1, b, B, sBk, sBn,
+                                     bb, out, ld, 1, b, 1.f, 0.f));
+  if (S.g.last < b) {
+    const int64_t o = static_cast<int64_t>(full) * b;
+    POETX_TRY(simt_gemm<TI, float, TO>(st, static_cast<int>(T), S.g.last, S.g.last, 1, in + o, ld, 1,
+                                       0, B + full * bb, sBk, sBn, 0, out + o, ld, 1, 0, 1.f, 0.f));
+  }
+  return POETX_OK;
+}
+
+// G[k] = A[:, blk]^T Bm[:, blk] (b x b per block, fp32), contraction over T.
+poetx_status simt_gradblocks(cudaStream_t st, const SideLayout& S, const float* A, const float* Bm,
+                             float* G, int64_t T, int64_t ld) {
+  const int b = S.g.b;
+  const int64_t bb = static_cast<int64_t>(b) * b;
+  POETX_CUDA(cudaMemsetAsync(G, 0, static_cast<size_t>(S.g.nblk) * bb * 4, st));
+  const int full = S.g.nblk - (S.g.last < b ? 1 : 0);
+  POETX_TRY(simt_gemm<float, float, float>(st, b, b, static_cast<int>(T), full, A, 1, ld, b, Bm, ld, 1,
+                                           b, G, b, 1, bb, 1.f, 0.f));
+  if (S.g.last < b) {
+    const int64_t o = static_cast<int64_t>(full) * b;
+    POETX_TRY(simt_gemm<float, float, float>(st, S.g.last, S.g.last, static_cast<int>(T), 1, A + o, 1,
+                                             ld, 0, Bm + o, ld, 1, 0, G + full * bb, b, 1, 0, 1.f,
+                                             0.f));
+  }
+  return POETX_OK;
+}
+
+struct Ctx {
+  const poetx_layer_desc& d;
+  ParamsLayout L;
+  WorkLayout W;
+  const uint8_t* params;
+  uint8_t* ws;
+  cudaStream_t st;
+  const int32_t* piR() const { return reinterpret_cast<const int32_t*>(params + L.off_piR); }
+  const int32_t* piRinv() const { return reinterpret_cast<const int32_t*>(params + L.off_piRinv); }
+  const int32_t* piP() const { return reinterpret_cast<const int32_t*>(params + L.off_piP); }
+  const int32_t* piPinv() const { return reinterpret_cast<const int32_t*>(params + L.off_piPinv); }
+  template <typename T> T* w(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+  template <typename T> const T* p(size_t off) const { return reinterpret_cast<const T*>(params + off); }
+};
+
+poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs) {
+  const int m = c.d.m, n = c.d.n;
+  float* u = c.w<float>(c.W.off_n1);
+  float* v = c.w<float>(c.W.off_n2);
+  float* h = hs ? hs : c.w<float>(c.W.off_m1);
+  float* z = c.w<float>(c.W.off_m2);
+  POETX_TRY(gather_cols<float>(c.st, X, u, c.piP(), T, n));
+  POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
+  POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1, n, 0,
+                                           h, m, 1, 0, 1.f, 0.f));
+  POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, h, z, T, m, true));
+  POETX_TRY(gather_cols<float>(c.st, z, Y, c.piRinv(), T, m));
+  return POETX_OK;
+}
+
+poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X, int64_t T,
+                      __nv_bfloat16* Y, __nv_bfloat16* hs) {
+  const int m = c.d.m, n = c.d.n;
+  auto* u = c.w<__nv_bfloat16>(c.W.off_n1);
+  auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
+  auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
+  auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
+  const SideLayout &R = c.L.R, &P = c.L.P;
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
+  POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
+  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
+  POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, z, Y, c.piRinv(), T, m));
+  return POETX_OK;
+}
+
+poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accumulate) {
+  float* GR = c.w<float>(c.W.off_GR);
+  float* GP = c.w<float>(c.W.off_GP);
+  float* t1 = c.w<float>(c.W.off_t1);
+  float* t2 = c.w<float>(c.W.off_t2);
+  float* nsc = c.w<float>(c.W.off_nsc);
+  if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0)
+    POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
+  if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0)
+    POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
+  return POETX_OK;
+}
+
+poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const float* dY,
+                      const float* hs, int64_t T, float* dX) {
+  const int m = c.d.m, n = c.d.n;
+  float* u = c.w<float>(c.W.off_n1);
+  float* v = c.w<float>(c.W.off_n2);
+  float* hbuf = c.w<float>(c.W.off_m1);
+  float* dz = c.w<float>(c.W.off_m2);
+  float* dh = c.w<float>(c.W.off_m3);
+  POETX_TRY(gather_cols<float>(c.st, X, u, c.piP(), T, n));
+  const float* h = hs;
+  if (!hs) {
+    POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
+    POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1, n,
+                                             0, hbuf, m, 1, 0, 1.f, 0.f));
+    h = hbuf;
+  }
+  POETX_TRY(gather_cols<float>(c.st, dY, dz, c.piR(), T, m));
+  POETX_TRY(simt_gradblocks(c.st, c.L.R, dz, h, c.w<float>(c.W.off_GR), T, m));
+  POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, dz, dh, T, m, false));
+  float* dv = v;
+  POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), n, m, 1, dh, m, 1, 0, W0p, n, 1, 0,
+                                           dv, n, 1, 0, 1.f, 0.f));
+  POETX_TRY(simt_gradblocks(c.st, c.L.P, dv, u, c.w<float>(c.W.off_GP), T, n));
+  float* du = u;
+  POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, dv, du, T, n, false));
+  if (dX) POETX_TRY(gather_cols<float>(c.st, du, dX, c.piPinv(), T, n));
+  return POETX_OK;
+}
+
+poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X,
+                      const __nv_bfloat16* dY, const __nv_bfloat16* hs, int64_t T,
+                      __nv_bfloat16* dX) {
+  const int m = c.d.m, n = c.d.n;
+  const SideLayout &R = c.L.R, &P = c.L.P;
+  auto* u = c.w<__nv_bfloat16>(c.W.off_n1);
+  auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
+  auto* hbuf = c.w<__nv_bfloat16>(c.W.off_m1);
+  auto* dz = c.w<__nv_bfloat16>(c.W.off_m2);
+  auto* dh = c.w<__nv_bfloat16>(c.W.off_m3);
+  float* partR = c.w<float>(c.W.off_partR);
+  float* partP = c.w<float>(c.W.off_partP);
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
+  const __nv_bfloat16* h = hs;
+  if (!hs) {  // activation recompute (POET-Xmem)
+    POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
+    POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
+    h = hbuf;
+  }
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
+  POETX_TRY(tc_blockdiag(c.st, dz, c.p<__nv_bfloat16>(R.off_BsbT), dh, T, m, R.sb, R.nsb));
+  POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, c.W.splitsR));
+  auto* dv = v;
+  POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
+  POETX_TRY(tc_gradred(c.st, P, dv, u, partP, T, c.W.splitsP));
+  auto* du = u;
+  POETX_TRY(tc_blockdiag(c.st, dv, c.p<__nv_bfloat16>(P.off_BsbT), du, T, n, P.sb, P.nsb));
+  if (dX) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+  gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
+      partR, static_cast<int64_t>(R.nsb) * R.sb * R.sb, c.W.splitsR, R.g, R.sb, c.w<float>(c.W.off_GR));
+  POETX_LAUNCHED();
+  gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0, c.st>>>(
+      partP, static_cast<int64_t>(P.nsb) * P.sb * P.sb, c.W.splitsP, P.g, P.sb, c.w<float>(c.W.off_GP));
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+poetx_status check_tensor(const void* p) {
+  if (!p) return POETX_ERR_INVALID_ARG;
+  if (!aligned(p, 16)) return POETX_ERR_MISALIGNED;
+  return POETX_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* poetx_status_string(int32_t s) {
+  switch (s) {
+    case POETX_OK: return "POETX_OK";
+    case POETX_ERR_INVALID_ARG: return "POETX_ERR_INVALID_ARG";
+    case POETX_ERR_UNSUPPORTED: return "POETX_ERR_UNSUPPORTED";
+    case POETX_ERR_MISALIGNED: return "POETX_ERR_MISALIGNED";
+    case POETX_ERR_CUDA: return "POETX_ERR_CUDA";
+    case POETX_ERR_TIMEOUT: return "POETX_ERR_TIMEOUT";
+    default: return "POETX_ERR_UNKNOWN";
+  }
+}
+
+int32_t poetx_version(void) { return 1000; }
+
+poetx_status poetx_perm_generate(uint64_t seed, int32_t d, int32_t* host_out) {
+  if (d < 1 || !host_out) return POETX_ERR_INVALID_ARG;
+  make_permutation(seed, d, host_out);
+  return POETX_OK;
+}
+
+int64_t poetx_gen_length(int32_t d, int32_t b) {
+  if (d < 1 || b < 1 || b > d) return -1;
+  const SideGeom g = side_geom(d, b);
+  return static_cast<int64_t>(g.nblk - 1) * b * (b - 1) / 2 +
+         static_cast<int64_t>(g.last) * (g.last - 1) / 2;
+}
+
+size_t poetx_params_size(const poetx_layer_desc* d) {
+  if (check_desc(d) != POETX_OK) return 0;
+  return params_layout(*d).total;
+}
+
+poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR, const float* genP,
+                                void* params, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (!params) return POETX_ERR_INVALID_ARG;
+  if ((poetx_gen_length(desc->m, desc->b_R) > 0 && !genR) ||
+      (poetx_gen_length(desc->n, desc->b_P) > 0 && !genP))
+    return POETX_ERR_INVALID_ARG;
+  if (!aligned(params, kAlign)) return POETX_ERR_MISALIGNED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ParamsLayout L = params_layout(*desc);
+  uint8_t* pb = reinterpret_cast<uint8_t*>(params);
+  std::vector<int32_t> piR, piRinv, piP, piPinv;
+  perm_and_inverse(desc->seed_R, desc->m, piR, piRinv);
+  perm_and_inverse(desc->seed_P, desc->n, piP, piPinv);
+  POETX_TRY(ring_upload(st,
+                        {{piR.data(), piR.size()}, {piRinv.data(), piRinv.size()},
+                         {piP.data(), piP.size()}, {piPinv.data(), piPinv.size()}},
+                        {pb + L.off_piR, pb + L.off_piRinv, pb + L.off_piP, pb + L.off_piPinv}));
+  POETX_TRY(build_side(st, *desc, L.R, genR, pb));
+  POETX_TRY(build_side(st, *desc, L.P, genP, pb));
+  return POETX_OK;
+}
+
+poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* params, const void* W0,
+                                   void* W0p, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (!params || !W0 || !W0p || W0 == W0p) return POETX_ERR_INVALID_ARG;
+  if (!aligned(params, kAlign)) return POETX_ERR_MISALIGNED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ParamsLayout L = params_layout(*desc);
+  const uint8_t* pb = reinterpret_cast<const uint8_t*>(params);
+  const int32_t* piR = reinterpret_cast<const int32_t*>(pb + L.off_piR);
+  const int32_t* piP = reinterpret_cast<const int32_t*>(pb + L.off_piP);
+  const int grid = std::min(desc->m, device_sm_count() * 8);
+  if (desc->dtype == POETX_DTYPE_BF16)
+    gather2d_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(W0), reinterpret_cast<__nv_bfloat16*>(W0p), piR, piP,
+        desc->m, desc->n);
+  else
+    gather2d_kernel<float, float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(W0),
+                                                        reinterpret_cast<float*>(W0p), piR, piP,
+                                                        desc->m, desc->n);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T) {
+  if (check_desc(desc) != POETX_OK || T < 0) return 0;
+  return work_layout(*desc, params_layout(*desc), T, device_sm_count()).total;
+}
+
+poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params, const void* W0p,
+                              const void* X, int64_t T, void* Y, void* saved_h, void* workspace,
+                              void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (T < 0) return POETX_ERR_INVALID_ARG;
+  if (T == 0) return POETX_OK;
+  if (!params || !workspace) return POETX_ERR_INVALID_ARG;
+  POETX_TRY(check_tensor(W0p));
+  POETX_TRY(check_tensor(X));
+  POETX_TRY(check_tensor(Y));
+  if (saved_h) POETX_TRY(check_tensor(saved_h));
+  if (!aligned(params, kAlign) || !aligned(workspace, kAlign)) return POETX_ERR_MISALIGNED;
+  if (T > (int64_t(1) << 31) - 256) return POETX_ERR_UNSUPPORTED;
+  const ParamsLayout L = params_layout(*desc);
+  Ctx c{*desc, L, work_layout(*desc, L, T, device_sm_count()),
+        reinterpret_cast<const uint8_t*>(params), reinterpret_cast<uint8_t*>(workspace),
+        reinterpret_cast<cudaStream_t>(stream)};
+  if (desc->dtype == POETX_DTYPE_FP32)
+    return fwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X), T,
+                    reinterpret_cast<float*>(Y), reinterpret_cast<float*>(saved_h));
+  return fwd_bf16(c, reinterpret_cast<const __nv_bfloat16*>(W0p),
+                  reinterpret_cast<const __nv_bfloat16*>(X), T, reinterpret_cast<__nv_bfloat16*>(Y),
+                  reinterpret_cast<__nv_bfloat16*>(saved_h));
+}
+
+poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params, const void* W0p,
+                              const void* X, const void* dY, const void* saved_h, int64_t T, void* dX,
+                              float* dGenR, float* dGenP, int32_t accumulate, void* workspace,
+                              void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (T < 0) return POETX_ERR_INVALID_ARG;
+  if (!params || !workspace) return POETX_ERR_INVALID_ARG;
+  if ((poetx_gen_length(desc->m, desc->b_R) > 0 && !dGenR) ||
+      (poetx_gen_length(desc->n, desc->b_P) > 0 && !dGenP))
+    return POETX_ERR_INVALID_ARG;
+  if (T == 0) {
+    // No tokens: the generator gradients are zero (with accumulate: unchanged).
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    if (!accumulate) {
+      const int64_t lr = poetx_gen_length(desc->m, desc->b_R);
+      const int64_t lp = poetx_gen_length(desc->n, desc->b_P);
+      if (lr > 0) POETX_CUDA(cudaMemsetAsync(dGenR, 0, lr * 4, st0));
+      if (lp > 0) POETX_CUDA(cudaMemsetAsync(dGenP, 0, lp * 4, st0));
+    }
+    return POETX_OK;
+  }
+  POETX_TRY(check_tensor(W0p));
+  POETX_TRY(check_tensor(X));
+  POETX_TRY(check_tensor(dY));
+  if (saved_h) POETX_TRY(check_tensor(saved_h));
+  if (dX) POETX_TRY(check_tensor(dX));
+  if (!aligned(params, kAlign) || !aligned(workspace, kAlign)) return POETX_ERR_MISALIGNED;
+  if (T > (int64_t(1) << 31) - 256) return POETX_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ParamsLayout L = params_layout(*desc);
+  Ctx c{*desc, L, work_layout(*desc, L, T, device_sm_count()),
+        reinterpret_cast<const uint8_t*>(params), reinterpret_cast<uint8_t*>(workspace), st};
+  if (desc->dtype == POETX_DTYPE_FP32)
+    POETX_TRY(bwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X),
+                       reinterpret_cast<const float*>(dY), reinterpret_cast<const float*>(saved_h), T,
+                       reinterpret_cast<float*>(dX)));
+  else
+    POETX_TRY(bwd_bf16(c, reinterpret_cast<const __nv_bfloat16*>(W0p),
+                       reinterpret_cast<const __nv_bfloat16*>(X),
+                       reinterpret_cast<const __nv_bfloat16*>(dY),
+                       reinterpret_cast<const __nv_bfloat16*>(saved_h), T,
+                       reinterpret_cast<__nv_bfloat16*>(dX)));
+  return bwd_common_tail(c, dGenR, dGenP, accumulate);
+}
+
+size_t poetx_merge_workspace_size(const poetx_layer_desc* desc) {
+  if (check_desc(desc) != POETX_OK) return 0;
+  const size_t mn = static_cast<size_t>(desc->m) * desc->n * 4;
+  return align_up(mn) * 2 + align_up(static_cast<size_t>(desc->m) * 4) +
+         align_up(static_cast<size_t>(desc->n) * 4);
+}
+
+poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void* W0p,
+                         uint64_t new_seed_R, uint64_t new_seed_P, void* workspace, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (!params || !workspace) return POETX_ERR_INVALID_ARG;
+  POETX_TRY(check_tensor(W0p));
+  if (!aligned(params, kAlign) || !aligned(workspace, kAlign)) return POETX_ERR_MISALIGNED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int m = desc->m, n = desc->n;
+  const ParamsLayout L = params_layout(*desc);
+  const uint8_t* pb = reinterpret_cast<const uint8_t*>(params);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const size_t mn = align_up(static_cast<size_t>(m) * n * 4);
+  float* T1 = reinterpret_cast<float*>(ws);
+  float* K = reinterpret_cast<float*>(ws + mn);
+  int32_t* rhoR = reinterpret_cast<int32_t*>(ws + 2 * mn);
+  int32_t* rhoP = reinterpret_cast<int32_t*>(ws + 2 * mn + align_up(static_cast<size_t>(m) * 4));
+  // T1 = W0' blockdiag(B_P): row-local blocks along n (not transposed).
+  if (desc->dtype == POETX_DTYPE_BF16)
+    POETX_TRY(simt_blocks<__nv_bfloat16, float>(st, L.P, pb, reinterpret_cast<const __nv_bfloat16*>(W0p),
+                                                T1, m, n, false));
+  else
+    POETX_TRY(simt_blocks<float, float>(st, L.P, pb, reinterpret_cast<const float*>(W0p), T1, m, n,
+                                        false));
+  // K = blockdiag(B_R) T1: block k of rows is B_R,k (b x b) times T1[rows of k, :].
+  {
+    const SideLayout& S = L.R;
+    const int b = S.g.b;
+    const int64_t bb = static_cast<int64_t>(b) * b;
+    const float* BR = reinterpret_cast<const float*>(pb + S.off_B);
+    const int full = S.g.nblk - (S.g.last < b ? 1 : 0);
+    POETX_TRY(simt_gemm<float, float, float>(st, b, n, b, full, BR, b, 1, bb, T1, n, 1,
+                                             static_cast<int64_t>(b) * n, K, n, 1,
+                                             static_cast<int64_t>(b) * n, 1.f, 0.f));
+    if (S.g.last < b) {
+      const int64_t o = static_cast<int64_t>(full) * b * n;
+      POETX_TRY(simt_gemm<float, float, float>(st, S.g.last, n, S.g.last, 1, BR + full * bb, b, 1, 0,
+                                               T1 + o, n, 1, 0, K + o, n, 1, 0, 1.f, 0.f));
+    }
+  }
+  // rho = pi_old^-1 o pi_new on both sides.
+  std::vector<int32_t> oR, oRi, oP, oPi, nR, nRi, nP, nPi;
+  perm_and_inverse(desc->seed_R, m, oR, oRi);
+  perm_and_inverse(desc->seed_P, n, oP, oPi);
+  perm_and_inverse(new_seed_R, m, nR, nRi);
+  perm_and_inverse(new_seed_P, n, nP, nPi);
+  std::vector<int32_t> rR(m), rP(n);
+  for (int i = 0; i < m; ++i) rR[i] = oRi[nR[i]];
+  for (int j = 0; j < n; ++j) rP[j] = oPi[nP[j]];
+  POETX_TRY(ring_upload(st, {{rR.data(), rR.size()}, {rP.data(), rP.size()}}, {rhoR, rhoP}));
+  const int grid = std::min(m, device_sm_count() * 8);
+  if (desc->dtype == POETX_DTYPE_BF16)
+    gather2d_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(
+        K, reinterpret_cast<__nv_bfloat16*>(W0p), rhoR, rhoP, m, n);
+  else
+    gather2d_kernel<float, float><<<grid, 256, 0, st>>>(K, reinterpret_cast<float*>(W0p), rhoR, rhoP,
+                                                        m, n);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params, const void* W0p,
+                                    const void* X_host, const void* dY_host, int64_t T, void* X_dev,
+                                    void* dY_dev, void* Y_dev, void* saved_h_dev, void* dX_dev,
+                                    float* dGenR_dev, float* dGenP_dev, float* dGenR_host,
+                                    float* dGenP_host, void* workspace, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (T < 0 || !X_host || !dY_host || !X_dev || !dY_dev || !dGenR_host || !dGenP_host)
+    return POETX_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t e = desc->dtype == POETX_DTYPE_BF16 ? 2 : 4;
+  POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, static_cast<size_t>(T) * desc->n * e,
+                             cudaMemcpyHostToDevice, st));
+  POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
+                             cudaMemcpyHostToDevice, st));
+  POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, workspace, stream));
+  POETX_TRY(poetx_linear_bwd(desc, params, W0p, X_dev, dY_dev, saved_h_dev, T, dX_dev, dGenR_dev,
+                             dGenP_dev, 0, workspace, stream));
+  const int64_t lr = poetx_gen_length(desc->m, desc->b_R), lp = poetx_gen_length(desc->n, desc->b_P);
+  if (lr > 0)
+    POETX_CUDA(cudaMemcpyAsync(dGenR_host, dGenR_dev, lr * 4, cudaMemcpyDeviceToHost, st));
+  if (lp > 0)
+    POETX_CUDA(cudaMemcpyAsync(dGenP_host, dGenP_dev, lp * 4, cudaMemcpyDeviceToHost, st));
+  POETX_CUDA(cudaStreamSynchronize(st));
+  return POETX_OK;
+}
+
+poetx_status poetx_device_status(int32_t reset) {
+  POETX_CUDA(cudaDeviceSynchronize());
+  unsigned int w = 0;
+  POETX_CUDA(cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w)));
+  if (reset) {
+    const unsigned int zero = 0;
+    POETX_CUDA(cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)));
+  }
+  if (w & kStatusTimeout) return POETX_ERR_TIMEOUT;
+  if (w & kStatusBadArgs) return POETX_ERR_INVALID_ARG;
+  return POETX_OK;
+}
+
+}  // extern "C"
+
+namespace {
+__device__ int g_selftest_result;
+}
+
+extern "C" {
+
+poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return POETX_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  POETX_CUDA(cudaStreamSynchronize(st));
+  unsigned int before = 0;
+  POETX_CUDA(cudaMemcpyFromSymbol(&before, g_status_word, sizeof(before)));
+  int* result = nullptr;
+  POETX_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&result), g_selftest_result));
+  POETX_CUDA(cudaMemsetAsync(result, 0, sizeof(int), st));
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(timeout_ns, result);
+  POETX_LAUNCHED();
+  POETX_CUDA(cudaStreamSynchronize(st));
+  int r = 0;
+  unsigned int after = 0;
+  POETX_CUDA(cudaMemcpyFromSymbol(&r, g_selftest_result, sizeof(r)));
+  POETX_CUDA(cudaMemcpyFromSymbol(&after, g_status_word, sizeof(after)));
+  // leave the status word as it was: this timeout was requested
+  POETX_CUDA(cudaMemcpyToSymbol(g_status_word, &before, sizeof(before)));
+  if (r == 2 && (after & kStatusTimeout)) return POETX_ERR_TIMEOUT;
+  if (r == 1) return POETX_OK;
+  return POETX_ERR_CUDA;
+}
+
+void poetx_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+"""Shared helpers of the GPU parity tests: run one layer through the C ABI and
+through the fp64 oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import synth
+
+
+def rel_fro(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def make_inputs(m, n, bR, bP, T, dtype, index=0, t0=0, t1=None, gstd=synth.STD_GEN):
+    lin = synth.Linear("case", n, m)
+    lr, lp = O.packed_length(m, bR), O.packed_length(n, bP)
+    inp = synth.layer_inputs(lin, index, T, dtype, lr, lp, t0=t0, t1=t1)
+    if gstd != synth.STD_GEN:
+        inp.genR = inp.genR * (gstd / synth.STD_GEN)
+        inp.genP = inp.genP * (gstd / synth.STD_GEN)
+    return inp
+
+
+def run_gpu(px, desc, inp, recompute: bool, want_dX=True, dev="cuda"):
+    """Forward + backward through the C ABI; returns CPU float64 numpy arrays."""
+    T = inp.X.shape[0]
+    layer = px.Layer(desc, max(T, 1), device=dev)
+    layer.build(inp.genR.to(dev), inp.genP.to(dev))
+    W0 = inp.W0.to(dev)
+    layer.premerge(W0)
+    X = inp.X.to(dev)
+    dY = inp.dY.to(dev)
+    Y = torch.empty(T, desc.m, dtype=layer.dtype, device=dev)
+    h = None if recompute else torch.empty(T, desc.m, dtype=layer.dtype, device=dev)
+    layer.forward(X, Y, saved_h=h)
+    dX = torch.empty(T, desc.n, dtype=layer.dtype, device=dev) if want_dX else None
+    dgR = torch.empty(layer.len_R, dtype=torch.float32, device=dev)
+    dgP = torch.empty(layer.len_P, dtype=torch.float32, device=dev)
+    layer.backward(X, dY, dX, dgR, dgP, saved_h=h)
+    torch.cuda.synchronize()
+    st = px.poetx_device_status(reset=True)
+    assert st == px.POETX_OK, px.poetx_status_string(st)
+    f = lambda t: None if t is None else t.double().cpu().numpy()
+    return dict(Y=f(Y), dX=f(dX), dgR=f(dgR), dgP=f(dgP), W0p=f(layer.W0p), layer=layer)
+
+
+def run_oracle(spec: O.LayerSpec, inp):
+    W0 = inp.W0.double().numpy()
+    X = inp.X.double().numpy()
+    dY = inp.dY.double().numpy()
+    gR = inp.genR.double().numpy()
+    gP = inp.genP.double().numpy()
+    dX, dgR, dgP, ex = O.backward(spec, W0, X, dY, gR, gP)
+    return dict(Y=ex["Y"], dX=dX, dgR=dgR, dgP=dgP, W0p=ex["W0p"], h=ex["h"])

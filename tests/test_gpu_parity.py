@@ -1,0 +1,144 @@
+"""GPU parity of the CUDA path against the fp64 oracle (needs a B300).
+
+Every case runs forward + backward through the C ABI and through the oracle
+on identical seeded inputs (the oracle consumes the already-rounded values)
+and compares Y, dX and both packed generator gradients by relative Frobenius
+error: <= 1e-5 for fp32, <= 2e-2 for bf16 with fp32 accumulation.  The
+pre-merged weight W0' is a pure permutation copy and must match bit for bit,
+which also checks the device permutations against the oracle's.
+
+Shapes span several 128-token tiles with a ragged token tail, ragged last
+blocks (b not dividing the dimension), every bf16 block size, m != n, both
+Cayley and Neumann modes, and stored-h versus recompute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_cases import make_inputs, rel_fro, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def px():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import orthogonal_equivalence_reparameterized_poetx_b300 as m
+    return m
+
+
+def _case(px, m, n, bR, bP, T, dtype, mode="cayley", k=3, recompute=False, index=0, gstd=0.01):
+    inp = make_inputs(m, n, bR, bP, T, dtype, index=index, gstd=gstd)
+    desc = px.make_desc(m, n, bR, bP, inp.seed_R, inp.seed_P, dtype=dtype, mode=mode, neumann_k=k)
+    spec = O.LayerSpec(m, n, bR, bP, inp.seed_R, inp.seed_P,
+                       "neumann" if mode == "neumann" else "exact", k)
+    g = run_gpu(px, desc, inp, recompute)
+    o = run_oracle(spec, inp)
+    assert np.array_equal(g["W0p"], o["W0p"]), "pre-merged weight must be a bit-exact copy"
+    tol = TOL[dtype]
+    errs = {k_: rel_fro(g[k_], o[k_]) for k_ in ("Y", "dX", "dgR", "dgP") if o[k_].size}
+    for k_, e in errs.items():
+        assert e <= tol, f"{k_}: rel Frobenius {e:.3e} > {tol:.0e} ({errs})"
+    return errs
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_fp32_workload_256(px):
+    # single POET-X linear 256 -> 256, b = 32, 512 tokens, stored h
+    _case(px, 256, 256, 32, 32, 512, "fp32")
+
+
+def test_fp32_ragged_blocks_and_tokens_recompute(px):
+    _case(px, 200, 136, 64, 48, 77, "fp32", recompute=True, gstd=0.05)
+
+
+def test_fp32_neumann(px):
+    _case(px, 128, 128, 32, 32, 100, "fp32", mode="neumann", gstd=0.05)
+
+
+def test_fp32_blocked_builder_b256(px):
+    _case(px, 512, 384, 256, 128, 64, "fp32", gstd=0.02)
+
+
+# ------------------------------------------------------------------ bf16 path
+
+@pytest.mark.parametrize("recompute", [False, True])
+def test_bf16_b32_ragged_tokens(px, recompute):
+    _case(px, 384, 256, 32, 32, 1000, "bf16", recompute=recompute)
+
+
+def test_bf16_b64(px):
+    _case(px, 256, 640, 64, 64, 300, "bf16")
+
+
+def test_bf16_b128(px):
+    _case(px, 512, 512, 128, 128, 513, "bf16")
+
+
+def test_bf16_b512_ragged_block_and_b256(px):
+    # 768 = 512 + ragged 256 on the R side; P side b = 256
+    _case(px, 768, 512, 512, 256, 260, "bf16", recompute=True)
+
+
+def test_bf16_ragged_superblock(px):
+    # 1376 = 10 x 128 + 96: the last 128-wide super-block is partial
+    _case(px, 1376, 512, 32, 32, 128, "bf16")
+    _case(px, 512, 1376, 32, 32, 128, "bf16", index=1)
+
+
+def test_bf16_neumann(px):
+    _case(px, 256, 256, 128, 128, 200, "bf16", mode="neumann", gstd=0.05)
+
+
+def test_bf16_single_token_and_single_block(px):
+    _case(px, 128, 128, 128, 128, 1, "bf16")
+
+
+# ------------------------------------------------------------------ other ABI behaviour
+
+def test_accumulate_adds_into_generator_gradients(px):
+    inp = make_inputs(256, 256, 64, 64, 200, "bf16")
+    desc = px.make_desc(256, 256, 64, 64, inp.seed_R, inp.seed_P, dtype="bf16")
+    g = run_gpu(px, desc, inp, recompute=True)
+    layer = g["layer"]
+    dev = "cuda"
+    X, dY = inp.X.to(dev), inp.dY.to(dev)
+    dgR = torch.from_numpy(g["dgR"]).float().to(dev)
+    dgP = torch.from_numpy(g["dgP"]).float().to(dev)
+    layer.backward(X, dY, None, dgR, dgP, accumulate=True)
+    torch.cuda.synchronize()
+    assert rel_fro(dgR.double().cpu().numpy(), 2 * g["dgR"]) < 1e-6
+    assert rel_fro(dgP.double().cpu().numpy(), 2 * g["dgP"]) < 1e-6
+
+
+def test_zero_tokens(px):
+    desc = px.make_desc(128, 128, 32, 32, 1, 2, dtype="bf16")
+    layer = px.Layer(desc, 1)
+    X = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    layer.forward(X, Y)
+    dgR = torch.full((layer.len_R,), 3.0, device="cuda")
+    dgP = torch.full((layer.len_P,), 3.0, device="cuda")
+    layer.backward(X, Y, None, dgR, dgP)
+    torch.cuda.synchronize()
+    assert float(dgR.abs().max()) == 0.0 and float(dgP.abs().max()) == 0.0
+
+
+def test_bounded_wait_gives_up_and_reports_timeout(px):
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    st = px.poetx_selftest_bounded_wait(2_000_000)      # 2 ms deadline on a barrier nobody completes
+    t1.record()
+    torch.cuda.synchronize()
+    assert st == px.POETX_ERR_TIMEOUT
+    assert t0.elapsed_time(t1) < 2000.0
+    # the self-test restores the status word; the context stays usable
+    assert px.poetx_device_status(reset=False) == px.POETX_OK
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0
