@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the POET-X orthogonal-equivalence linear layer on B300.
+
+One step = the whole hot path over one batch of synthetic tokens for every
+linear of the workload: build the blocks from the generators (permutations
+plus Cayley builder), forward (gather, P blocks, W0' GEMM, R blocks,
+scatter), backward (gather, R^T blocks, per-block token reductions, dgrad
+GEMM, P^T blocks, scatter, Cayley backward and packing) and, where the
+workload says so, the merge W0 <- R W0 P under fresh permutations.
+
+Prints one JSON line.  `value` is whole-job tokens/s with inputs resident in
+HBM; `e2e` is the same metric through the C ABI from pinned host buffers,
+host<->device copies included; `roofline` covers the kernel class with the
+largest device time; `cpu_baseline` times the fp64 oracle on a bounded token
+sample on this host's cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY] [--b B]
+    python bench.py --impl reference ...      # the fp64 oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("POET-X linear fwd+bwd tokens/s and TFLOP/s (fraction of bf16 peak), 1×B300")
+DEFAULT_WORKLOAD = "d2048_block"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--b", type=int, default=None, help="block size (default: first of the workload)")
+    ap.add_argument("--mode", default="cayley", choices=["cayley", "neumann"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample tokens per linear")
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="oracle tokens per linear per step of the reference arm")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (small profiling cases only)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload arithmetic
+
+def block_square_sum(d: int, b: int) -> int:
+    full, last = d // b, d % b
+    return full * b * b + last * last
+
+
+def step_flops(wl, b: int) -> float:
+    """Algorithmic tensor flops of one step over all linears.
+
+    fwd: 2Tmn (GEMM) + 2T(sum b_P^2 + sum b_R^2) (block transforms);
+    bwd: 2Tmn (dgrad) + 4T sum b_R^2 (R^T transform and dB_R) + 4T sum b_P^2;
+    recompute adds 2Tmn + 2T sum b_P^2.  Builder, Cayley backward and merge
+    are fp32 CUDA-core work and are not counted here.
+    """
+    T = wl.tokens
+    f = 0.0
+    for lin in wl.linears:
+        sR, sP = block_square_sum(lin.m, b), block_square_sum(lin.n, b)
+        f += 4.0 * T * lin.m * lin.n + 6.0 * T * (sR + sP)
+        if wl.recompute:
+            f += 2.0 * T * lin.m * lin.n + 2.0 * T * sP
+    return f
+
+
+def gemm_flops_per_step(wl, kind: str) -> float:
+    T = wl.tokens
+    f = 0.0
+    for lin in wl.linears:
+        if kind == "gemm_fwd":
+            f += 2.0 * T * lin.m * lin.n * (2 if wl.recompute else 1)
+        elif kind == "gemm_dgrad":
+            f += 2.0 * T * lin.m * lin.n
+    return f
+
+
+def kind_flops_per_step(wl, b: int, kind: str) -> float:
+    T = wl.tokens
+    f = 0.0
+    for lin in wl.linears:
+        sR, sP = block_square_sum(lin.m, b), block_square_sum(lin.n, b)
+        if kind in ("gemm_fwd", "gemm_dgrad"):
+            return gemm_flops_per_step(wl, kind)
+        if kind == "blockdiag":
+            # fwd P and R, bwd R^T and P^T, recompute P
+            f += 2.0 * T * (2 * sP + 2 * sR + (sP if wl.recompute else 0))
+        elif kind == "gradred":
+            f += 2.0 * T * (sR + sP)
+    return f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d["bf16_tflops_sustained"], source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "orthogonal_equivalence_reparameterized_poetx_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kind: str, workload: str, b: int):
+    """DRAM bytes per launch of `kind` from a committed ncu summary, or None
+    when the kernels changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    e = d.get("entries", {}).get(f"{workload}/b{b}/{kind}")
+    return None if e is None else e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- the fp64 oracle as baseline
+
+def oracle_sample(wl, b: int, tokens: int, mode: str):
+    """Times the oracle (fwd+bwd incl. block build) on `tokens` tokens of every
+    linear; returns (seconds, threads)."""
+    import oracle as O
+    try:
+        import threadpoolctl
+        threads = max(i["num_threads"] for i in threadpoolctl.threadpool_info())
+    except Exception:
+        threads = os.cpu_count()
+    total = 0.0
+    for li, lin in enumerate(wl.linears):
+        spec = O.LayerSpec(lin.m, lin.n, b, b, synth.SEED_PERM_R + li, synth.SEED_PERM_P + li,
+                           "neumann" if mode == "neumann" else "exact", 3)
+        inp = synth.layer_inputs(lin, li, wl.tokens, wl.dtype, O.packed_length(lin.m, b),
+                                 O.packed_length(lin.n, b), t0=0, t1=tokens)
+        args = [inp.W0.double().numpy(), inp.X.double().numpy(), inp.dY.double().numpy(),
+                inp.genR.double().numpy(), inp.genP.double().numpy()]
+        t0 = time.perf_counter()
+        O.backward(spec, *args)
+        total += time.perf_counter() - t0
+    return total, threads
+
+
+def run_reference(args, wl, b, rank):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(wl, b, args.ref_tokens, args.mode)
+    times = []
+    threads = None
+    for _ in range(args.steps):
+        t, threads = oracle_sample(wl, b, args.ref_tokens, args.mode)
+        times.append(t)
+    tot = sum(times)
+    tps = args.ref_tokens * args.steps / tot
+    sample = (f"{len(wl.linears)} linears x {args.ref_tokens} tokens per step (of {wl.tokens}), "
+              f"fwd+bwd with block build, fp64 numpy; merge not timed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, b, args),
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, b, args):
+    return {
+        "workload": wl.key, "description": wl.description,
+        "linears": [f"{l.name}:{l.n}->{l.m}" for l in wl.linears],
+        "tokens": wl.tokens, "b": b, "mode": args.mode, "recompute": wl.recompute,
+        "merge_each_step": wl.merge_each_step,
+        "l2": "inputs larger than L2 (activations of all linears, several GB per step)",
+        "parallelism": f"dp{args.gpus}",
+    }
+
+
+# ---------------------------------------------------------------- the CUDA path
+
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        import dataclasses
+        wl = dataclasses.replace(wl, tokens=args.tokens)
+    b = args.b or wl.block_sizes[0]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, wl, b, rank)
+        return
+
+    import torch
+    import orthogonal_equivalence_reparameterized_poetx_b300 as px
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    T = wl.tokens
+
+    # ---- resident state and inputs (seeded host generation, copied once)
+    layers = []
+    ws_bytes = 0
+    for li, lin in enumerate(wl.linears):
+        desc = px.make_desc(lin.m, lin.n, b, b, synth.SEED_PERM_R + li, synth.SEED_PERM_P + li,
+                            dtype=wl.dtype, mode=args.mode)
+        lr, lp = px.poetx_gen_length(lin.m, b), px.poetx_gen_length(lin.n, b)
+        inp = synth.layer_inputs(lin, li, T, wl.dtype, lr, lp)
+        st = dict(lin=lin, desc=desc, lr=lr, lp=lp)
+        st["params"] = torch.empty(px.poetx_params_size(desc), dtype=torch.uint8, device=dev)
+        st["W0p"] = torch.empty(lin.m, lin.n, dtype=dt, device=dev)
+        st["genR"], st["genP"] = inp.genR.to(dev), inp.genP.to(dev)
+        st["X"], st["dY"] = inp.X.to(dev), inp.dY.to(dev)
+        st["Y"] = torch.empty(T, lin.m, dtype=dt, device=dev)
+        st["dX"] = torch.empty(T, lin.n, dtype=dt, device=dev)
+        st["h"] = None if wl.recompute else torch.empty(T, lin.m, dtype=dt, device=dev)
+        st["dgR"] = torch.empty(lr, dtype=torch.float32, device=dev)
+        st["dgP"] = torch.empty(lp, dtype=torch.float32, device=dev)
+        W0 = inp.W0.to(dev)
+        px.poetx_params_build(desc, st["genR"], st["genP"], st["params"], stream)
+        px.poetx_weight_premerge(desc, st["params"], W0, st["W0p"], stream)
+        ws_bytes = max(ws_bytes, px.poetx_workspace_size(desc, T),
+                       px.poetx_merge_workspace_size(desc))
+        layers.append(st)
+        del inp, W0
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+
+    step_counter = [0]
+
+    def step():
+        s = step_counter[0]
+        for st in layers:
+            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], stream)
+        for st in layers:
+            px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
+                                workspace, stream)
+        for st in reversed(layers):
+            px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"], T,
+                                st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
+            if dist is not None:
+                dist.all_reduce(st["dgR"])
+                dist.all_reduce(st["dgP"])
+        if wl.merge_each_step:
+            for li, st in enumerate(layers):
+                nR = synth.SEED_MERGE_R + 100 * (s + 1) + li
+                nP = synth.SEED_MERGE_P + 100 * (s + 1) + li
+                px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, workspace, stream)
+                st["desc"].seed_R, st["desc"].seed_P = nR, nP
+        step_counter[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if px.poetx_device_status(reset=True) != px.POETX_OK:
+        raise SystemExit("device status reported a timeout during warm-up")
+
+    # ---- timed region (device-resident inputs)
+    px.poetx_profile_reset()
+    px.poetx_profile_enable(True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
+    clocks = ClockSampler(gpu_idx)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    launches0 = px.poetx_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = px.poetx_launch_count() - launches0
+    clk = clocks.stop()
+    px.poetx_profile_enable(False)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    status = px.poetx_device_status(reset=True)
+
+    kinds = {}
+    for k, name in enumerate(px.KIND_NAMES):
+        g, ms = px.poetx_profile_read(k)
+        if g:
+            kinds[name] = {"groups": g, "ms": ms}
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_s = world * T * args.steps / (elapsed_ms / 1e3)
+    flops = step_flops(wl, b)
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    peaks = load_peaks()
+
+    # ---- roofline of the kernel class with the largest device time
+    top = max(kinds, key=lambda k: kinds[k]["ms"])
+    roof = None
+    if top in ("gemm_fwd", "gemm_dgrad", "blockdiag", "gradred"):
+        per_step = kind_flops_per_step(wl, b, top)
+        launches_top = kinds[top]["groups"]
+        achieved = per_step * args.steps / (kinds[top]["ms"] / 1e3) / 1e12
+        roof = {"kernel": top, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_sustained"],
+                "peak_source": f"{peaks['source']} bf16 sustained",
+                "launches": launches_top,
+                "avg_launch_ms": kinds[top]["ms"] / launches_top,
+                "flops_per_launch": per_step * args.steps / launches_top,
+                "traffic": measured_traffic(top, wl.key, b)}
+    elif top == "gather":
+        # algorithmic bytes: read + write of every gathered activation
+        by = 0
+        for lin in wl.linears:
+            by += 2 * T * (2 * lin.n + 2 * lin.m) * (2 if wl.dtype == "bf16" else 4)
+        achieved = by * args.steps / (kinds[top]["ms"] / 1e3) / 1e9
+        roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None}
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic: seeded N(0,1) activations, N(0,0.02^2) W0, "
+                                   "N(0,0.01^2) packed generators",
+        "config": workload_config(wl, b, args),
+        "tflops": tflops, "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
+        "tflops_frac_of_bf16_burst": tflops / peaks["bf16"],
+        "step_tflop": flops / 1e12, "roofline": roof, "kernels": kinds,
+        "gpu_launches": launches, "clocks": clk,
+        "device_status": px.poetx_status_string(status),
+    }
+
+    # ---- end to end through the C ABI from pinned host buffers
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist)
+
+    # ---- the oracle on this host's cores (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, threads = oracle_sample(wl, b, args.cpu_tokens, args.mode)
+        line["cpu_baseline"] = {
+            "value": args.cpu_tokens / secs, "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{len(wl.linears)} linears x {args.cpu_tokens} tokens (of {T}), fwd+bwd "
+                       f"with block build, fp64 numpy, {secs:.1f} s; merge not timed")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist):
+    T = wl.tokens
+    maxn = max(l.n for l in wl.linears)
+    maxm = max(l.m for l in wl.linears)
+    # one pinned host buffer per operand, sized for the widest linear; each
+    # linear copies its own T x n (T x m) prefix every step
+    Xh = torch.empty(T * maxn, dtype=layers[0]["X"].dtype, pin_memory=True)
+    dYh = torch.empty(T * maxm, dtype=layers[0]["X"].dtype, pin_memory=True)
+    wide_n = max(layers, key=lambda s: s["lin"].n)
+    wide_m = max(layers, key=lambda s: s["lin"].m)
+    Xh[: T * wide_n["lin"].n].copy_(wide_n["X"].reshape(-1).cpu())
+    dYh[: T * wide_m["lin"].m].copy_(wide_m["dY"].reshape(-1).cpu())
+    ghR = {id(st): torch.empty(st["lr"], dtype=torch.float32, pin_memory=True) for st in layers}
+    ghP = {id(st): torch.empty(st["lp"], dtype=torch.float32, pin_memory=True) for st in layers}
+    h2d = sum(T * (st["lin"].n + st["lin"].m) * Xh.element_size() for st in layers)
+    d2h = sum((st["lr"] + st["lp"]) * 4 for st in layers)
+    cnt = [0]
+
+    def step():
+        s = cnt[0]
+        for st in layers:
+            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], stream)
+        for st in layers:
+            px.poetx_linear_step_host(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
+                                      st["dY"], st["Y"], st["h"], st["dX"], st["dgR"], st["dgP"],
+                                      ghR[id(st)], ghP[id(st)], workspace, stream)
+        if wl.merge_each_step:
+            for li, st in enumerate(layers):
+                nR = synth.SEED_MERGE_R + 100 * (1000 + s) + li
+                nP = synth.SEED_MERGE_P + 100 * (1000 + s) + li
+                px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, workspace, stream)
+                st["desc"].seed_R, st["desc"].seed_P = nR, nP
+        torch.cuda.synchronize(dev)
+        cnt[0] += 1
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([el], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": world * T * args.steps / el, "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": 1e3 * el / args.steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -205,6 +205,33 @@ poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
  * launches; 0 restores the default (2 s). */
 void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
 
+/* Kernel classes reported by the profiling counters below. */
+enum {
+  POETX_KIND_GEMM_FWD = 0,    /* h = v W0'^T on tcgen05 (forward and recompute)   */
+  POETX_KIND_GEMM_DGRAD = 1,  /* dv = dh W0' on tcgen05                            */
+  POETX_KIND_BLOCKDIAG = 2,   /* block-diagonal transforms on tcgen05              */
+  POETX_KIND_GRADRED = 3,     /* per-block token reductions dz^T h, dv^T u        */
+  POETX_KIND_GATHER = 4,      /* feature permutations (gather / scatter)           */
+  POETX_KIND_BUILD = 5,       /* Cayley / Neumann block builder                    */
+  POETX_KIND_GENBWD = 6,      /* partial reduction, Cayley backward, packing       */
+  POETX_KIND_MERGE = 7,       /* merge and weight pre-merge                        */
+  POETX_KIND_SIMT = 8,        /* fp32 CUDA-core path of the layer                  */
+  POETX_NUM_KINDS = 9
+};
+
+/* Profiling.  While enabled, each group of launches of one kernel class is
+ * bracketed by CUDA events recorded on the launching stream (for the tensor-
+ * core classes a group is a single launch).  poetx_profile_read synchronises
+ * on those events and returns, for `kind`, the number of groups and their
+ * summed device time in milliseconds.  poetx_profile_reset forgets all
+ * records.  poetx_launch_count returns the number of kernel launches the
+ * library has made since the process started (always counted). */
+void poetx_profile_enable(int32_t on);
+void poetx_profile_reset(void);
+poetx_status poetx_profile_read(int32_t kind, int64_t* groups, double* total_ms);
+const char* poetx_profile_kind_name(int32_t kind);
+int64_t poetx_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,9 @@ __all__ = [
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
     "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
-    "poetx_set_wait_timeout_ns", "Layer", "EXPORTED_SYMBOLS",
+    "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
+    "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count", "KIND_NAMES", "Layer",
+    "EXPORTED_SYMBOLS",
 ]
 
 POETX_OK, POETX_ERR_INVALID_ARG, POETX_ERR_UNSUPPORTED = 0, 1, 2
@@ -39,8 +41,12 @@ EXPORTED_SYMBOLS = [
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
     "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
-    "poetx_set_wait_timeout_ns",
+    "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
+    "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
 ]
+
+KIND_NAMES = ["gemm_fwd", "gemm_dgrad", "blockdiag", "gradred", "gather", "build", "genbwd",
+              "merge", "simt"]
 
 
 class PoetxError(RuntimeError):
@@ -92,6 +98,12 @@ def _load():
         "poetx_device_status": (I32, [I32]),
         "poetx_selftest_bounded_wait": (I32, [U64, P]),
         "poetx_set_wait_timeout_ns": (V, [U64]),
+        "poetx_profile_enable": (V, [I32]),
+        "poetx_profile_reset": (V, []),
+        "poetx_profile_read": (I32, [I32, ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_double)]),
+        "poetx_profile_kind_name": (ctypes.c_char_p, [I32]),
+        "poetx_launch_count": (I64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -209,6 +221,29 @@ def poetx_selftest_bounded_wait(timeout_ns: int, stream=None) -> int:
 
 def poetx_set_wait_timeout_ns(timeout_ns: int):
     LIB.poetx_set_wait_timeout_ns(timeout_ns)
+
+
+def poetx_profile_enable(on: bool = True):
+    LIB.poetx_profile_enable(1 if on else 0)
+
+
+def poetx_profile_reset():
+    LIB.poetx_profile_reset()
+
+
+def poetx_profile_read(kind: int):
+    """(groups, total_ms) of the timed launch groups of one kernel class."""
+    g, ms = ctypes.c_int64(), ctypes.c_double()
+    _check(LIB.poetx_profile_read(kind, ctypes.byref(g), ctypes.byref(ms)), "poetx_profile_read")
+    return g.value, ms.value
+
+
+def poetx_profile_kind_name(kind: int) -> str:
+    return LIB.poetx_profile_kind_name(kind).decode()
+
+
+def poetx_launch_count() -> int:
+    return LIB.poetx_launch_count()
 
 
 class Layer:

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -34,6 +35,52 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ profiling
+std::atomic<int64_t> g_launches{0};
+
+struct ProfRecord {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<ProfRecord> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+Profiler g_prof;
+
+// Brackets the launches made during its lifetime with events on `st`.
+struct ProfScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t start = nullptr;
+  ProfScope(int k, cudaStream_t s) : kind(k), st(s) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    start = g_prof.get();
+    cudaEventRecord(start, st);
+  }
+  ~ProfScope() {
+    if (!start) return;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    cudaEvent_t stop = g_prof.get();
+    cudaEventRecord(stop, st);
+    g_prof.recs.push_back(ProfRecord{kind, start, stop});
+  }
+};
 
 // ------------------------------------------------------------------ permutations
 // splitmix64 (Steele, Lea & Flood, OOPSLA 2014) drives a Fisher-Yates shuffle;
@@ -245,6 +292,7 @@ inline bool aligned(const void* p, size_t a) {
 
 #define POETX_LAUNCHED()                         \
   do {                                           \
+    g_launches.fetch_add(1, std::memory_order_relaxed); \
     if (cudaGetLastError() != cudaSuccess) return POETX_ERR_CUDA; \
   } while (0)
 
@@ -277,6 +325,7 @@ template <typename T>
 poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* idx, int64_t rows,
                          int d) {
   if (rows <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GATHER, st);
   const size_t smem = static_cast<size_t>(d) * sizeof(T);
   if (smem > 48 * 1024) {
     static std::once_flag once;
@@ -352,6 +401,7 @@ poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap
 poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
                          int K) {
   if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GEMM_FWD, st);
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
   CUtensorMap ta, tb;
@@ -372,6 +422,7 @@ poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C,
 poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
                          int K) {
   if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GEMM_DGRAD, st);
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
   CUtensorMap ta, tb;
@@ -392,6 +443,7 @@ poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C,
 poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void* out, int64_t T,
                           int d, int sb, int nsb) {
   if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_BLOCKDIAG, st);
   const int BN = sb >= 256 ? 256 : 128;
   CUtensorMap ta, tb;
   POETX_TRY(tmap_bf16(&ta, in, T, d, d, 128));
@@ -412,6 +464,7 @@ poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, con
                         float* partial, int64_t T, int expected_splits) {
   const Splits sp = gradred_splits(S, T, device_sm_count());
   if (sp.splits != expected_splits) return POETX_ERR_INVALID_ARG;
+  ProfScope prof(POETX_KIND_GRADRED, st);
   const int d = S.g.d, sb = S.sb, nsb = S.nsb;
   CUtensorMap ta, tb;
   POETX_TRY(tmap_bf16(&ta, A, T, d, d, 64));
@@ -432,6 +485,7 @@ poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, con
 
 poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
                         const float* gen, uint8_t* params) {
+  ProfScope prof(POETX_KIND_BUILD, st);
   float* B = reinterpret_cast<float*>(params + S.off_B);
   float* M = reinterpret_cast<float*>(params + S.off_M);
   float* Q = reinterpret_cast<float*>(params + S.off_Q);
@@ -519,6 +573,7 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
 poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
                                 const uint8_t* params, const float* G, float* t1, float* t2,
                                 float* nsc, float* dGen, int accumulate) {
+  ProfScope prof(POETX_KIND_GENBWD, st);
   const int b = S.g.b, nb = S.g.nblk;
   const int64_t bb = static_cast<int64_t>(b) * b;
   const float* M = reinterpret_cast<const float*>(params + S.off_M);
@@ -691,10 +746,13 @@ poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T,
   float* h = hs ? hs : c.w<float>(c.W.off_m1);
   float* z = c.w<float>(c.W.off_m2);
   POETX_TRY(gather_cols<float>(c.st, X, u, c.piP(), T, n));
-  POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
-  POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1, n, 0,
-                                           h, m, 1, 0, 1.f, 0.f));
-  POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, h, z, T, m, true));
+  {
+    ProfScope prof(POETX_KIND_SIMT, c.st);
+    POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
+    POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1, n,
+                                             0, h, m, 1, 0, 1.f, 0.f));
+    POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, h, z, T, m, true));
+  }
   POETX_TRY(gather_cols<float>(c.st, z, Y, c.piRinv(), T, m));
   return POETX_OK;
 }
@@ -738,21 +796,27 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
   float* dh = c.w<float>(c.W.off_m3);
   POETX_TRY(gather_cols<float>(c.st, X, u, c.piP(), T, n));
   const float* h = hs;
-  if (!hs) {
-    POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
-    POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1, n,
-                                             0, hbuf, m, 1, 0, 1.f, 0.f));
-    h = hbuf;
+  {
+    ProfScope prof(POETX_KIND_SIMT, c.st);
+    if (!hs) {
+      POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, u, v, T, n, true));
+      POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), m, n, 1, v, n, 1, 0, W0p, 1,
+                                               n, 0, hbuf, m, 1, 0, 1.f, 0.f));
+      h = hbuf;
+    }
   }
   POETX_TRY(gather_cols<float>(c.st, dY, dz, c.piR(), T, m));
-  POETX_TRY(simt_gradblocks(c.st, c.L.R, dz, h, c.w<float>(c.W.off_GR), T, m));
-  POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, dz, dh, T, m, false));
   float* dv = v;
-  POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), n, m, 1, dh, m, 1, 0, W0p, n, 1, 0,
-                                           dv, n, 1, 0, 1.f, 0.f));
-  POETX_TRY(simt_gradblocks(c.st, c.L.P, dv, u, c.w<float>(c.W.off_GP), T, n));
   float* du = u;
-  POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, dv, du, T, n, false));
+  {
+    ProfScope prof(POETX_KIND_SIMT, c.st);
+    POETX_TRY(simt_gradblocks(c.st, c.L.R, dz, h, c.w<float>(c.W.off_GR), T, m));
+    POETX_TRY(simt_blocks<float, float>(c.st, c.L.R, c.params, dz, dh, T, m, false));
+    POETX_TRY(simt_gemm<float, float, float>(c.st, static_cast<int>(T), n, m, 1, dh, m, 1, 0, W0p, n, 1,
+                                             0, dv, n, 1, 0, 1.f, 0.f));
+    POETX_TRY(simt_gradblocks(c.st, c.L.P, dv, u, c.w<float>(c.W.off_GP), T, n));
+    POETX_TRY(simt_blocks<float, float>(c.st, c.L.P, c.params, dv, du, T, n, false));
+  }
   if (dX) POETX_TRY(gather_cols<float>(c.st, du, dX, c.piPinv(), T, n));
   return POETX_OK;
 }
@@ -785,6 +849,7 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   auto* du = u;
   POETX_TRY(tc_blockdiag(c.st, dv, c.p<__nv_bfloat16>(P.off_BsbT), du, T, n, P.sb, P.nsb));
   if (dX) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+  ProfScope prof(POETX_KIND_GENBWD, c.st);
   gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
       partR, static_cast<int64_t>(R.nsb) * R.sb * R.sb, c.W.splitsR, R.g, R.sb, c.w<float>(c.W.off_GR));
   POETX_LAUNCHED();
@@ -872,6 +937,7 @@ poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* par
   const int32_t* piR = reinterpret_cast<const int32_t*>(pb + L.off_piR);
   const int32_t* piP = reinterpret_cast<const int32_t*>(pb + L.off_piP);
   const int grid = std::min(desc->m, device_sm_count() * 8);
+  ProfScope prof(POETX_KIND_MERGE, st);
   if (desc->dtype == POETX_DTYPE_BF16)
     gather2d_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(
         reinterpret_cast<const __nv_bfloat16*>(W0), reinterpret_cast<__nv_bfloat16*>(W0p), piR, piP,
@@ -982,6 +1048,7 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
   float* K = reinterpret_cast<float*>(ws + mn);
   int32_t* rhoR = reinterpret_cast<int32_t*>(ws + 2 * mn);
   int32_t* rhoP = reinterpret_cast<int32_t*>(ws + 2 * mn + align_up(static_cast<size_t>(m) * 4));
+  ProfScope prof(POETX_KIND_MERGE, st);
   // T1 = W0' blockdiag(B_P): row-local blocks along n (not transposed).
   if (desc->dtype == POETX_DTYPE_BF16)
     POETX_TRY(simt_blocks<__nv_bfloat16, float>(st, L.P, pb, reinterpret_cast<const __nv_bfloat16*>(W0p),
@@ -1099,5 +1166,49 @@ poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream) {
 void poetx_set_wait_timeout_ns(uint64_t timeout_ns) {
   g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
 }
+
+}  // extern "C"
+
+extern "C" {
+
+void poetx_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.on = on != 0;
+}
+
+void poetx_profile_reset(void) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  for (auto& r : g_prof.recs) {
+    g_prof.pool.push_back(r.start);
+    g_prof.pool.push_back(r.stop);
+  }
+  g_prof.recs.clear();
+}
+
+poetx_status poetx_profile_read(int32_t kind, int64_t* groups, double* total_ms) {
+  if (kind < 0 || kind >= POETX_NUM_KINDS || !groups || !total_ms) return POETX_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  int64_t n = 0;
+  double ms = 0.0;
+  for (auto& r : g_prof.recs) {
+    if (r.kind != kind) continue;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return POETX_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) return POETX_ERR_CUDA;
+    ms += t;
+    ++n;
+  }
+  *groups = n;
+  *total_ms = ms;
+  return POETX_OK;
+}
+
+const char* poetx_profile_kind_name(int32_t kind) {
+  static const char* names[POETX_NUM_KINDS] = {"gemm_fwd", "gemm_dgrad", "blockdiag", "gradred",
+                                               "gather", "build", "genbwd", "merge", "simt"};
+  return (kind >= 0 && kind < POETX_NUM_KINDS) ? names[kind] : "unknown";
+}
+
+int64_t poetx_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

@@ -21,6 +21,7 @@ regenerate a sampled row of a 65536-token input without building the rest.
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import List, Optional, Sequence
 
 import numpy as np
@@ -94,13 +95,24 @@ def rows(seed: int, t0: int, t1: int, cols: int, std: float) -> np.ndarray:
         return np.zeros((0, cols), dtype=np.float32)
     out = np.empty((t1 - t0, cols), dtype=np.float32)
     c0, c1 = t0 // CHUNK_ROWS, (t1 - 1) // CHUNK_ROWS
-    for c in range(c0, c1 + 1):
+
+    def fill(c):
         rng = np.random.default_rng([seed, c])
         blk = rng.standard_normal((CHUNK_ROWS, cols), dtype=np.float32)
         lo, hi = max(t0, c * CHUNK_ROWS), min(t1, (c + 1) * CHUNK_ROWS)
         out[lo - t0:hi - t0] = blk[lo - c * CHUNK_ROWS:hi - c * CHUNK_ROWS]
-    if std != 1.0:
-        out *= np.float32(std)
+        if std != 1.0:
+            out[lo - t0:hi - t0] *= np.float32(std)
+
+    nchunks = c1 - c0 + 1
+    if nchunks >= 16:
+        # chunks are independent streams, so threads change nothing in the values
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(c0, c1 + 1)))
+    else:
+        for c in range(c0, c1 + 1):
+            fill(c)
     return out
 
 
