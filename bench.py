@@ -318,11 +318,42 @@ def main():
     torch.cuda.synchronize(dev)
 
     step_counter = [0]
+    # Per-layer work that does not depend on other layers (building the blocks
+    # from the generators, and the merge) is issued on one side stream per
+    # layer and joined with events; forward and backward run on `stream`.
+    # Each merge has its own scratch so concurrent merges do not share it.
+    side = [torch.cuda.Stream(dev) for _ in layers]
+    merge_ws = ([torch.empty(px.poetx_merge_workspace_size(st["desc"]), dtype=torch.uint8,
+                             device=dev) for st in layers] if wl.merge_each_step else None)
+
+    def fan_out(fn):
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done = []
+        for li, st in enumerate(layers):
+            side[li].wait_event(ev)
+            fn(li, st, side[li])
+            e = torch.cuda.Event()
+            e.record(side[li])
+            done.append(e)
+        for e in done:
+            stream.wait_event(e)
+
+    def build_all():
+        fan_out(lambda li, st, ss: px.poetx_params_build(st["desc"], st["genR"], st["genP"],
+                                                         st["params"], ss))
+
+    def merge_all(s):
+        def one(li, st, ss):
+            nR = synth.SEED_MERGE_R + 100 * (s + 1) + li
+            nP = synth.SEED_MERGE_P + 100 * (s + 1) + li
+            px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, merge_ws[li], ss)
+            st["desc"].seed_R, st["desc"].seed_P = nR, nP
+        fan_out(one)
 
     def step():
         s = step_counter[0]
-        for st in layers:
-            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], stream)
+        build_all()
         for st in layers:
             px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
                                 workspace, stream)
@@ -333,11 +364,7 @@ def main():
                 dist.all_reduce(st["dgR"])
                 dist.all_reduce(st["dgP"])
         if wl.merge_each_step:
-            for li, st in enumerate(layers):
-                nR = synth.SEED_MERGE_R + 100 * (s + 1) + li
-                nP = synth.SEED_MERGE_P + 100 * (s + 1) + li
-                px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, workspace, stream)
-                st["desc"].seed_R, st["desc"].seed_P = nR, nP
+            merge_all(s)
         step_counter[0] += 1
 
     for _ in range(args.warmup):
@@ -386,7 +413,11 @@ def main():
     peaks = load_peaks()
 
     # ---- roofline of the kernel class with the largest device time
-    top = max(kinds, key=lambda k: kinds[k]["ms"])
+    # candidates: kernel classes issued on the main stream one launch at a time
+    # (builds and merges run concurrently on side streams, so their summed
+    # group times are not wall time)
+    serial = {k: v for k, v in kinds.items() if k not in ("build", "merge")}
+    top = max(serial, key=lambda k: serial[k]["ms"])
     roof = None
     if top in ("gemm_fwd", "gemm_dgrad", "blockdiag", "gradred"):
         per_step = kind_flops_per_step(wl, b, top)
@@ -402,9 +433,11 @@ def main():
                 "traffic": measured_traffic(top, wl.key, b)}
     elif top == "gather":
         # algorithmic bytes: read + write of every gathered activation
+        # per layer: X -> u in the forward and again in the backward, z -> Y,
+        # dY -> dz and du -> dX; each reads and writes T x d elements
         by = 0
         for lin in wl.linears:
-            by += 2 * T * (2 * lin.n + 2 * lin.m) * (2 if wl.dtype == "bf16" else 4)
+            by += 2 * T * (3 * lin.n + 2 * lin.m) * (2 if wl.dtype == "bf16" else 4)
         achieved = by * args.steps / (kinds[top]["ms"] / 1e3) / 1e9
         roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None}
@@ -425,7 +458,8 @@ def main():
 
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist)
+        line["e2e"] = run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
+                              build_all, merge_all)
 
     # ---- the oracle on this host's cores (rank 0, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -441,7 +475,8 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist):
+def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist, build_all,
+            merge_all):
     T = wl.tokens
     maxn = max(l.n for l in wl.linears)
     maxm = max(l.m for l in wl.linears)
@@ -461,18 +496,13 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist)
 
     def step():
         s = cnt[0]
-        for st in layers:
-            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], stream)
+        build_all()
         for st in layers:
             px.poetx_linear_step_host(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
                                       st["dY"], st["Y"], st["h"], st["dX"], st["dgR"], st["dgP"],
                                       ghR[id(st)], ghP[id(st)], workspace, stream)
         if wl.merge_each_step:
-            for li, st in enumerate(layers):
-                nR = synth.SEED_MERGE_R + 100 * (1000 + s) + li
-                nP = synth.SEED_MERGE_P + 100 * (1000 + s) + li
-                px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, workspace, stream)
-                st["desc"].seed_R, st["desc"].seed_P = nR, nP
+            merge_all(1000 + s)
         torch.cuda.synchronize(dev)
         cnt[0] += 1
 

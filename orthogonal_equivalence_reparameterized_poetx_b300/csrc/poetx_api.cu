@@ -326,16 +326,47 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
                          int d) {
   if (rows <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_GATHER, st);
-  const size_t smem = static_cast<size_t>(d) * sizeof(T);
+  if ((static_cast<size_t>(d) * sizeof(T)) % 16 != 0) {
+    const int grid = static_cast<int>(std::min<int64_t>(rows, device_sm_count() * 8));
+    gather_cols_scalar_kernel<T><<<grid, 256, 0, st>>>(in, out, idx, rows, d);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
+  const size_t row_bytes = static_cast<size_t>(d) * sizeof(T);
+  if constexpr (sizeof(T) == 2) {
+    // interleaved row pairs, about 32 KB staged per iteration (at least one pair)
+    const int ppi = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (16 * 1024) / row_bytes)));
+    const size_t smem = 2 * row_bytes * ppi;
+    if (smem > 48 * 1024) {
+      static std::once_flag once2;
+      std::call_once(once2, [] {
+        cudaFuncSetAttribute(gather_cols_bf16x2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             200 * 1024);
+      });
+      if (smem > 200 * 1024) return POETX_ERR_UNSUPPORTED;
+    }
+    const int64_t iters = (rows + 2 * ppi - 1) / (2 * ppi);
+    const int grid = static_cast<int>(std::min<int64_t>(iters, device_sm_count() * 8));
+    gather_cols_bf16x2_kernel<<<grid, 256, smem, st>>>(reinterpret_cast<const uint4*>(in),
+                                                       reinterpret_cast<uint4*>(out), idx, rows, d,
+                                                       ppi);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
+  // stage about 32 KB of rows per iteration (at least one row)
+  const int rpi = static_cast<int>(std::max<size_t>(1, std::min<size_t>(16, (32 * 1024) / row_bytes)));
+  const size_t smem = row_bytes * rpi;
   if (smem > 48 * 1024) {
     static std::once_flag once;
     std::call_once(once, [] {
       cudaFuncSetAttribute(gather_cols_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            200 * 1024);
     });
+    if (smem > 200 * 1024) return POETX_ERR_UNSUPPORTED;
   }
-  const int grid = static_cast<int>(std::min<int64_t>(rows, device_sm_count() * 8));
-  gather_cols_kernel<T><<<grid, 256, smem, st>>>(in, out, idx, rows, d);
+  const int64_t iters = (rows + rpi - 1) / rpi;
+  const int grid = static_cast<int>(std::min<int64_t>(iters, device_sm_count() * 8));
+  gather_cols_kernel<T><<<grid, 256, smem, st>>>(in, out, idx, rows, d, rpi);
   POETX_LAUNCHED();
   return POETX_OK;
 }
@@ -380,10 +411,10 @@ poetx_status tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
 
 template <int BN, bool A_MN, bool B_MN, TileMode MODE, typename OutT>
 poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
-                       TcGemmArgs args) {
+                       const CUtensorMap& tc, TcGemmArgs args) {
   if (args.num_tiles <= 0) return POETX_OK;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, MODE, OutT>;
-  constexpr int smem = TcGemmCfg<BN>::SMEM_BYTES;
+  constexpr int smem = TcGemmCfg<BN, MODE != TileMode::GradRed>::SMEM_BYTES;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -392,7 +423,7 @@ poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap
   if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
   args.timeout_ns = g_timeout_ns;
   const int grid = std::min(args.num_tiles, device_sm_count());
-  kern<<<grid, 192, smem, st>>>(ta, tb, args);
+  kern<<<grid, 320, smem, st>>>(ta, tb, tc, args);
   POETX_LAUNCHED();
   return POETX_OK;
 }
@@ -404,9 +435,10 @@ poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C,
   ProfScope prof(POETX_KIND_GEMM_FWD, st);
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
   POETX_TRY(tmap_bf16(&tb, W, N, K, K, BN));
+  POETX_TRY(tmap_bf16(&tc, C, T, N, N, 128));
   TcGemmArgs a{};
   a.M = static_cast<int>(T);
   a.N = N;
@@ -414,8 +446,8 @@ poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C,
   a.C = C;
   a.ldc = N;
   a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
-  if (wide) return launch_tc<256, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
-  return launch_tc<128, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+  if (wide) return launch_tc<256, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
+  return launch_tc<128, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
 }
 
 // dv (T x N) = A (T x K) * W, W row-major K x N (B operand MN-major).
@@ -425,9 +457,10 @@ poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C,
   ProfScope prof(POETX_KIND_GEMM_DGRAD, st);
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
   POETX_TRY(tmap_bf16(&tb, W, K, N, N, 64));
+  POETX_TRY(tmap_bf16(&tc, C, T, N, N, 128));
   TcGemmArgs a{};
   a.M = static_cast<int>(T);
   a.N = N;
@@ -435,8 +468,8 @@ poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C,
   a.C = C;
   a.ldc = N;
   a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
-  if (wide) return launch_tc<256, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
-  return launch_tc<128, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, a);
+  if (wide) return launch_tc<256, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
+  return launch_tc<128, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
 }
 
 // out[:, s] = in[:, s] * S_s^T over super-blocks: in/out T x d, Ssb (nsb*sb) x sb.
@@ -445,9 +478,10 @@ poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void
   if (T <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_BLOCKDIAG, st);
   const int BN = sb >= 256 ? 256 : 128;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   POETX_TRY(tmap_bf16(&ta, in, T, d, d, 128));
   POETX_TRY(tmap_bf16(&tb, Ssb, static_cast<uint64_t>(nsb) * sb, sb, sb, BN));
+  POETX_TRY(tmap_bf16(&tc, out, T, d, d, 128));
   TcGemmArgs a{};
   a.M = static_cast<int>(T);
   a.N = d;
@@ -455,8 +489,8 @@ poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void
   a.C = out;
   a.ldc = d;
   a.num_tiles = static_cast<int>((T + 127) / 128) * ((d + BN - 1) / BN);
-  if (BN == 256) return launch_tc<256, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, a);
-  return launch_tc<128, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, a);
+  if (BN == 256) return launch_tc<256, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, tc, a);
+  return launch_tc<128, false, false, TileMode::BlockDiag, __nv_bfloat16>(st, ta, tb, tc, a);
 }
 
 // partial[p][s] = sum_{t in split p} A[t, s]^T B[t, s] (fp32, sb x sb per super-block).
@@ -478,10 +512,55 @@ poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, con
   a.split_stride = static_cast<int64_t>(nsb) * sb * sb;
   const int tps = sb / 128;
   a.num_tiles = sp.splits * nsb * tps * tps;
-  return launch_tc<128, true, true, TileMode::GradRed, float>(st, ta, tb, a);
+  return launch_tc<128, true, true, TileMode::GradRed, float>(st, ta, tb, ta, a);
 }
 
 // ------------------------------------------------------------------ builder
+
+bool fused_cayley_ok(const poetx_layer_desc& d, int b) {
+  return d.mode == POETX_MODE_CAYLEY && b <= 128;
+}
+
+CayleySide cayley_side(const poetx_layer_desc& d, const SideLayout& S, const float* gen,
+                       uint8_t* params) {
+  const bool bf = d.dtype == POETX_DTYPE_BF16;
+  CayleySide c;
+  c.gen = gen;
+  c.s = S.g;
+  c.B = reinterpret_cast<float*>(params + S.off_B);
+  c.M = reinterpret_cast<float*>(params + S.off_M);
+  c.Q = reinterpret_cast<float*>(params + S.off_Q);
+  c.sb = S.sb;
+  c.nsb = S.nsb;
+  c.Bsb = bf ? reinterpret_cast<__nv_bfloat16*>(params + S.off_Bsb) : nullptr;
+  c.BsbT = bf ? reinterpret_cast<__nv_bfloat16*>(params + S.off_BsbT) : nullptr;
+  return c;
+}
+
+// Exact Cayley blocks of one side, or of both sides at once when `second`
+// is given (same block size), in a single launch.
+poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, const CayleySide& a,
+                                  const CayleySide* second) {
+  const int b = a.s.b;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const int lim = 128 * 129 * 4;
+    cudaFuncSetAttribute(cayley_block_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(cayley_block_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(cayley_block_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(cayley_block_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  });
+  const size_t smem = d.dtype == POETX_DTYPE_BF16 ? static_cast<size_t>(b) * (b + 1) * 4 : 0;
+  const int R = std::min(b, 1024 / b);
+  const int grid = a.s.nblk + (second ? second->s.nblk : 0);
+  auto kern = b == 128 ? cayley_block_kernel<128>
+            : b == 64  ? cayley_block_kernel<64>
+            : b == 32  ? cayley_block_kernel<32>
+                       : cayley_block_kernel<0>;
+  kern<<<grid, b * R, smem, st>>>(a, second ? *second : a);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
 
 poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
                         const float* gen, uint8_t* params) {
@@ -491,34 +570,28 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
   float* Q = reinterpret_cast<float*>(params + S.off_Q);
   const int b = S.g.b, nb = S.g.nblk;
   const int64_t bb = static_cast<int64_t>(b) * b;
+  if (fused_cayley_ok(d, b)) {
+    POETX_TRY(launch_cayley_blocks(st, d, cayley_side(d, S, gen, params), nullptr));
+    return POETX_OK;
+  }
   unpack_kernel<<<nb, 256, 0, st>>>(gen, S.g, Q, M);
   POETX_LAUNCHED();
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(gj_invert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         128 * 128 * 4 + 2 * 128 * 4);
-  });
   if (d.mode == POETX_MODE_CAYLEY) {
-    if (b <= 128) {
-      const size_t smem = static_cast<size_t>(b) * b * 4 + 2 * b * 4;
-      gj_invert_kernel<<<nb, 1024, smem, st>>>(M, bb, b, M, bb, b, b);
-      POETX_LAUNCHED();
-    } else {
-      // Block Gauss-Jordan with 128-wide panels: for panel k,
+    {
+      // b > 128: block Gauss-Jordan with 128-wide panels: for panel k,
       // C = A[:, k], D = A_kk^-1, R = D A[k, :], A -= C R, A[k, :] = R,
       // A[:, k] = -C D, A_kk = D.
       float* Cc = reinterpret_cast<float*>(params + S.off_s1);
       float* D = reinterpret_cast<float*>(params + S.off_s2);
       float* Rr = reinterpret_cast<float*>(params + S.off_s3);
       const int P = 128;
-      const size_t smem = static_cast<size_t>(P) * P * 4 + 2 * P * 4;
       for (int k = 0; k < b / P; ++k) {
         const int o = k * P;
         copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(b) * P), nb), 256, 0, st>>>(
             M + o, bb, b, Cc, static_cast<int64_t>(b) * P, P, b, P, 1.f, 0.f);
         POETX_LAUNCHED();
-        gj_invert_kernel<<<nb, 1024, smem, st>>>(M + static_cast<int64_t>(o) * b + o, bb, b, D,
-                                                 static_cast<int64_t>(P) * P, P, P);
+        gj_invert128_kernel<<<nb, 1024, 0, st>>>(M + static_cast<int64_t>(o) * b + o, bb, b, D,
+                                                 static_cast<int64_t>(P) * P, P);
         POETX_LAUNCHED();
         POETX_TRY(simt_gemm<float, float, float>(st, P, b, P, nb, D, P, 1, static_cast<int64_t>(P) * P,
                                                  M + static_cast<int64_t>(o) * b, b, 1, bb, Rr, b, 1,
@@ -635,7 +708,7 @@ struct PinnedRing {
   std::mutex mu;
   uint8_t* buf = nullptr;
   size_t slot_bytes = 0;
-  static constexpr int kSlots = 8;
+  static constexpr int kSlots = 32;
   cudaEvent_t ev[kSlots] = {};
   bool pending[kSlots] = {};
   int next = 0;
@@ -921,6 +994,11 @@ poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR,
                         {{piR.data(), piR.size()}, {piRinv.data(), piRinv.size()},
                          {piP.data(), piP.size()}, {piPinv.data(), piPinv.size()}},
                         {pb + L.off_piR, pb + L.off_piRinv, pb + L.off_piP, pb + L.off_piPinv}));
+  if (desc->b_R == desc->b_P && fused_cayley_ok(*desc, desc->b_R)) {
+    ProfScope prof(POETX_KIND_BUILD, st);
+    const CayleySide r = cayley_side(*desc, L.R, genR, pb), p = cayley_side(*desc, L.P, genP, pb);
+    return launch_cayley_blocks(st, *desc, r, &p);
+  }
   POETX_TRY(build_side(st, *desc, L.R, genR, pb));
   POETX_TRY(build_side(st, *desc, L.P, genP, pb));
   return POETX_OK;

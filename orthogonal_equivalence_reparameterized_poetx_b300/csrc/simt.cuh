@@ -105,40 +105,110 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemmArgs g) {
 
 // ------------------------------------------------------------------ gathers
 // out[r][j] = in[r][idx[j]] for `rows` rows of d elements (row-local feature
-// permutation).  A CTA stages whole rows in shared memory with 16-byte loads,
-// then writes the permuted row with 16-byte stores, so global traffic is one
-// coalesced read and one coalesced write per element.
+// permutation).  A CTA stages `rows_per_iter` consecutive rows (one
+// contiguous span) in shared memory with 16-byte loads, then writes each
+// permuted row with 16-byte stores; the index vector of an output chunk is
+// loaded once and reused for every staged row.  Global traffic is one
+// coalesced read and one coalesced write per element.  d must be a multiple
+// of 16 / sizeof(T) (checked by the caller).
 template <typename T>
 __global__ void __launch_bounds__(256) gather_cols_kernel(const T* __restrict__ in,
                                                           T* __restrict__ out,
                                                           const int32_t* __restrict__ idx,
-                                                          int64_t rows, int d) {
+                                                          int64_t rows, int d, int rows_per_iter) {
   extern __shared__ __align__(16) uint8_t gsm[];
-  T* row = reinterpret_cast<T*>(gsm);
+  T* buf = reinterpret_cast<T*>(gsm);
+  uint4* buf4 = reinterpret_cast<uint4*>(gsm);
   constexpr int VEC = 16 / sizeof(T);
-  const bool vec_ok = (d % VEC) == 0;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const T* src = in + r * d;
-    T* dst = out + r * d;
-    if (vec_ok) {
-      for (int c = threadIdx.x; c < d / VEC; c += blockDim.x)
-        reinterpret_cast<uint4*>(row)[c] = __ldcs(reinterpret_cast<const uint4*>(src) + c);
-    } else {
-      for (int c = threadIdx.x; c < d; c += blockDim.x) row[c] = src[c];
-    }
+  const int vpr = d / VEC;
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_iter; r0 < rows;
+       r0 += static_cast<int64_t>(gridDim.x) * rows_per_iter) {
+    const int nr = static_cast<int>(min(static_cast<int64_t>(rows_per_iter), rows - r0));
+    const uint4* src = reinterpret_cast<const uint4*>(in + r0 * d);
+    for (int v = threadIdx.x; v < nr * vpr; v += blockDim.x) buf4[v] = src[v];
     __syncthreads();
-    if (vec_ok) {
-      for (int c = threadIdx.x; c < d / VEC; c += blockDim.x) {
-        alignas(16) T v[VEC];
+    for (int c = threadIdx.x; c < vpr; c += blockDim.x) {
+      int id[VEC];
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) v[q] = row[__ldg(idx + c * VEC + q)];
-        reinterpret_cast<uint4*>(dst)[c] = *reinterpret_cast<const uint4*>(v);
+      for (int q = 0; q < VEC; ++q) id[q] = __ldg(idx + c * VEC + q);
+      for (int rr = 0; rr < nr; ++rr) {
+        uint4 o;
+        if constexpr (sizeof(T) == 2) {
+          const uint16_t* row = reinterpret_cast<const uint16_t*>(buf) + rr * d;
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = static_cast<uint32_t>(row[id[2 * q]]) |
+                   (static_cast<uint32_t>(row[id[2 * q + 1]]) << 16);
+          o = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(buf) + rr * d;
+          o = make_uint4(row[id[0]], row[id[1]], row[id[2]], row[id[3]]);
+        }
+        reinterpret_cast<uint4*>(out + (r0 + rr) * d)[c] = o;
       }
-    } else {
-      for (int c = threadIdx.x; c < d; c += blockDim.x) dst[c] = row[__ldg(idx + c)];
     }
     __syncthreads();
   }
+}
+
+// bf16 version with rows staged in interleaved pairs: shared word c of pair p
+// holds (row 2p)[c] in its low half and (row 2p+1)[c] in its high half, so one
+// random 4-byte shared-memory read serves both rows (half the bank-conflicted
+// reads of a per-row gather).  `pairs_per_iter` pairs (2 rows each) are
+// staged per iteration; an odd last row pairs with zeros and is not stored.
+__global__ void __launch_bounds__(256) gather_cols_bf16x2_kernel(const uint4* __restrict__ in,
+                                                                 uint4* __restrict__ out,
+                                                                 const int32_t* __restrict__ idx,
+                                                                 int64_t rows, int d,
+                                                                 int pairs_per_iter) {
+  extern __shared__ __align__(16) uint8_t gsm[];
+  uint32_t* w = reinterpret_cast<uint32_t*>(gsm);
+  const int vpr = d / 8;  // 16-byte vectors per row
+  const int64_t rows_per_iter = 2 * static_cast<int64_t>(pairs_per_iter);
+  for (int64_t r0 = blockIdx.x * rows_per_iter; r0 < rows; r0 += gridDim.x * rows_per_iter) {
+    const int nr = static_cast<int>(min(rows_per_iter, rows - r0));
+    const int np = (nr + 1) / 2;
+    for (int v = threadIdx.x; v < np * vpr; v += blockDim.x) {
+      const int p = v / vpr, c = v % vpr;
+      const int64_t ra = r0 + 2 * p;
+      const uint4 a = in[ra * vpr + c];
+      const uint4 b = (2 * p + 1 < nr) ? in[(ra + 1) * vpr + c] : make_uint4(0, 0, 0, 0);
+      uint4* dst = reinterpret_cast<uint4*>(w + static_cast<int64_t>(p) * d + 8 * c);
+      dst[0] = make_uint4(__byte_perm(a.x, b.x, 0x5410), __byte_perm(a.x, b.x, 0x7632),
+                          __byte_perm(a.y, b.y, 0x5410), __byte_perm(a.y, b.y, 0x7632));
+      dst[1] = make_uint4(__byte_perm(a.z, b.z, 0x5410), __byte_perm(a.z, b.z, 0x7632),
+                          __byte_perm(a.w, b.w, 0x5410), __byte_perm(a.w, b.w, 0x7632));
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < vpr; c += blockDim.x) {
+      const int4 i0 = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c);
+      const int4 i1 = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c + 1);
+      for (int p = 0; p < np; ++p) {
+        const uint32_t* pw = w + static_cast<int64_t>(p) * d;
+        const uint32_t q0 = pw[i0.x], q1 = pw[i0.y], q2 = pw[i0.z], q3 = pw[i0.w];
+        const uint32_t q4 = pw[i1.x], q5 = pw[i1.y], q6 = pw[i1.z], q7 = pw[i1.w];
+        const int64_t ra = r0 + 2 * p;
+        out[ra * vpr + c] = make_uint4(__byte_perm(q0, q1, 0x5410), __byte_perm(q2, q3, 0x5410),
+                                       __byte_perm(q4, q5, 0x5410), __byte_perm(q6, q7, 0x5410));
+        if (2 * p + 1 < nr)
+          out[(ra + 1) * vpr + c] =
+              make_uint4(__byte_perm(q0, q1, 0x7632), __byte_perm(q2, q3, 0x7632),
+                         __byte_perm(q4, q5, 0x7632), __byte_perm(q6, q7, 0x7632));
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Scalar version for widths that are not a multiple of 16 bytes.
+template <typename T>
+__global__ void __launch_bounds__(256) gather_cols_scalar_kernel(const T* __restrict__ in,
+                                                                 T* __restrict__ out,
+                                                                 const int32_t* __restrict__ idx,
+                                                                 int64_t rows, int d) {
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
+    for (int c = threadIdx.x; c < d; c += blockDim.x) out[r * d + c] = in[r * d + __ldg(idx + c)];
 }
 
 // out[i][j] = convert(in[ridx[i]][cidx[j]]), both row-major with `cols`
@@ -188,41 +258,162 @@ __global__ void __launch_bounds__(256) unpack_kernel(const float* __restrict__ g
   }
 }
 
-// In-place Gauss-Jordan inversion of P x P sub-matrices (P <= 128) without
-// pivoting: the matrices inverted here are I - Q for skew Q and the pivot
-// blocks of its block elimination, whose symmetric parts are >= I, so every
-// pivot is >= 1 in magnitude and no exchange is needed.  Matrix z is read
-// at in + z*in_bs with leading dimension in_ld and written likewise to out.
-__global__ void __launch_bounds__(1024) gj_invert_kernel(const float* in, int64_t in_bs, int in_ld,
-                                                         float* out, int64_t out_bs, int out_ld,
-                                                         int P) {
-  extern __shared__ __align__(16) float gj_sm[];
-  float* a = gj_sm;            // P x P
-  float* col = a + P * P;      // P
-  float* rowv = col + P;       // P
-  const int z = blockIdx.x;
-  const float* src = in + z * in_bs;
-  for (int e = threadIdx.x; e < P * P; e += blockDim.x) a[e] = src[(e / P) * in_ld + (e % P)];
+// Register Gauss-Jordan inversion of a P x P matrix (P <= 128) by one CTA of
+// P * R threads, R = min(P, 1024 / P): thread (ty, tx) owns column j = tx and
+// rows i = ty + R*r (r < NR = ceil(P / R) <= 16) in registers.  No pivoting:
+// the matrices inverted here are I - Q for skew Q and pivot blocks of its
+// block elimination, whose symmetric parts are >= I, so every pivot has
+// magnitude >= 1.  The pivot row and column are published through a
+// double-buffered shared array, one barrier per pivot.  PT > 0 fixes P at
+// compile time (the index arithmetic folds away); PT == 0 reads P at run time.
+constexpr int kGjMaxRows = 16;
+
+template <int PT>
+struct GjShape {
+  int P, R, NR;
+  __device__ __forceinline__ explicit GjShape(int p_runtime)
+      : P(PT > 0 ? PT : p_runtime),
+        R(PT > 0 ? (PT < 1024 / PT ? PT : 1024 / PT) : min(p_runtime, 1024 / p_runtime)),
+        NR((P + R - 1) / R) {}
+};
+
+template <int PT>
+__device__ __forceinline__ void gj_register_invert(float (&a)[kGjMaxRows], const GjShape<PT>& sh,
+                                                   int tx, int ty, float* rowbuf, float* colbuf) {
+  const int P = sh.P, R = sh.R, NR = sh.NR;
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) {
+    const int i = ty + R * r;
+    if (r < NR && i < P) {
+      if (i == 0) rowbuf[tx] = a[r];
+      if (tx == 0) colbuf[i] = a[r];
+    }
+  }
   __syncthreads();
   for (int k = 0; k < P; ++k) {
-    if (threadIdx.x < P) {
-      col[threadIdx.x] = a[threadIdx.x * P + k];
-      rowv[threadIdx.x] = a[k * P + threadIdx.x];
-    }
-    __syncthreads();
-    const float p = 1.0f / rowv[k];
-    for (int e = threadIdx.x; e < P * P; e += blockDim.x) {
-      const int i = e / P, j = e % P;
-      float v;
-      if (i == k) v = (j == k) ? p : rowv[j] * p;
-      else if (j == k) v = -col[i] * p;
-      else v = fmaf(-col[i] * p, rowv[j], a[e]);
-      a[e] = v;
+    const int cur = (k & 1) * 128, nxt = 128 - cur;
+    const float p = 1.0f / rowbuf[cur + k];
+    const float rj = rowbuf[cur + tx] * p;
+    const bool col_k = (tx == k), col_k1 = (tx == k + 1);
+#pragma unroll
+    for (int r = 0; r < kGjMaxRows; ++r) {
+      const int i = ty + R * r;
+      if (r < NR && i < P) {
+        float v = a[r];
+        if (i == k) v = col_k ? p : v * p;
+        else if (col_k) v = -v * p;
+        else v = fmaf(-colbuf[cur + i], rj, v);
+        a[r] = v;
+        if (i == k + 1) rowbuf[nxt + tx] = v;
+        if (col_k1) colbuf[nxt + i] = v;
+      }
     }
     __syncthreads();
   }
-  float* dst = out + z * out_bs;
-  for (int e = threadIdx.x; e < P * P; e += blockDim.x) dst[(e / P) * out_ld + (e % P)] = a[e];
+}
+
+// Exact Cayley blocks for b <= 128, one CTA per block: unpack the packed
+// generator into A = I - Q (identity on the padding of a ragged block),
+// invert it in registers (M = (I - Q)^-1), and write M, B = 2M - I, Q and,
+// when Bsb is given, the bf16 super-block rows of this block (B and B^T on
+// the diagonal, zeros elsewhere).
+struct CayleySide {
+  const float* gen;
+  SideGeom s;
+  float* B;
+  float* M;
+  float* Q;
+  int sb, nsb;
+  __nv_bfloat16* Bsb;
+  __nv_bfloat16* BsbT;
+};
+
+// Blocks [0, first.s.nblk) belong to `first`, the rest to `second` (the R and
+// P sides of a layer built in one launch when their block sizes agree).
+template <int PT>
+__global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide first,
+                                                            const CayleySide second) {
+  const bool is_first = static_cast<int>(blockIdx.x) < first.s.nblk;
+  const CayleySide& cs = is_first ? first : second;
+  const float* __restrict__ gen = cs.gen;
+  const SideGeom s = cs.s;
+  float* __restrict__ Bout = cs.B;
+  float* __restrict__ Mout = cs.M;
+  float* __restrict__ Qout = cs.Q;
+  const int sb = cs.sb, nsb = cs.nsb;
+  __nv_bfloat16* __restrict__ Bsb = cs.Bsb;
+  __nv_bfloat16* __restrict__ BsbT = cs.BsbT;
+  __shared__ float rowbuf[256], colbuf[256];
+  extern __shared__ float bsm[];  // P x (P + 1) staging of B for the transposed writes
+  const GjShape<PT> sh(s.b);
+  const int P = sh.P, R = sh.R, NR = sh.NR;
+  const int tx = threadIdx.x % P, ty = threadIdx.x / P;
+  const int k = is_first ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - first.s.nblk;
+  const int sz = block_size(s, k);
+  const float* g = gen + static_cast<int64_t>(k) * P * (P - 1) / 2;
+  float* Mk = Mout + static_cast<int64_t>(k) * P * P;
+  float* Bk = Bout + static_cast<int64_t>(k) * P * P;
+  float* Qk = Qout + static_cast<int64_t>(k) * P * P;
+  float a[kGjMaxRows];
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) {
+    const int i = ty + R * r, j = tx;
+    float q = 0.f;
+    if (r < NR && i < P) {
+      if (i < sz && j < sz && i != j) {
+        if (i < j) q = g[i * sz - i * (i + 1) / 2 + (j - i - 1)];
+        else q = -g[j * sz - j * (j + 1) / 2 + (i - j - 1)];
+      }
+      Qk[i * P + j] = q;
+    }
+    a[r] = (i == j ? 1.f : 0.f) - q;
+  }
+  gj_register_invert<PT>(a, sh, tx, ty, rowbuf, colbuf);
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) {
+    const int i = ty + R * r;
+    if (r < NR && i < P) {
+      const float bv = 2.f * a[r] - (i == tx ? 1.f : 0.f);
+      Mk[i * P + tx] = a[r];
+      Bk[i * P + tx] = bv;
+      if (Bsb) bsm[i * (P + 1) + tx] = bv;
+    }
+  }
+  if (!Bsb) return;
+  __syncthreads();
+  // rows [k*b, k*b + b) of the super-block arrays; the last block also zeroes
+  // the rows that no block owns (features beyond nblk * b).
+  const int r0 = k * P;
+  const int r1 = (k == s.nblk - 1) ? nsb * sb : r0 + P;
+  const int c0 = r0 % sb;
+  for (int e = threadIdx.x; e < (r1 - r0) * sb; e += blockDim.x) {
+    const int rr = e / sb, c = e % sb;
+    float v = 0.f, vt = 0.f;
+    if (rr < P && c >= c0 && c < c0 + P) {
+      v = bsm[rr * (P + 1) + (c - c0)];
+      vt = bsm[(c - c0) * (P + 1) + rr];
+    }
+    const int64_t o = static_cast<int64_t>(r0 + rr) * sb + c;
+    Bsb[o] = __float2bfloat16_rn(v);
+    BsbT[o] = __float2bfloat16_rn(vt);
+  }
+}
+
+// Inverse of the 128 x 128 diagonal sub-block of matrix z: read at
+// in + z*in_bs with leading dimension in_ld, written to out likewise.
+__global__ void __launch_bounds__(1024) gj_invert128_kernel(const float* in, int64_t in_bs, int in_ld,
+                                                            float* out, int64_t out_bs, int out_ld) {
+  __shared__ float rowbuf[256], colbuf[256];
+  const GjShape<128> sh(128);
+  const int tx = threadIdx.x % 128, ty = threadIdx.x / 128;
+  const float* src = in + blockIdx.x * in_bs;
+  float a[kGjMaxRows];
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) a[r] = src[static_cast<int64_t>(ty + 8 * r) * in_ld + tx];
+  gj_register_invert<128>(a, sh, tx, ty, rowbuf, colbuf);
+  float* dst = out + blockIdx.x * out_bs;
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) dst[static_cast<int64_t>(ty + 8 * r) * out_ld + tx] = a[r];
 }
 
 // dst[z](i,j) = alpha * src[z](i,j) (+ beta * I(i,j)) over rows x cols.

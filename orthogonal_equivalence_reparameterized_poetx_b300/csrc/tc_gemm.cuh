@@ -4,12 +4,16 @@
 // memory, fp32 accumulation in tensor memory (TMEM), and an epilogue that
 // reads TMEM with tcgen05.ld and stores bf16 or fp32.
 //
-// One CTA per SM (persistent), 6 warps:
+// One CTA per SM (persistent), 10 warps:
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+//   warps 2..9  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31 and
+//               64-column half (w-2)/4 of every 128-column slice of the tile
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the
-// epilogue of one tile overlaps the main loop of the next.
+// epilogue of one tile overlaps the main loop of the next.  bf16 results are
+// staged per 128-column slice in a 128-byte-swizzled shared buffer and
+// written with TMA bulk tensor stores (whole lines, clipped at the edges);
+// fp32 partials of the token reductions are stored directly.
 //
 // Three tile schedules cover every contraction of the layer:
 //   Dense      h = v W0'^T (B K-major) and dv = dh W0' (B MN-major): tiles of
@@ -45,7 +49,7 @@ struct TcGemmArgs {
   uint64_t timeout_ns;
 };
 
-template <int BN>
+template <int BN, bool STAGED>
 struct TcGemmCfg {
   static constexpr int BM = 128;
   static constexpr int BK = 64;
@@ -54,8 +58,10 @@ struct TcGemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN >= 256) ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+  static constexpr int OUT_BYTES = STAGED ? 128 * 128 * 2 : 0;  // one 128 x 128 bf16 slice
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + 256;
+  static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct TileInfo {
@@ -99,15 +105,17 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const TcGemmArgs& a) {
 }
 
 template <int BN, bool A_MN, bool B_MN, TileMode MODE, typename OutT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcGemmArgs args) {
-  using Cfg = TcGemmCfg<BN>;
+                   const __grid_constant__ CUtensorMap tmC, const TcGemmArgs args) {
+  constexpr bool STAGED = (MODE != TileMode::GradRed);
+  using Cfg = TcGemmCfg<BN, STAGED>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint8_t* out_stage = smem + STAGES * Cfg::STAGE_BYTES;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -126,13 +134,14 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 256);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (STAGED) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -234,7 +243,9 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int g = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = g * 32 + lane;
+    const bool leader = (warp == 2 && lane == 0);
     int it = 0;
     for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
       const TileInfo t = decode_tile<BN, MODE>(tile, args);
@@ -245,54 +256,62 @@ __global__ void __launch_bounds__(192, 1)
       const bool empty_tile = t.nk <= 0;  // no MMA wrote this accumulator: store zeros
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(g * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
+      for (int sl = 0; sl < BN / 128; ++sl) {
+        // this warp's 64 columns of the 128-column slice: two loads, one wait
+        const int c0 = sl * 128 + half * 64;
+        uint32_t r[2][32];
+        tmem_ld_32x32b_x32(taddr + c0, r[0]);
+        tmem_ld_32x32b_x32(taddr + c0 + 32, r[1]);
         tmem_ld_wait();
+        if (sl == BN / 128 - 1) {  // accumulator fully read: release it to the MMA warp
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
         if (empty_tile) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) r[q] = 0u;
+          for (int q = 0; q < 32; ++q) r[0][q] = r[1][q] = 0u;
         }
         if constexpr (MODE == TileMode::GradRed) {
-          float* out = reinterpret_cast<float*>(args.C) + t.p * args.split_stride +
-                       static_cast<int64_t>(t.s) * args.sb * args.sb +
-                       static_cast<int64_t>(t.i * 128 + row) * args.sb + t.j * 128 + c * 32;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4*>(out)[q] =
-                make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+          for (int hh = 0; hh < 2; ++hh) {
+            float* out = reinterpret_cast<float*>(args.C) + t.p * args.split_stride +
+                         static_cast<int64_t>(t.s) * args.sb * args.sb +
+                         static_cast<int64_t>(t.i * 128 + row) * args.sb + t.j * 128 + c0 + 32 * hh;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<uint4*>(out)[q] =
+                  make_uint4(r[hh][4 * q], r[hh][4 * q + 1], r[hh][4 * q + 2], r[hh][4 * q + 3]);
+          }
         } else {
-          const int grow = t.m0 + row;
-          const int gcol = t.n0 + c * 32;
-          if (grow < args.M) {
-            if constexpr (sizeof(OutT) == 2) {
-              __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.C) +
-                                   static_cast<int64_t>(grow) * args.ldc + gcol;
+          // the previous slice's TMA stores must have read the staging buffer
+          if (leader) bulk_wait_read_all();
+          named_barrier(1, 256);
+          // 128-byte-swizzled box `half` (64 columns x 128 rows): 16-byte chunk q
+          // of row `row` sits at chunk (q ^ (row % 8)).
+          uint8_t* box = out_stage + half * (128 * 128);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if (gcol + 8 * q < args.N) {
-                  uint4 v;
-                  v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-                  v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-                  v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-                  v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-                  reinterpret_cast<uint4*>(out)[q] = v;
-                }
-              }
-            } else {
-              float* out = reinterpret_cast<float*>(args.C) +
-                           static_cast<int64_t>(grow) * args.ldc + gcol;
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                if (gcol + 4 * q < args.N)
-                  reinterpret_cast<uint4*>(out)[q] =
-                      make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-            }
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = r[q >> 2] + (q & 3) * 8;
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
+            v.y = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
+            v.z = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
+            v.w = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
+            *reinterpret_cast<uint4*>(box + row * 128 + ((q ^ (row & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          named_barrier(1, 256);
+          if (leader && t.n0 + sl * 128 < args.N) {
+            const int x = t.n0 + sl * 128;
+            tma_store_2d(&tmC, out_stage, x, t.m0);
+            if (x + 64 < args.N) tma_store_2d(&tmC, out_stage + 128 * 128, x + 64, t.m0);
+            bulk_commit();
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+    }
+    if constexpr (STAGED) {
+      if (leader) bulk_wait_all();
     }
   }
 
