@@ -205,6 +205,37 @@ poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
  * launches; 0 restores the default (2 s). */
 void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
 
+/* Forward for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc or grow a memory pool at the point of use (for
+ * example code that runs while a CUDA graph is being captured, inference
+ * runtimes that own every byte of device memory in a fixed arena, or hosts
+ * whose allocator belongs to another framework).  It computes exactly what
+ * poetx_linear_fwd computes, with the same arguments except `workspace`:
+ * its scratch is a fixed, file-scope device array of
+ * POETX_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Limits and behaviour:
+ *   - Sizes whose poetx_workspace_size(desc, T) exceeds
+ *     POETX_NOALLOC_SCRATCH_BYTES are rejected with POETX_ERR_UNSUPPORTED
+ *     before any launch (use poetx_linear_fwd with your own workspace).
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.  The
+ *     first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call outside any stream capture.
+ *   - Every call on a device shares the same scratch and leaves its contents
+ *     behind; the forward writes every scratch byte it reads, so nothing
+ *     needs to start at zero.  Calls whose executions overlap on the GPU
+ *     (different streams without ordering between them) race on the scratch:
+ *     order them on one stream or with events.
+ *   - Other arguments, errors and precision are those of poetx_linear_fwd. */
+#define POETX_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* params,
+                                      const void* W0p, const void* X, int64_t T, void* Y,
+                                      void* saved_h, void* stream);
+
 /* Kernel classes reported by the profiling counters below. */
 enum {
   POETX_KIND_GEMM_FWD = 0,    /* h = v W0'^T on tcgen05 (forward and recompute)   */

@@ -28,7 +28,7 @@ __all__ = [
     "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count", "KIND_NAMES", "Layer",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "poetx_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 POETX_OK, POETX_ERR_INVALID_ARG, POETX_ERR_UNSUPPORTED = 0, 1, 2
@@ -43,7 +43,11 @@ EXPORTED_SYMBOLS = [
     "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
+    "poetx_linear_fwd_noalloc",
 ]
+
+# Size of the library's fixed forward scratch (POETX_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KIND_NAMES = ["gemm_fwd", "gemm_dgrad", "blockdiag", "gradred", "gather", "build", "genbwd",
               "merge", "simt"]
@@ -104,6 +108,7 @@ def _load():
                                      ctypes.POINTER(ctypes.c_double)]),
         "poetx_profile_kind_name": (ctypes.c_char_p, [I32]),
         "poetx_launch_count": (I64, []),
+        "poetx_linear_fwd_noalloc": (I32, [D, P, P, P, I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -190,6 +195,16 @@ def poetx_linear_bwd(desc, params, W0p, X, dY, saved_h, T, dX, dGenR, dGenP, acc
                                 _ptr(saved_h), T, _ptr(dX), _ptr(dGenR), _ptr(dGenP),
                                 int(accumulate), _ptr(workspace), _stream(stream)),
            "poetx_linear_bwd")
+
+
+def poetx_linear_fwd_noalloc(desc, params, W0p, X, T, Y, saved_h, stream=None):
+    """Forward without a workspace argument: the library's fixed device scratch
+    of NOALLOC_SCRATCH_BYTES serves as workspace, so the call allocates
+    nothing (for callers that cannot allocate device memory).  Calls that
+    overlap on the GPU share that scratch and race."""
+    _check(LIB.poetx_linear_fwd_noalloc(ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X), T,
+                                        _ptr(Y), _ptr(saved_h), _stream(stream)),
+           "poetx_linear_fwd_noalloc")
 
 
 def poetx_merge_workspace_size(desc) -> int:

@@ -1290,3 +1290,39 @@ const char* poetx_profile_kind_name(int32_t kind) {
 int64_t poetx_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free forward
+// Scratch for poetx_linear_fwd_noalloc: a fixed device array in this module.
+// In host code its name is only a host-side stand-in, so the device address
+// is looked up once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[POETX_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+extern "C" poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* params,
+                                                 const void* W0p, const void* X, int64_t T, void* Y,
+                                                 void* saved_h, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (T < 0) return POETX_ERR_INVALID_ARG;
+  if (T == 0) return POETX_OK;
+  const size_t need = poetx_workspace_size(desc, T);
+  if (need == 0 || need > POETX_NOALLOC_SCRATCH_BYTES) return POETX_ERR_UNSUPPORTED;
+  int dev = 0;
+  POETX_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return POETX_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* addr = nullptr;
+      POETX_CUDA(cudaGetSymbolAddress(&addr, g_noalloc_scratch));
+      g_noalloc_addr[dev] = addr;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, scratch, stream);
+}
