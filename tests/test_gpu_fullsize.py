@@ -1,0 +1,113 @@
+"""GPU parity at the workloads' full shapes and token counts (needs a B300).
+
+Each case runs one linear of a workload at its full size through the same
+C-ABI calls and launch configuration the benchmark times.  Outputs that the
+oracle can compute one by one are compared on sampled tokens: Y and dX rows
+depend only on the same rows of X and dY.  The generator gradients sum over
+every token, so they are checked two ways: against the oracle on the first
+2048 tokens at the same shapes (the same kernels and split logic at a token
+count the fp64 oracle finishes in seconds), and at full size by additivity
+over token shards (full-T gradient = gradient of the first half accumulated
+with that of the second half through the `accumulate` argument).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from tests.gpu_cases import rel_fro
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+T_SLICE = 2048
+
+CASES = [
+    # (workload, linear index, b)
+    ("llama60m_block", 4, 32),      # gate 512 -> 1376
+    ("llama60m_block", 6, 32),      # down 1376 -> 512
+    ("d1024_block", 5, 64),         # up 1024 -> 2816, recompute
+    ("d2048_block", 4, 128),        # gate 2048 -> 5632, stored h
+    ("d2048_block", 0, 256),        # q 2048 -> 2048, b = 256
+    ("d4096_ffn", 0, 512),          # up 4096 -> 11008, b = 512 (ragged 256 block), recompute
+    ("d4096_ffn", 1, 32),           # down 11008 -> 4096, b = 32, recompute
+]
+
+
+@pytest.fixture(scope="module")
+def px():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import orthogonal_equivalence_reparameterized_poetx_b300 as m
+    return m
+
+
+def _run(px, desc, params, W0p, X, dY, T, recompute, dgR, dgP, accumulate=False, want_out=True):
+    dev = "cuda"
+    m, n = desc.m, desc.n
+    dt = torch.bfloat16
+    ws = torch.empty(px.poetx_workspace_size(desc, T), dtype=torch.uint8, device=dev)
+    Y = torch.empty(T, m, dtype=dt, device=dev) if want_out else None
+    h = None if recompute else torch.empty(T, m, dtype=dt, device=dev)
+    dX = torch.empty(T, n, dtype=dt, device=dev) if want_out else None
+    if want_out or not recompute:
+        Yb = Y if Y is not None else torch.empty(T, m, dtype=dt, device=dev)
+        px.poetx_linear_fwd(desc, params, W0p, X, T, Yb, h, ws)
+    px.poetx_linear_bwd(desc, params, W0p, X, dY, h, T, dX, dgR, dgP, accumulate, ws)
+    return Y, dX
+
+
+@pytest.mark.parametrize("wkey,li,b", CASES)
+def test_full_size_linear(px, wkey, li, b):
+    wl = synth.WORKLOADS[wkey]
+    lin = wl.linears[li]
+    T, m, n = wl.tokens, lin.m, lin.n
+    lr, lp = O.packed_length(m, b), O.packed_length(n, b)
+    inp = synth.layer_inputs(lin, li, T, wl.dtype, lr, lp)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype=wl.dtype)
+    dev = "cuda"
+    params = torch.empty(px.poetx_params_size(desc), dtype=torch.uint8, device=dev)
+    W0p = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    genR, genP = inp.genR.to(dev), inp.genP.to(dev)
+    px.poetx_params_build(desc, genR, genP, params)
+    px.poetx_weight_premerge(desc, params, inp.W0.to(dev), W0p)
+    X, dY = inp.X.to(dev), inp.dY.to(dev)
+    dgR = torch.empty(lr, device=dev)
+    dgP = torch.empty(lp, device=dev)
+    Y, dX = _run(px, desc, params, W0p, X, dY, T, wl.recompute, dgR, dgP)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+
+    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P)
+    W0 = inp.W0.double().numpy()
+    gR, gP = inp.genR.double().numpy(), inp.genP.double().numpy()
+
+    # (1) sampled rows of Y and dX against the oracle row by row
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, T // 2, T - 129, T - 1],
+                                     np.random.default_rng(li).integers(0, T, 9)]))
+    Xs, dYs = inp.X[rows].double().numpy(), inp.dY[rows].double().numpy()
+    dX_o, _, _, ex = O.backward(spec, W0, Xs, dYs, gR, gP)
+    assert rel_fro(Y[rows].double().cpu().numpy(), ex["Y"]) <= TOL
+    assert rel_fro(dX[rows].double().cpu().numpy(), dX_o) <= TOL
+
+    # (2) generator gradients on the first T_SLICE tokens against the oracle
+    sR, sP = torch.empty_like(dgR), torch.empty_like(dgP)
+    _run(px, desc, params, W0p, X[:T_SLICE], dY[:T_SLICE], T_SLICE, wl.recompute, sR, sP,
+         want_out=False)
+    torch.cuda.synchronize()
+    _, dgR_o, dgP_o, _ = O.backward(spec, W0, inp.X[:T_SLICE].double().numpy(),
+                                    inp.dY[:T_SLICE].double().numpy(), gR, gP)
+    assert rel_fro(sR.double().cpu().numpy(), dgR_o) <= TOL
+    assert rel_fro(sP.double().cpu().numpy(), dgP_o) <= TOL
+
+    # (3) full-T gradients are additive over token shards
+    hR, hP = torch.empty_like(dgR), torch.empty_like(dgP)
+    half = (T // 2) // 128 * 128
+    _run(px, desc, params, W0p, X[:half], dY[:half], half, wl.recompute, hR, hP, want_out=False)
+    _run(px, desc, params, W0p, X[half:], dY[half:], T - half, wl.recompute, hR, hP,
+         accumulate=True, want_out=False)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+    assert rel_fro(hR.double().cpu().numpy(), dgR.double().cpu().numpy()) <= 1e-4
+    assert rel_fro(hP.double().cpu().numpy(), dgP.double().cpu().numpy()) <= 1e-4

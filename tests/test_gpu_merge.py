@@ -1,0 +1,81 @@
+"""GPU parity of the merge W0 <- R W0 P and of the weight pre-merge (needs a B300).
+
+The merge folds the current orthogonal factors into the base weight and
+re-expresses it under fresh permutations ("POET-X: Memory-efficient LLM
+Training by Scaling Orthogonal Transformation", Methodologie §1, the update
+W <- R_i W P_i).  Checked against the oracle's dense R W0 P, re-based under
+the new permutations, and by the invariance that defines it: with the
+generators reset to zero and the new seeds, the merged layer computes the
+same Y as the layer before the merge.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_cases import make_inputs, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": 1e-5, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def px():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import orthogonal_equivalence_reparameterized_poetx_b300 as m
+    return m
+
+
+@pytest.mark.parametrize("dtype,m,n,bR,bP,mode", [
+    ("fp32", 128, 96, 32, 32, "cayley"),
+    ("fp32", 200, 136, 64, 48, "cayley"),      # ragged blocks on both sides
+    ("bf16", 384, 256, 64, 64, "cayley"),
+    ("bf16", 768, 512, 512, 256, "cayley"),    # blocked builder, ragged R block
+    ("bf16", 256, 256, 128, 128, "neumann"),
+])
+def test_merge_matches_oracle_and_preserves_the_map(px, dtype, m, n, bR, bP, mode):
+    T = 200
+    inp = make_inputs(m, n, bR, bP, T, dtype, index=5, gstd=0.05)
+    desc = px.make_desc(m, n, bR, bP, inp.seed_R, inp.seed_P, dtype=dtype, mode=mode)
+    layer = px.Layer(desc, T)
+    layer.build(inp.genR.cuda(), inp.genP.cuda())
+    layer.premerge(inp.W0.cuda())
+    X = inp.X.cuda()
+    Y_old = torch.empty(T, m, dtype=layer.dtype, device="cuda")
+    layer.forward(X, Y_old)
+    new_R, new_P = 8101, 9102
+    layer.merge(new_R, new_P)
+    torch.cuda.synchronize()
+    W0p_new = layer.W0p.double().cpu().numpy()
+
+    spec = O.LayerSpec(m, n, bR, bP, inp.seed_R, inp.seed_P,
+                       "neumann" if mode == "neumann" else "exact", 3)
+    want = O.merge(spec, inp.W0.double().numpy(), inp.genR.double().numpy(),
+                   inp.genP.double().numpy(), new_R, new_P)
+    assert rel_fro(W0p_new, want) <= TOL[dtype]
+
+    # the merged layer with zero generators under the new seeds computes the same map
+    d2 = px.make_desc(m, n, bR, bP, new_R, new_P, dtype=dtype, mode=mode)
+    l2 = px.Layer(d2, T)
+    l2.build(torch.zeros_like(inp.genR).cuda(), torch.zeros_like(inp.genP).cuda())
+    l2.W0p.copy_(layer.W0p)
+    Y_new = torch.empty(T, m, dtype=layer.dtype, device="cuda")
+    l2.forward(X, Y_new)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+    assert rel_fro(Y_new.double().cpu().numpy(), Y_old.double().cpu().numpy()) <= TOL[dtype]
+
+
+def test_premerge_is_an_exact_permutation_copy(px):
+    m, n = 1376, 512
+    inp = make_inputs(m, n, 32, 32, 1, "bf16", index=6)
+    desc = px.make_desc(m, n, 32, 32, inp.seed_R, inp.seed_P, dtype="bf16")
+    layer = px.Layer(desc, 1)
+    layer.build(inp.genR.cuda(), inp.genP.cuda())
+    layer.premerge(inp.W0.cuda())
+    torch.cuda.synchronize()
+    piR, piP = O.permutation(inp.seed_R, m), O.permutation(inp.seed_P, n)
+    want = inp.W0.float().numpy()[piR][:, piP]
+    assert np.array_equal(layer.W0p.float().cpu().numpy(), want)
