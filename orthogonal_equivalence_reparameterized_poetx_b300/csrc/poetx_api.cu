@@ -574,7 +574,7 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
     POETX_TRY(launch_cayley_blocks(st, d, cayley_side(d, S, gen, params), nullptr));
     return POETX_OK;
   }
-  unpack_kernel<<<nb, 256, 0, st>>>(gen, S.g, Q, M);
+  unpack_kernel<<<dim3(nb, (b + 7) / 8), 256, 0, st>>>(gen, S.g, Q, M);
   POETX_LAUNCHED();
   if (d.mode == POETX_MODE_CAYLEY) {
     {
@@ -690,7 +690,7 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
     }
     GQ = cur;
   }
-  pack_grad_kernel<<<nb, 256, 0, st>>>(GQ, S.g, dGen, accumulate);
+  pack_grad_kernel<<<dim3(nb, (b + 7) / 8), 256, 0, st>>>(GQ, S.g, dGen, accumulate);
   POETX_LAUNCHED();
   return POETX_OK;
 }

@@ -238,23 +238,29 @@ __device__ __forceinline__ int block_size(const SideGeom& s, int k) {
   return (k == s.nblk - 1) ? s.last : s.b;
 }
 
-// Unpacks the strict upper triangle of block k into Q (b x b, zero padded
-// beyond the block's size) and writes A = I - Q (identity on the padding).
+// Unpacks the strict upper triangle of block k = blockIdx.x into Q (b x b,
+// zero padded beyond the block's size) and writes A = I - Q (identity on the
+// padding).  One warp per row i (grid.y covers rows 8 at a time); entry
+// (i, j), i < j, of a block of size sz sits at i*sz - i(i+1)/2 + (j-i-1).
 __global__ void __launch_bounds__(256) unpack_kernel(const float* __restrict__ gen, SideGeom s,
                                                      float* __restrict__ Q, float* __restrict__ A) {
   const int k = blockIdx.x;
+  const int i = blockIdx.y * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (i >= s.b) return;
   const int sz = block_size(s, k);
-  const int64_t off = static_cast<int64_t>(k) * s.b * (s.b - 1) / 2;
-  const int64_t bb = static_cast<int64_t>(s.b) * s.b;
-  for (int e = threadIdx.x; e < s.b * s.b; e += blockDim.x) {
-    const int i = e / s.b, j = e % s.b;
+  const float* g = gen + static_cast<int64_t>(k) * s.b * (s.b - 1) / 2;
+  float* Qr = Q + (static_cast<int64_t>(k) * s.b + i) * s.b;
+  float* Ar = A ? A + (static_cast<int64_t>(k) * s.b + i) * s.b : nullptr;
+  const int row_base = i * sz - i * (i + 1) / 2 - i - 1;  // + j for j > i
+  for (int j = lane; j < s.b; j += 32) {
     float q = 0.f;
-    if (i < sz && j < sz && i != j) {
-      if (i < j) q = gen[off + static_cast<int64_t>(i) * sz - i * (i + 1) / 2 + (j - i - 1)];
-      else q = -gen[off + static_cast<int64_t>(j) * sz - j * (j + 1) / 2 + (i - j - 1)];
+    if (i < sz && j < sz) {
+      if (i < j) q = g[row_base + j];
+      else if (j < i) q = -g[j * sz - j * (j + 1) / 2 - j - 1 + i];
     }
-    Q[k * bb + e] = q;
-    if (A) A[k * bb + e] = (i == j ? 1.f : 0.f) - q;
+    Qr[j] = q;
+    if (Ar) Ar[j] = (i == j ? 1.f : 0.f) - q;
   }
 }
 
@@ -312,6 +318,104 @@ __device__ __forceinline__ void gj_register_invert(float (&a)[kGjMaxRows], const
   }
 }
 
+__device__ __forceinline__ float sel4(const float (&v)[4], int q) {
+  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
+}
+
+// Same inversion with pivots taken four at a time (P % 4 == 0).  For the
+// panel K = {k0..k0+3} with pivot block D = A_KK:
+//   A_ij -= (A_iK D^-1) A_Kj     (i, j outside K)
+//   A_Kj  = D^-1 A_Kj,  A_iK = -A_iK D^-1,  A_KK = D^-1.
+// D's symmetric part stays >= I (Schur complements of I - Q), so its
+// unpivoted inverse is well conditioned.  Each round: every thread inverts
+// D in registers, 128 threads form c_i = A_iK D^-1, and each element takes a
+// rank-4 update (one 16-byte shared load, four FMAs); two barriers per four
+// pivots.  `sm` holds 2560 floats.
+template <int PT>
+__device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], const GjShape<PT>& sh,
+                                                    int tx, int ty, float* sm) {
+  const int P = sh.P, R = sh.R, NR = sh.NR;
+  float* rowK0 = sm;          // [2][4][128]: panel rows A_Kj
+  float* colK0 = sm + 1024;   // [2][128][4]: panel columns A_iK
+  float* cK = sm + 2048;      // [128][4]: c_i = A_iK D^-1
+#pragma unroll
+  for (int r = 0; r < kGjMaxRows; ++r) {
+    const int i = ty + R * r;
+    if (r < NR && i < P) {
+      if (i < 4) rowK0[i * 128 + tx] = a[r];
+      if (tx < 4) colK0[i * 4 + tx] = a[r];
+    }
+  }
+  __syncthreads();
+  for (int k0 = 0, buf = 0; k0 < P; k0 += 4, buf ^= 1) {
+    const float* rk = rowK0 + buf * 512;
+    const float* ck = colK0 + buf * 512;
+    float D[4][4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) D[p][q] = rk[p * 128 + k0 + q];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {  // in-place unpivoted Gauss-Jordan on the 4 x 4 block
+      const float pv = 1.0f / D[p][p];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) D[p][q] = (q == p) ? pv : D[p][q] * pv;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i == p) continue;
+        const float f = D[i][p];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) D[i][q] = (q == p) ? -f * pv : fmaf(-f, D[p][q], D[i][q]);
+      }
+    }
+    if (ty == 0) {
+      const float4 ai = *reinterpret_cast<const float4*>(ck + tx * 4);
+      float4 c;
+      c.x = ai.x * D[0][0] + ai.y * D[1][0] + ai.z * D[2][0] + ai.w * D[3][0];
+      c.y = ai.x * D[0][1] + ai.y * D[1][1] + ai.z * D[2][1] + ai.w * D[3][1];
+      c.z = ai.x * D[0][2] + ai.y * D[1][2] + ai.z * D[2][2] + ai.w * D[3][2];
+      c.w = ai.x * D[0][3] + ai.y * D[1][3] + ai.z * D[2][3] + ai.w * D[3][3];
+      *reinterpret_cast<float4*>(cK + tx * 4) = c;
+    }
+    const float rj[4] = {rk[tx], rk[128 + tx], rk[256 + tx], rk[384 + tx]};
+    const int qj = tx - k0;
+    const bool colK = (qj >= 0 && qj < 4);
+    float nr[4], dcol[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      nr[q] = D[q][0] * rj[0] + D[q][1] * rj[1] + D[q][2] * rj[2] + D[q][3] * rj[3];
+      dcol[q] = sel4(D[q], qj & 3);
+    }
+    __syncthreads();  // cK ready
+    const int k1 = k0 + 4;
+    float* rkn = rowK0 + (buf ^ 1) * 512;
+    float* ckn = colK0 + (buf ^ 1) * 512;
+    const int qj1 = tx - k1;
+    const bool colK1 = (k1 < P) && (qj1 >= 0 && qj1 < 4);
+#pragma unroll
+    for (int r = 0; r < kGjMaxRows; ++r) {
+      const int i = ty + R * r;
+      if (r < NR && i < P) {
+        const int qi = i - k0;
+        float v;
+        if (qi >= 0 && qi < 4) {
+          v = colK ? sel4(dcol, qi) : sel4(nr, qi);
+        } else if (colK) {
+          v = -cK[i * 4 + qj];
+        } else {
+          const float4 c = *reinterpret_cast<const float4*>(cK + i * 4);
+          v = fmaf(-c.x, rj[0], fmaf(-c.y, rj[1], fmaf(-c.z, rj[2], fmaf(-c.w, rj[3], a[r]))));
+        }
+        a[r] = v;
+        const int qi1 = i - k1;
+        if (k1 < P && qi1 >= 0 && qi1 < 4) rkn[qi1 * 128 + tx] = v;
+        if (colK1) ckn[i * 4 + qj1] = v;
+      }
+    }
+    __syncthreads();  // next panel published; cK free
+  }
+}
+
 // Exact Cayley blocks for b <= 128, one CTA per block: unpack the packed
 // generator into A = I - Q (identity on the padding of a ragged block),
 // invert it in registers (M = (I - Q)^-1), and write M, B = 2M - I, Q and,
@@ -344,6 +448,7 @@ __global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide fir
   __nv_bfloat16* __restrict__ Bsb = cs.Bsb;
   __nv_bfloat16* __restrict__ BsbT = cs.BsbT;
   __shared__ float rowbuf[256], colbuf[256];
+  __shared__ __align__(16) float gj4_sm[2560];
   extern __shared__ float bsm[];  // P x (P + 1) staging of B for the transposed writes
   const GjShape<PT> sh(s.b);
   const int P = sh.P, R = sh.R, NR = sh.NR;
@@ -368,7 +473,8 @@ __global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide fir
     }
     a[r] = (i == j ? 1.f : 0.f) - q;
   }
-  gj_register_invert<PT>(a, sh, tx, ty, rowbuf, colbuf);
+  if (P % 4 == 0) gj_register_invert4<PT>(a, sh, tx, ty, gj4_sm);
+  else gj_register_invert<PT>(a, sh, tx, ty, rowbuf, colbuf);
 #pragma unroll
   for (int r = 0; r < kGjMaxRows; ++r) {
     const int i = ty + R * r;
@@ -403,14 +509,14 @@ __global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide fir
 // in + z*in_bs with leading dimension in_ld, written to out likewise.
 __global__ void __launch_bounds__(1024) gj_invert128_kernel(const float* in, int64_t in_bs, int in_ld,
                                                             float* out, int64_t out_bs, int out_ld) {
-  __shared__ float rowbuf[256], colbuf[256];
+  __shared__ __align__(16) float gj4_sm[2560];
   const GjShape<128> sh(128);
   const int tx = threadIdx.x % 128, ty = threadIdx.x / 128;
   const float* src = in + blockIdx.x * in_bs;
   float a[kGjMaxRows];
 #pragma unroll
   for (int r = 0; r < kGjMaxRows; ++r) a[r] = src[static_cast<int64_t>(ty + 8 * r) * in_ld + tx];
-  gj_register_invert<128>(a, sh, tx, ty, rowbuf, colbuf);
+  gj_register_invert4<128>(a, sh, tx, ty, gj4_sm);
   float* dst = out + blockIdx.x * out_bs;
 #pragma unroll
   for (int r = 0; r < kGjMaxRows; ++r) dst[static_cast<int64_t>(ty + 8 * r) * out_ld + tx] = a[r];
@@ -486,23 +592,22 @@ __global__ void __launch_bounds__(256) gradred_reduce_kernel(const float* __rest
   }
 }
 
-// Packed generator gradient: g[(i,j)] (+)= GQ[k](i,j) - GQ[k](j,i), i < j < size.
+// Packed generator gradient: g[(i,j)] (+)= GQ[k](i,j) - GQ[k](j,i), i < j < size,
+// for block k = blockIdx.x; one warp per row i (grid.y covers rows 8 at a
+// time), consecutive lanes on consecutive packed entries.
 __global__ void __launch_bounds__(256) pack_grad_kernel(const float* __restrict__ GQ, SideGeom s,
                                                         float* __restrict__ out, int accumulate) {
   const int k = blockIdx.x;
+  const int i = blockIdx.y * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
   const int sz = block_size(s, k);
-  const int64_t off = static_cast<int64_t>(k) * s.b * (s.b - 1) / 2;
-  const int64_t bb = static_cast<int64_t>(s.b) * s.b;
-  const int npairs = sz * (sz - 1) / 2;
-  for (int e = threadIdx.x; e < npairs; e += blockDim.x) {
-    // invert e = i*sz - i(i+1)/2 + (j-i-1): walk rows (sz <= 512, cheap)
-    int i = 0, rem = e;
-    while (rem >= sz - 1 - i) rem -= sz - 1 - i, ++i;
-    const int j = i + 1 + rem;
-    const float v = GQ[k * bb + static_cast<int64_t>(i) * s.b + j] -
-                    GQ[k * bb + static_cast<int64_t>(j) * s.b + i];
-    if (accumulate) out[off + e] += v;
-    else out[off + e] = v;
+  if (i >= sz - 1) return;
+  const float* G = GQ + static_cast<int64_t>(k) * s.b * s.b;
+  float* o = out + static_cast<int64_t>(k) * s.b * (s.b - 1) / 2 + (i * sz - i * (i + 1) / 2 - i - 1);
+  for (int j = i + 1 + lane; j < sz; j += 32) {
+    const float v = G[i * s.b + j] - G[j * s.b + i];
+    if (accumulate) o[j] += v;
+    else o[j] = v;
   }
 }
 
