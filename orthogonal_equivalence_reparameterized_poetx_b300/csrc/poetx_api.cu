@@ -185,9 +185,10 @@ ParamsLayout params_layout(const poetx_layer_desc& d) {
   return L;
 }
 
-// GradRed token splits: about four waves of tiles over the SMs, each split a
-// multiple of 64 tokens; the split count is recomputed from the rounded chunk
-// so that every split holds at least one token.
+// GradRed token splits: the smallest split count whose tiles keep at least 95%
+// of one wave's SMs busy (few partials to reduce), each split a multiple of 64
+// tokens; the count is recomputed from the rounded chunk so that every split
+// holds at least one token.
 struct Splits {
   int splits, chunk;
 };
@@ -196,8 +197,17 @@ Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
   const int tps = S.sb / 128;
   const int per_split = S.nsb * tps * tps;
   const int64_t Tc = std::max<int64_t>(T, 1);
-  int64_t target = (4 * nsm + per_split - 1) / per_split;
-  target = std::max<int64_t>(1, std::min<int64_t>(target, (Tc + 63) / 64));
+  const int64_t smax = std::max<int64_t>(1, std::min<int64_t>((4 * nsm + per_split - 1) / per_split,
+                                                              (Tc + 63) / 64));
+  int64_t target = smax;
+  for (int64_t sp = 1; sp <= smax; ++sp) {
+    const int64_t tiles = sp * per_split;
+    const int64_t rounds = (tiles + nsm - 1) / nsm;
+    if (tiles * 100 >= 95 * rounds * nsm) {
+      target = sp;
+      break;
+    }
+  }
   const int64_t per = (Tc + target - 1) / target;
   const int64_t chunk = (per + 63) / 64 * 64;
   const int64_t splits = (Tc + chunk - 1) / chunk;
@@ -846,16 +856,52 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   return POETX_OK;
 }
 
+bool fused_cayley_bwd_ok(const poetx_layer_desc& d, int b) {
+  return d.dtype == POETX_DTYPE_BF16 && d.mode == POETX_MODE_CAYLEY && (b == 32 || b == 64 || b == 128);
+}
+
+// Fused reduction + Cayley backward + packing for one side (see cayley_bwd_kernel).
+poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_t* params,
+                              const float* partial, int splits, float* dGen, int accumulate) {
+  ProfScope prof(POETX_KIND_GENBWD, st);
+  const int b = S.g.b;
+  const size_t smem = 3 * static_cast<size_t>(b) * (b + 4) * 4;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(cayley_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         3 * 128 * 132 * 4);
+    cudaFuncSetAttribute(cayley_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         3 * 64 * 68 * 4);
+  });
+  const float* M = reinterpret_cast<const float*>(params + S.off_M);
+  const int64_t stride = static_cast<int64_t>(S.nsb) * S.sb * S.sb;
+  auto kern = b == 128 ? cayley_bwd_kernel<128> : b == 64 ? cayley_bwd_kernel<64> : cayley_bwd_kernel<32>;
+  const int threads = (b / 4) * (b / 4);
+  kern<<<S.g.nblk, threads, smem, st>>>(partial, stride, splits, S.g, S.sb, M, dGen, accumulate);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accumulate) {
   float* GR = c.w<float>(c.W.off_GR);
   float* GP = c.w<float>(c.W.off_GP);
   float* t1 = c.w<float>(c.W.off_t1);
   float* t2 = c.w<float>(c.W.off_t2);
   float* nsc = c.w<float>(c.W.off_nsc);
-  if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0)
-    POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
-  if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0)
-    POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
+  if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0) {
+    if (fused_cayley_bwd_ok(c.d, c.d.b_R))
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.W.splitsR, dGenR,
+                                 accumulate));
+    else
+      POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
+  }
+  if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0) {
+    if (fused_cayley_bwd_ok(c.d, c.d.b_P))
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.W.splitsP, dGenP,
+                                 accumulate));
+    else
+      POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
+  }
   return POETX_OK;
 }
 
@@ -923,12 +969,20 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   POETX_TRY(tc_blockdiag(c.st, dv, c.p<__nv_bfloat16>(P.off_BsbT), du, T, n, P.sb, P.nsb));
   if (dX) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
   ProfScope prof(POETX_KIND_GENBWD, c.st);
-  gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
-      partR, static_cast<int64_t>(R.nsb) * R.sb * R.sb, c.W.splitsR, R.g, R.sb, c.w<float>(c.W.off_GR));
-  POETX_LAUNCHED();
-  gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0, c.st>>>(
-      partP, static_cast<int64_t>(P.nsb) * P.sb * P.sb, c.W.splitsP, P.g, P.sb, c.w<float>(c.W.off_GP));
-  POETX_LAUNCHED();
+  // exact Cayley blocks of b <= 128: the generator backward runs fused per block
+  // in bwd_common_tail; otherwise reduce the partials into G here.
+  if (!fused_cayley_bwd_ok(c.d, R.g.b)) {
+    gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
+        partR, static_cast<int64_t>(R.nsb) * R.sb * R.sb, c.W.splitsR, R.g, R.sb,
+        c.w<float>(c.W.off_GR));
+    POETX_LAUNCHED();
+  }
+  if (!fused_cayley_bwd_ok(c.d, P.g.b)) {
+    gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0, c.st>>>(
+        partP, static_cast<int64_t>(P.nsb) * P.sb * P.sb, c.W.splitsP, P.g, P.sb,
+        c.w<float>(c.W.off_GP));
+    POETX_LAUNCHED();
+  }
   return POETX_OK;
 }
 

@@ -169,16 +169,33 @@ __global__ void __launch_bounds__(256) gather_cols_bf16x2_kernel(const uint4* __
   for (int64_t r0 = blockIdx.x * rows_per_iter; r0 < rows; r0 += gridDim.x * rows_per_iter) {
     const int nr = static_cast<int>(min(rows_per_iter, rows - r0));
     const int np = (nr + 1) / 2;
-    for (int v = threadIdx.x; v < np * vpr; v += blockDim.x) {
-      const int p = v / vpr, c = v % vpr;
-      const int64_t ra = r0 + 2 * p;
-      const uint4 a = in[ra * vpr + c];
-      const uint4 b = (2 * p + 1 < nr) ? in[(ra + 1) * vpr + c] : make_uint4(0, 0, 0, 0);
-      uint4* dst = reinterpret_cast<uint4*>(w + static_cast<int64_t>(p) * d + 8 * c);
-      dst[0] = make_uint4(__byte_perm(a.x, b.x, 0x5410), __byte_perm(a.x, b.x, 0x7632),
-                          __byte_perm(a.y, b.y, 0x5410), __byte_perm(a.y, b.y, 0x7632));
-      dst[1] = make_uint4(__byte_perm(a.z, b.z, 0x5410), __byte_perm(a.z, b.z, 0x7632),
-                          __byte_perm(a.w, b.w, 0x5410), __byte_perm(a.w, b.w, 0x7632));
+    // four iterations' loads in flight before any shared-memory store
+    const int total = np * vpr;
+    for (int v0 = threadIdx.x; v0 < total; v0 += 4 * blockDim.x) {
+      uint4 a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        a[u] = b[u] = make_uint4(0, 0, 0, 0);
+        if (v < total) {
+          const int p = v / vpr, c = v - p * vpr;
+          const int64_t ra = r0 + 2 * p;
+          a[u] = in[ra * vpr + c];
+          if (2 * p + 1 < nr) b[u] = in[(ra + 1) * vpr + c];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < total) {
+          const int p = v / vpr, c = v - p * vpr;
+          uint4* dst = reinterpret_cast<uint4*>(w + static_cast<int64_t>(p) * d + 8 * c);
+          dst[0] = make_uint4(__byte_perm(a[u].x, b[u].x, 0x5410), __byte_perm(a[u].x, b[u].x, 0x7632),
+                              __byte_perm(a[u].y, b[u].y, 0x5410), __byte_perm(a[u].y, b[u].y, 0x7632));
+          dst[1] = make_uint4(__byte_perm(a[u].z, b[u].z, 0x5410), __byte_perm(a[u].z, b[u].z, 0x7632),
+                              __byte_perm(a[u].w, b[u].w, 0x5410), __byte_perm(a[u].w, b[u].w, 0x7632));
+        }
+      }
     }
     __syncthreads();
     for (int c = threadIdx.x; c < vpr; c += blockDim.x) {
@@ -608,6 +625,97 @@ __global__ void __launch_bounds__(256) pack_grad_kernel(const float* __restrict_
     const float v = G[i * s.b + j] - G[j * s.b + i];
     if (accumulate) o[j] += v;
     else o[j] = v;
+  }
+}
+
+// Cayley backward of one block per CTA (b = P in {32, 64, 128}, bf16 path), fused:
+//   G   = sum over token splits of the reduction partials (fixed order);
+//   GQ  = 2 M^T G M^T with M = (I - Q)^-1;
+//   g_ij (+)= GQ[i][j] - GQ[j][i] packed row by row (i < j < size).
+// (P/4)^2 threads, each owning a 4 x 4 tile of the products; matrices live in
+// shared memory with rows padded to P + 4 floats so 16-byte loads stay
+// aligned.  The second product reads T^T and M^T so both operands are
+// contiguous along the loop.
+template <int P>
+__global__ void __launch_bounds__((P / 4) * (P / 4)) cayley_bwd_kernel(
+    const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s, int sb,
+    const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
+  constexpr int LD = P + 4;
+  constexpr int NT = (P / 4) * (P / 4);
+  extern __shared__ __align__(16) float cbs[];
+  float* Gs = cbs;             // G, then T^T
+  float* Ms = cbs + P * LD;    // M, then GQ
+  float* Mt = Ms + P * LD;     // M^T
+  const int k = blockIdx.x;
+  const float* Mk = Mall + static_cast<int64_t>(k) * P * P;
+  for (int e = threadIdx.x; e < P * P; e += NT) {
+    const int i = e / P, j = e % P;
+    const int a = k * P + i, c = k * P + j;   // features of this block
+    const int sbi = a / sb;
+    const int64_t off = static_cast<int64_t>(sbi) * sb * sb +
+                        static_cast<int64_t>(a - sbi * sb) * sb + (c - sbi * sb);
+    float v = 0.f;
+    for (int p = 0; p < splits; ++p) v += partial[p * split_stride + off];
+    Gs[i * LD + j] = v;
+    const float m = Mk[e];
+    Ms[i * LD + j] = m;
+    Mt[j * LD + i] = m;
+  }
+  __syncthreads();
+  const int tr = threadIdx.x / (P / 4), tc = threadIdx.x % (P / 4);
+  float acc[4][4];
+  // T = M^T G: T[i][j] = sum_q M[q][i] G[q][j]
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < P; ++q) {
+    const float4 a = *reinterpret_cast<const float4*>(Ms + q * LD + 4 * tr);
+    const float4 g = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
+    const float av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], gv[y], acc[x][y]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) Gs[(4 * tc + y) * LD + 4 * tr + x] = acc[x][y];  // T^T
+  __syncthreads();
+  // GQ = 2 T M^T: GQ[i][j] = 2 sum_q T^T[q][i] M^T[q][j]
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < P; ++q) {
+    const float4 t = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tr);
+    const float4 m = *reinterpret_cast<const float4*>(Mt + q * LD + 4 * tc);
+    const float tv[4] = {t.x, t.y, t.z, t.w}, mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mv[y], acc[x][y]);
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    *reinterpret_cast<float4*>(Ms + (4 * tr + x) * LD + 4 * tc) =
+        make_float4(2.f * acc[x][0], 2.f * acc[x][1], 2.f * acc[x][2], 2.f * acc[x][3]);
+  __syncthreads();
+  // pack: one warp per row
+  const int sz = block_size(s, k);
+  float* o = out + static_cast<int64_t>(k) * P * (P - 1) / 2;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = NT / 32;
+  for (int i = warp; i < sz - 1; i += nwarps) {
+    float* oi = o + (i * sz - i * (i + 1) / 2 - i - 1);
+    for (int j = i + 1 + lane; j < sz; j += 32) {
+      const float v = Ms[i * LD + j] - Ms[j * LD + i];
+      if (accumulate) oi[j] += v;
+      else oi[j] = v;
+    }
   }
 }
 
