@@ -236,6 +236,24 @@ poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* 
                                       const void* W0p, const void* X, int64_t T, void* Y,
                                       void* saved_h, void* stream);
 
+/* Pipelined schedule of the bf16 forward and backward.  With T >=
+ * min_tokens the library splits the tokens into `chunks` (2..4) and runs the
+ * GEMM of one chunk on a partition of `*_gemm_sms` SMs while the gathers,
+ * block transforms and token reductions of neighbouring chunks run on the
+ * remaining SMs (two CUDA green contexts with their own streams, ordered
+ * with events against the caller's stream).  The results are those of the
+ * sequential schedule: the same kernels on disjoint token ranges.
+ * chunks <= 1 disables the pipeline (the default); 0 for an SM count or
+ * min_tokens keeps its current value.  Applies to calls made after it, on
+ * every device. */
+void poetx_set_pipeline(int32_t chunks, int32_t fwd_gemm_sms, int32_t bwd_gemm_sms,
+                        int64_t min_tokens);
+
+/* 1 if the pipelined schedule is enabled and the current device can be
+ * partitioned (green contexts available), else 0.  May create the green
+ * contexts on first use. */
+int32_t poetx_pipeline_active(void);
+
 /* Kernel classes reported by the profiling counters below. */
 enum {
   POETX_KIND_GEMM_FWD = 0,    /* h = v W0'^T on tcgen05 (forward and recompute)   */

@@ -232,6 +232,30 @@ int device_sm_count() {
   return nsm;
 }
 
+// SMs that launches from this host thread may use: the whole device, or the
+// size of the green-context partition the current pipeline stage runs in.
+thread_local int t_cta_budget = 0;
+int launch_sms() { return t_cta_budget > 0 ? t_cta_budget : device_sm_count(); }
+
+struct CtaBudget {
+  int prev;
+  explicit CtaBudget(int n) : prev(t_cta_budget) { t_cta_budget = n; }
+  ~CtaBudget() { t_cta_budget = prev; }
+};
+
+// Most token chunks a pipelined forward or backward uses.
+constexpr int kMaxChunks = 4;
+
+// Upper bound on reduction partial slots for T tokens split into at most
+// kMaxChunks chunks, whatever SM budget each chunk runs under.
+int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
+  const int tps = S.sb / 128;
+  const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
+  const int64_t smax = std::max<int64_t>(
+      1, std::min<int64_t>((4 * device_sm_count() + per_split - 1) / per_split, (T + 63) / 64));
+  return smax * kMaxChunks;
+}
+
 WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t T, int nsm) {
   WorkLayout W{};
   const size_t e = d.dtype == POETX_DTYPE_BF16 ? 2 : 4;
@@ -244,8 +268,9 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   W.off_m3 = off; off = align_up(off + tm);
   W.splitsR = W.splitsP = 0;
   if (d.dtype == POETX_DTYPE_BF16) {
-    W.splitsR = gradred_splits(P.R, T, nsm).splits;
-    W.splitsP = gradred_splits(P.P, T, nsm).splits;
+    (void)nsm;
+    W.splitsR = static_cast<int>(partial_slots_bound(P.R, T));
+    W.splitsP = static_cast<int>(partial_slots_bound(P.P, T));
     W.off_partR = off;
     off = align_up(off + static_cast<size_t>(W.splitsR) * P.R.nsb * P.R.sb * P.R.sb * 4);
     W.off_partP = off;
@@ -337,7 +362,7 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
   if (rows <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_GATHER, st);
   if ((static_cast<size_t>(d) * sizeof(T)) % 16 != 0) {
-    const int grid = static_cast<int>(std::min<int64_t>(rows, device_sm_count() * 8));
+    const int grid = static_cast<int>(std::min<int64_t>(rows, launch_sms() * 8));
     gather_cols_scalar_kernel<T><<<grid, 256, 0, st>>>(in, out, idx, rows, d);
     POETX_LAUNCHED();
     return POETX_OK;
@@ -356,7 +381,7 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
       if (smem > 200 * 1024) return POETX_ERR_UNSUPPORTED;
     }
     const int64_t iters = (rows + 2 * ppi - 1) / (2 * ppi);
-    const int grid = static_cast<int>(std::min<int64_t>(iters, device_sm_count() * 8));
+    const int grid = static_cast<int>(std::min<int64_t>(iters, launch_sms() * 6));
     gather_cols_bf16x2_kernel<<<grid, 256, smem, st>>>(reinterpret_cast<const uint4*>(in),
                                                        reinterpret_cast<uint4*>(out), idx, rows, d,
                                                        ppi);
@@ -375,7 +400,7 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
     if (smem > 200 * 1024) return POETX_ERR_UNSUPPORTED;
   }
   const int64_t iters = (rows + rpi - 1) / rpi;
-  const int grid = static_cast<int>(std::min<int64_t>(iters, device_sm_count() * 8));
+  const int grid = static_cast<int>(std::min<int64_t>(iters, launch_sms() * 8));
   gather_cols_kernel<T><<<grid, 256, smem, st>>>(in, out, idx, rows, d, rpi);
   POETX_LAUNCHED();
   return POETX_OK;
@@ -432,7 +457,7 @@ poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap
   });
   if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
   args.timeout_ns = g_timeout_ns;
-  const int grid = std::min(args.num_tiles, device_sm_count());
+  const int grid = std::min(args.num_tiles, launch_sms());
   kern<<<grid, 320, smem, st>>>(ta, tb, tc, args);
   POETX_LAUNCHED();
   return POETX_OK;
@@ -504,10 +529,12 @@ poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void
 }
 
 // partial[p][s] = sum_{t in split p} A[t, s]^T B[t, s] (fp32, sb x sb per super-block).
+// Writes sp.splits partial slots starting at `partial` and adds that count to
+// *slots (the caller appends the next call's slots after them).
 poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, const void* B,
-                        float* partial, int64_t T, int expected_splits) {
-  const Splits sp = gradred_splits(S, T, device_sm_count());
-  if (sp.splits != expected_splits) return POETX_ERR_INVALID_ARG;
+                        float* partial, int64_t T, int* slots) {
+  const Splits sp = gradred_splits(S, T, launch_sms());
+  *slots += sp.splits;
   ProfScope prof(POETX_KIND_GRADRED, st);
   const int d = S.g.d, sb = S.sb, nsb = S.nsb;
   CUtensorMap ta, tb;
@@ -820,6 +847,8 @@ struct Ctx {
   const int32_t* piPinv() const { return reinterpret_cast<const int32_t*>(params + L.off_piPinv); }
   template <typename T> T* w(size_t off) const { return reinterpret_cast<T*>(ws + off); }
   template <typename T> const T* p(size_t off) const { return reinterpret_cast<const T*>(params + off); }
+  // reduction partial slots written by the backward (bf16 path)
+  mutable int slotsR = 0, slotsP = 0;
 };
 
 poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs) {
@@ -840,6 +869,167 @@ poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T,
   return POETX_OK;
 }
 
+// ------------------------------------------------------------------ green-context pipeline
+// The bf16 forward and backward can run as a software pipeline over token
+// chunks on two disjoint SM partitions (CUDA green contexts): the GEMM stages
+// of chunk k on one partition while the memory-bound stages (gathers, block
+// transforms, token reductions) of neighbouring chunks run on the other.
+// Stages are ordered by events; the first and last memory stages use the
+// whole device on the caller's stream.  Every stage is the same kernel as in
+// the sequential schedule, on disjoint token ranges of the same buffers.
+
+typedef CUresult (*PFN_cuDeviceGet_t)(CUdevice*, int);
+typedef CUresult (*PFN_cuDeviceGetDevResource_t)(CUdevice, CUdevResource*, CUdevResourceType);
+typedef CUresult (*PFN_cuDevSmResourceSplitByCount_t)(CUdevResource*, unsigned int*,
+                                                     const CUdevResource*, CUdevResource*,
+                                                     unsigned int, unsigned int);
+typedef CUresult (*PFN_cuDevResourceGenerateDesc_t)(CUdevResourceDesc*, CUdevResource*, unsigned int);
+typedef CUresult (*PFN_cuGreenCtxCreate_t)(CUgreenCtx*, CUdevResourceDesc, CUdevice, unsigned int);
+typedef CUresult (*PFN_cuGreenCtxStreamCreate_t)(CUstream*, CUgreenCtx, unsigned int, int);
+
+// Off by default: measured on B300 at d = 2048 and d = 4096 the partitioned
+// schedule is slower than the sequential one (the gathers and block
+// transforms are bound by per-SM throughput, so they slow down in proportion
+// to the SMs they lose, as do the GEMMs).
+struct PipeCfg {
+  int chunks = 1;          // token chunks (1 disables the pipeline)
+  int fwd_gemm_sms = 112;  // SMs of the GEMM partition in the forward
+  int bwd_gemm_sms = 72;   // and in the backward
+  int64_t min_tokens = 8192;
+};
+PipeCfg g_pipe;
+std::mutex g_pipe_mu;
+
+struct GreenPart {
+  bool ok = false;
+  int ng = 0, nm = 0;
+  cudaStream_t sg = nullptr, sm = nullptr;
+};
+
+template <typename F>
+bool driver_fn(const char* name, F* out) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, CUDART_VERSION, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p)
+    return false;
+  *out = reinterpret_cast<F>(p);
+  return true;
+}
+
+// Two green contexts on the current device: `ng` SMs for GEMMs and the rest
+// for memory-bound stages, each with a non-blocking stream.  Cached per
+// (device, ng); ok == false if the driver cannot partition.
+GreenPart green_partition(int ng) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<int, int>, GreenPart>> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GreenPart{};
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& e : cache)
+    if (e.first.first == dev && e.first.second == ng) return e.second;
+  GreenPart gp;
+  PFN_cuDeviceGet_t dget;
+  PFN_cuDeviceGetDevResource_t getres;
+  PFN_cuDevSmResourceSplitByCount_t split;
+  PFN_cuDevResourceGenerateDesc_t gendesc;
+  PFN_cuGreenCtxCreate_t gcreate;
+  PFN_cuGreenCtxStreamCreate_t gstream;
+  if (driver_fn("cuDeviceGet", &dget) && driver_fn("cuDeviceGetDevResource", &getres) &&
+      driver_fn("cuDevSmResourceSplitByCount", &split) &&
+      driver_fn("cuDevResourceGenerateDesc", &gendesc) && driver_fn("cuGreenCtxCreate", &gcreate) &&
+      driver_fn("cuGreenCtxStreamCreate", &gstream)) {
+    CUdevice cd;
+    CUdevResource all, grp, rest;
+    unsigned int n = 1;
+    CUdevResourceDesc dg, dm;
+    CUgreenCtx cg, cm;
+    CUstream sg, sm;
+    if (dget(&cd, dev) == CUDA_SUCCESS && getres(cd, &all, CU_DEV_RESOURCE_TYPE_SM) == CUDA_SUCCESS &&
+        split(&grp, &n, &all, &rest, 0, static_cast<unsigned>(ng)) == CUDA_SUCCESS && n == 1 &&
+        rest.sm.smCount > 0 && gendesc(&dg, &grp, 1) == CUDA_SUCCESS &&
+        gendesc(&dm, &rest, 1) == CUDA_SUCCESS &&
+        gcreate(&cg, dg, cd, CU_GREEN_CTX_DEFAULT_STREAM) == CUDA_SUCCESS &&
+        gcreate(&cm, dm, cd, CU_GREEN_CTX_DEFAULT_STREAM) == CUDA_SUCCESS &&
+        gstream(&sg, cg, CU_STREAM_NON_BLOCKING, 0) == CUDA_SUCCESS &&
+        gstream(&sm, cm, CU_STREAM_NON_BLOCKING, 0) == CUDA_SUCCESS) {
+      gp.ok = true;
+      gp.ng = static_cast<int>(grp.sm.smCount);
+      gp.nm = static_cast<int>(rest.sm.smCount);
+      gp.sg = reinterpret_cast<cudaStream_t>(sg);
+      gp.sm = reinterpret_cast<cudaStream_t>(sm);
+    }
+  }
+  (void)cudaGetLastError();
+  cache.push_back({{dev, ng}, gp});
+  return gp;
+}
+
+// An event recorded on one stream for later waits on others.
+struct Ev {
+  cudaEvent_t e = nullptr;
+  ~Ev() {
+    if (e) cudaEventDestroy(e);
+  }
+  poetx_status record(cudaStream_t st) {
+    if (!e) POETX_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    POETX_CUDA(cudaEventRecord(e, st));
+    return POETX_OK;
+  }
+  poetx_status wait_on(cudaStream_t st) const {
+    POETX_CUDA(cudaStreamWaitEvent(st, e, 0));
+    return POETX_OK;
+  }
+};
+
+// Token chunks: `count` ranges, multiples of 128 tokens except the last.
+struct Chunks {
+  int count = 1;
+  int64_t t0[kMaxChunks] = {0};
+  int64_t len[kMaxChunks] = {0};
+};
+
+// Schedule of one bf16 pass: the pipeline when green partitions exist and T
+// is large enough, else one chunk on the caller's stream.
+struct Plan {
+  Chunks ch;
+  GreenPart gp;
+  bool piped = false;
+};
+
+Plan make_plan(int64_t T, bool backward) {
+  Plan pl;
+  PipeCfg cfg;
+  {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cfg = g_pipe;
+  }
+  const int C = std::min(std::max(cfg.chunks, 1), kMaxChunks);
+  if (C > 1 && T >= cfg.min_tokens && T >= C * 128) {
+    pl.gp = green_partition(backward ? cfg.bwd_gemm_sms : cfg.fwd_gemm_sms);
+    if (pl.gp.ok) {
+      pl.piped = true;
+      const int64_t per = ((T + C - 1) / C + 127) / 128 * 128;
+      int k = 0;
+      for (int64_t t = 0; t < T && k < kMaxChunks; t += per, ++k) {
+        pl.ch.t0[k] = t;
+        pl.ch.len[k] = std::min(per, T - t);
+      }
+      pl.ch.count = k;
+    }
+  }
+  if (!pl.piped) {
+    pl.ch.count = 1;
+    pl.ch.t0[0] = 0;
+    pl.ch.len[0] = T;
+  }
+  return pl;
+}
+
+// Forward, bf16:  A(k): X -> u (gather) -> v (P blocks);  G(k): h = v W0'^T;
+// Z(k): h -> z (R blocks) -> Y (scatter), on token chunk k.
+// Pipelined order (GEMM partition g, memory partition m, caller stream c):
+//   c: A(0) | g: G(0) G(1) ... G(C-1) | m: A(1), Z(0), A(2), Z(1), ... Z(C-2) | c: Z(C-1)
 poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X, int64_t T,
                       __nv_bfloat16* Y, __nv_bfloat16* hs) {
   const int m = c.d.m, n = c.d.n;
@@ -848,12 +1038,60 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
   auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
   const SideLayout &R = c.L.R, &P = c.L.P;
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
-  POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
-  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
-  POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, z, Y, c.piRinv(), T, m));
-  return POETX_OK;
+  const auto* BsbP = c.p<__nv_bfloat16>(P.off_Bsb);
+  const auto* BsbR = c.p<__nv_bfloat16>(R.off_Bsb);
+  const Plan pl = make_plan(T, false);
+  const Chunks& ch = pl.ch;
+  auto A = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, u + t0 * n, c.piP(), len, n));
+    return tc_blockdiag(st, u + t0 * n, BsbP, v + t0 * n, len, n, P.sb, P.nsb);
+  };
+  auto G = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    return tc_dense_nt(st, v + t0 * n, W0p, h + t0 * m, len, m, n);
+  };
+  auto Z = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    POETX_TRY(tc_blockdiag(st, h + t0 * m, BsbR, z + t0 * m, len, m, R.sb, R.nsb));
+    return gather_cols<__nv_bfloat16>(st, z + t0 * m, Y + t0 * m, c.piRinv(), len, m);
+  };
+  if (!pl.piped) {
+    POETX_TRY(A(0, c.st, 0));
+    POETX_TRY(G(0, c.st, 0));
+    return Z(0, c.st, 0);
+  }
+  const int C = ch.count;
+  const cudaStream_t sc = c.st, sg = pl.gp.sg, sm = pl.gp.sm;
+  const int ng = pl.gp.ng, nm = pl.gp.nm;
+  Ev start, evA[kMaxChunks], evG[kMaxChunks], done_m;
+  POETX_TRY(start.record(sc));
+  POETX_TRY(start.wait_on(sm));
+  POETX_TRY(A(0, sc, 0));
+  POETX_TRY(evA[0].record(sc));
+  POETX_TRY(evA[0].wait_on(sg));
+  POETX_TRY(A(1, sm, nm));
+  POETX_TRY(evA[1].record(sm));
+  POETX_TRY(G(0, sg, ng));
+  POETX_TRY(evG[0].record(sg));
+  for (int k = 1; k < C; ++k) {
+    POETX_TRY(evA[k].wait_on(sg));
+    POETX_TRY(G(k, sg, ng));
+    POETX_TRY(evG[k].record(sg));
+    POETX_TRY(evG[k - 1].wait_on(sm));
+    POETX_TRY(Z(k - 1, sm, nm));
+    if (k + 1 < C) {
+      POETX_TRY(A(k + 1, sm, nm));
+      POETX_TRY(evA[k + 1].record(sm));
+    }
+  }
+  POETX_TRY(done_m.record(sm));
+  POETX_TRY(evG[C - 1].wait_on(sc));
+  POETX_TRY(Z(C - 1, sc, 0));
+  return done_m.wait_on(sc);
 }
 
 bool fused_cayley_bwd_ok(const poetx_layer_desc& d, int b) {
@@ -890,14 +1128,14 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
   float* nsc = c.w<float>(c.W.off_nsc);
   if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_R))
-      POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.W.splitsR, dGenR,
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.slotsR, dGenR,
                                  accumulate));
     else
       POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
   }
   if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_P))
-      POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.W.splitsP, dGenP,
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.slotsP, dGenP,
                                  accumulate));
     else
       POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
@@ -940,6 +1178,14 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
   return POETX_OK;
 }
 
+// Backward, bf16, on token chunk k:
+//   RA(k) recompute only: X -> u (gather) -> v (P blocks);  RG(k): h = v W0'^T
+//   U(k)  stored h: X -> u (gather)
+//   R1(k) dY -> dz (gather) -> dh (R^T blocks);  GR(k): partials of dz^T h
+//   D(k)  dv = dh W0';  GP(k): partials of dv^T u;  E(k): dv -> du (P^T blocks) -> dX
+// Pipelined order: the GEMMs (RG, D) on the GEMM partition, the rest on the
+// memory partition; chunk 0's first stages and the last chunk's final
+// stages on the caller's stream with the whole device.
 poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X,
                       const __nv_bfloat16* dY, const __nv_bfloat16* hs, int64_t T,
                       __nv_bfloat16* dX) {
@@ -952,35 +1198,108 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   auto* dh = c.w<__nv_bfloat16>(c.W.off_m3);
   float* partR = c.w<float>(c.W.off_partR);
   float* partP = c.w<float>(c.W.off_partP);
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
-  const __nv_bfloat16* h = hs;
-  if (!hs) {  // activation recompute (POET-Xmem)
-    POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
-    POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
-    h = hbuf;
+  const auto* BsbP = c.p<__nv_bfloat16>(P.off_Bsb);
+  const auto* BsbRT = c.p<__nv_bfloat16>(R.off_BsbT);
+  const auto* BsbPT = c.p<__nv_bfloat16>(P.off_BsbT);
+  const bool recompute = (hs == nullptr);
+  const __nv_bfloat16* h = recompute ? hbuf : hs;
+  auto* dv = v;   // v of a chunk is dead once its h is formed
+  auto* du = u;   // u of a chunk is dead once its dv^T u partials are formed
+  const int64_t strideR = static_cast<int64_t>(R.nsb) * R.sb * R.sb;
+  const int64_t strideP = static_cast<int64_t>(P.nsb) * P.sb * P.sb;
+  c.slotsR = c.slotsP = 0;
+  const Plan pl = make_plan(T, true);
+  const Chunks& ch = pl.ch;
+  auto RA = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, u + t0 * n, c.piP(), len, n));
+    if (!recompute) return POETX_OK;
+    return tc_blockdiag(st, u + t0 * n, BsbP, v + t0 * n, len, n, P.sb, P.nsb);
+  };
+  auto RG = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    return tc_dense_nt(st, v + t0 * n, W0p, hbuf + t0 * m, len, m, n);
+  };
+  auto R1 = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    POETX_TRY(gather_cols<__nv_bfloat16>(st, dY + t0 * m, dz + t0 * m, c.piR(), len, m));
+    return tc_blockdiag(st, dz + t0 * m, BsbRT, dh + t0 * m, len, m, R.sb, R.nsb);
+  };
+  auto GR = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    return tc_gradred(st, R, dz + t0 * m, h + t0 * m, partR + c.slotsR * strideR, len, &c.slotsR);
+  };
+  auto D = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    return tc_dense_nn(st, dh + t0 * m, W0p, dv + t0 * n, len, n, m);
+  };
+  auto GPE = [&](int k, cudaStream_t st, int budget) -> poetx_status {
+    CtaBudget bg(budget);
+    const int64_t t0 = ch.t0[k], len = ch.len[k];
+    POETX_TRY(tc_gradred(st, P, dv + t0 * n, u + t0 * n, partP + c.slotsP * strideP, len, &c.slotsP));
+    if (!dX) return POETX_OK;
+    POETX_TRY(tc_blockdiag(st, dv + t0 * n, BsbPT, du + t0 * n, len, n, P.sb, P.nsb));
+    return gather_cols<__nv_bfloat16>(st, du + t0 * n, dX + t0 * n, c.piPinv(), len, n);
+  };
+  if (!pl.piped) {
+    POETX_TRY(RA(0, c.st, 0));
+    if (recompute) POETX_TRY(RG(0, c.st, 0));
+    POETX_TRY(R1(0, c.st, 0));
+    POETX_TRY(GR(0, c.st, 0));
+    POETX_TRY(D(0, c.st, 0));
+    POETX_TRY(GPE(0, c.st, 0));
+  } else {
+    const int C = ch.count;
+    const cudaStream_t sc = c.st, sg = pl.gp.sg, sm = pl.gp.sm;
+    const int ng = pl.gp.ng, nm = pl.gp.nm;
+    Ev start, evRA[kMaxChunks], evRG[kMaxChunks], evR1[kMaxChunks], evD[kMaxChunks], done_m;
+    POETX_TRY(start.record(sc));
+    POETX_TRY(start.wait_on(sm));
+    POETX_TRY(start.wait_on(sg));
+    for (int k = 0; k < C; ++k) {
+      const cudaStream_t mst = (k == 0) ? sc : sm;   // chunk 0's first stages: whole device
+      const int mb = (k == 0) ? 0 : nm;
+      POETX_TRY(RA(k, mst, mb));
+      if (recompute) {
+        POETX_TRY(evRA[k].record(mst));
+        POETX_TRY(evRA[k].wait_on(sg));
+        POETX_TRY(RG(k, sg, ng));
+        POETX_TRY(evRG[k].record(sg));
+      }
+      POETX_TRY(R1(k, mst, mb));
+      POETX_TRY(evR1[k].record(mst));
+      POETX_TRY(evR1[k].wait_on(sg));
+      if (k == 0) POETX_TRY(evR1[0].wait_on(sm));   // later chunks' stages follow chunk 0's
+      POETX_TRY(D(k, sg, ng));
+      POETX_TRY(evD[k].record(sg));
+      if (recompute) POETX_TRY(evRG[k].wait_on(sm));
+      POETX_TRY(GR(k, sm, nm));
+      if (k >= 1) {
+        POETX_TRY(evD[k - 1].wait_on(sm));
+        POETX_TRY(GPE(k - 1, sm, nm));
+      }
+    }
+    POETX_TRY(done_m.record(sm));
+    POETX_TRY(evD[C - 1].wait_on(sc));
+    POETX_TRY(done_m.wait_on(sc));
+    POETX_TRY(GPE(C - 1, sc, 0));
   }
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
-  POETX_TRY(tc_blockdiag(c.st, dz, c.p<__nv_bfloat16>(R.off_BsbT), dh, T, m, R.sb, R.nsb));
-  POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, c.W.splitsR));
-  auto* dv = v;
-  POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
-  POETX_TRY(tc_gradred(c.st, P, dv, u, partP, T, c.W.splitsP));
-  auto* du = u;
-  POETX_TRY(tc_blockdiag(c.st, dv, c.p<__nv_bfloat16>(P.off_BsbT), du, T, n, P.sb, P.nsb));
-  if (dX) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
   ProfScope prof(POETX_KIND_GENBWD, c.st);
   // exact Cayley blocks of b <= 128: the generator backward runs fused per block
   // in bwd_common_tail; otherwise reduce the partials into G here.
   if (!fused_cayley_bwd_ok(c.d, R.g.b)) {
     gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
-        partR, static_cast<int64_t>(R.nsb) * R.sb * R.sb, c.W.splitsR, R.g, R.sb,
-        c.w<float>(c.W.off_GR));
+        partR, strideR, c.slotsR, R.g, R.sb, c.w<float>(c.W.off_GR));
     POETX_LAUNCHED();
   }
   if (!fused_cayley_bwd_ok(c.d, P.g.b)) {
     gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0, c.st>>>(
-        partP, static_cast<int64_t>(P.nsb) * P.sb * P.sb, c.W.splitsP, P.g, P.sb,
-        c.w<float>(c.W.off_GP));
+        partP, strideP, c.slotsP, P.g, P.sb, c.w<float>(c.W.off_GP));
     POETX_LAUNCHED();
   }
   return POETX_OK;
@@ -1380,3 +1699,26 @@ extern "C" poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, c
   }
   return poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, scratch, stream);
 }
+
+extern "C" {
+
+void poetx_set_pipeline(int32_t chunks, int32_t fwd_gemm_sms, int32_t bwd_gemm_sms,
+                        int64_t min_tokens) {
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  g_pipe.chunks = std::min<int32_t>(std::max<int32_t>(chunks, 1), kMaxChunks);
+  if (fwd_gemm_sms > 0) g_pipe.fwd_gemm_sms = fwd_gemm_sms;
+  if (bwd_gemm_sms > 0) g_pipe.bwd_gemm_sms = bwd_gemm_sms;
+  if (min_tokens > 0) g_pipe.min_tokens = min_tokens;
+}
+
+int32_t poetx_pipeline_active(void) {
+  PipeCfg cfg;
+  {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cfg = g_pipe;
+  }
+  if (cfg.chunks <= 1) return 0;
+  return (green_partition(cfg.fwd_gemm_sms).ok && green_partition(cfg.bwd_gemm_sms).ok) ? 1 : 0;
+}
+
+}  // extern "C"
