@@ -447,8 +447,13 @@ def main():
         for lin in wl.linears:
             by += 2 * T * (3 * lin.n + 2 * lin.m) * (2 if wl.dtype == "bf16" else 4)
         achieved = by * args.steps / (kinds[top]["ms"] / 1e3) / 1e9
+        launches_top = kinds[top]["groups"]
         roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None}
+                "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                "peak_source": f"{peaks['source']} HBM copy", "launches": launches_top,
+                "avg_launch_ms": kinds[top]["ms"] / launches_top,
+                "algorithmic_bytes_per_launch": by * args.steps / launches_top,
+                "traffic": measured_traffic(top, wl.key, b)}
 
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
