@@ -326,57 +326,82 @@ def main():
     torch.cuda.synchronize(dev)
 
     step_counter = [0]
-    # Per-layer work that does not depend on other layers (building the blocks
-    # from the generators, and the merge) is issued on one side stream per
-    # layer and joined with events; forward and backward run on `stream`.
+    # Per-layer work that depends only on that layer (rebuilding its blocks
+    # from the generators, and the merge) runs on one side stream per layer,
+    # ordered by per-layer events: layer l's merge starts as soon as its own
+    # backward is done and its next build follows on the same side stream,
+    # while the main stream runs the other layers' forward and backward.
     # Each merge has its own scratch so concurrent merges do not share it.
     side = [torch.cuda.Stream(dev) for _ in layers]
     merge_ws = ([torch.empty(px.poetx_merge_workspace_size(st["desc"]), dtype=torch.uint8,
                              device=dev) for st in layers] if wl.merge_each_step else None)
+    bwd_done = [None] * len(layers)    # event after layer l's backward in the previous step
+    merged = [0]                       # merges issued so far (for fresh seeds)
 
-    def fan_out(fn):
-        ev = torch.cuda.Event()
-        ev.record(stream)
+    def merge_one(li, st, ss, tag):
+        nR = synth.SEED_MERGE_R + 100 * (tag + 1) + li
+        nP = synth.SEED_MERGE_P + 100 * (tag + 1) + li
+        px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, merge_ws[li], ss)
+        st["desc"].seed_R, st["desc"].seed_P = nR, nP
+
+    def build_all(tag=None):
+        """Issue every layer's (merge +) build on its side stream; returns per-layer
+        events the main stream waits on before that layer's forward."""
+        start = torch.cuda.Event()
+        start.record(stream)
+        ready = []
+        for li, st in enumerate(layers):
+            ss = side[li]
+            ss.wait_event(bwd_done[li] if bwd_done[li] is not None else start)
+            if wl.merge_each_step and bwd_done[li] is not None:
+                merge_one(li, st, ss, tag if tag is not None else step_counter[0])
+            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
+            e = torch.cuda.Event()
+            e.record(ss)
+            ready.append(e)
+        return ready
+
+    def drain_merges(tag):
+        """Merges of the last step (so that every timed step includes its merges)."""
+        if not wl.merge_each_step:
+            return
         done = []
         for li, st in enumerate(layers):
-            side[li].wait_event(ev)
-            fn(li, st, side[li])
+            ss = side[li]
+            ss.wait_event(bwd_done[li])
+            merge_one(li, st, ss, tag)
             e = torch.cuda.Event()
-            e.record(side[li])
+            e.record(ss)
             done.append(e)
         for e in done:
             stream.wait_event(e)
-
-    def build_all():
-        fan_out(lambda li, st, ss: px.poetx_params_build(st["desc"], st["genR"], st["genP"],
-                                                         st["params"], ss))
-
-    def merge_all(s):
-        def one(li, st, ss):
-            nR = synth.SEED_MERGE_R + 100 * (s + 1) + li
-            nP = synth.SEED_MERGE_P + 100 * (s + 1) + li
-            px.poetx_merge(st["desc"], st["params"], st["W0p"], nR, nP, merge_ws[li], ss)
-            st["desc"].seed_R, st["desc"].seed_P = nR, nP
-        fan_out(one)
+        for li in range(len(layers)):
+            bwd_done[li] = None
 
     def step():
         s = step_counter[0]
-        build_all()
-        for st in layers:
+        ready = build_all(s)
+        for li, st in enumerate(layers):
+            stream.wait_event(ready[li])
             px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
                                 workspace, stream)
-        for st in reversed(layers):
+        for li in reversed(range(len(layers))):
+            st = layers[li]
             px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"], T,
                                 st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
             if dist is not None:
                 dist.all_reduce(st["dgR"])
                 dist.all_reduce(st["dgP"])
-        if wl.merge_each_step:
-            merge_all(s)
+            e = torch.cuda.Event()
+            e.record(stream)
+            bwd_done[li] = e
+        # the merges of this step are issued at the start of the next step (they
+        # overlap its builds and forwards); the timed region ends with drain_merges
         step_counter[0] += 1
 
     for _ in range(args.warmup):
         step()
+    drain_merges(step_counter[0])
     torch.cuda.synchronize(dev)
     if px.poetx_device_status(reset=True) != px.POETX_OK:
         raise SystemExit("device status reported a timeout during warm-up")
@@ -396,6 +421,7 @@ def main():
     ev0.record(stream)
     for _ in range(args.steps):
         step()
+    drain_merges(step_counter[0])   # the last timed step's merges
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     launches = px.poetx_launch_count() - launches0
@@ -472,7 +498,7 @@ def main():
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
-                              build_all, merge_all)
+                              build_all, drain_merges, bwd_done)
 
     # ---- the oracle on this host's cores (rank 0, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -489,7 +515,7 @@ def main():
 
 
 def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist, build_all,
-            merge_all):
+            drain_merges, bwd_done):
     T = wl.tokens
     maxn = max(l.n for l in wl.linears)
     maxm = max(l.m for l in wl.linears)
@@ -509,13 +535,19 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
 
     def step():
         s = cnt[0]
-        build_all()
+        ready = build_all(1000 + s)
+        for e in ready:
+            stream.wait_event(e)
         for st in layers:
             px.poetx_linear_step_host(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
                                       st["dY"], st["Y"], st["h"], st["dX"], st["dgR"], st["dgP"],
                                       ghR[id(st)], ghP[id(st)], workspace, stream)
         if wl.merge_each_step:
-            merge_all(1000 + s)
+            for li in range(len(layers)):
+                e = torch.cuda.Event()
+                e.record(stream)
+                bwd_done[li] = e
+            drain_merges(1000 + s)
         torch.cuda.synchronize(dev)
         cnt[0] += 1
 

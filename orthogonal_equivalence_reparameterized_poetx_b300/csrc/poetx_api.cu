@@ -25,6 +25,7 @@
 #include "ptx.cuh"
 #include "simt.cuh"
 #include "tc_gemm.cuh"
+#include "tc_bdgr.cuh"
 
 using namespace poetx;
 
@@ -253,7 +254,9 @@ int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
   const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
   const int64_t smax = std::max<int64_t>(
       1, std::min<int64_t>((4 * device_sm_count() + per_split - 1) / per_split, (T + 63) / 64));
-  return smax * kMaxChunks;
+  // the fused transform + reduction writes one slot per CTA of a super-block
+  const int64_t fused = std::max<int64_t>(1, device_sm_count() / S.nsb);
+  return std::max(smax * kMaxChunks, fused);
 }
 
 WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t T, int nsm) {
@@ -350,6 +353,12 @@ poetx_status simt_gemm(cudaStream_t st, int M, int N, int K, int batch, const TA
                        TC* C, int64_t sCm, int64_t sCn, int64_t bsC, float alpha, float beta) {
   if (M <= 0 || N <= 0 || batch <= 0) return POETX_OK;
   SimtGemmArgs g{M, N, K, batch, A, sAm, sAk, bsA, B, sBk, sBn, bsB, C, sCm, sCn, bsC, alpha, beta};
+  if (M >= 128 && N >= 128) {
+    dim3 grid((N + 127) / 128, (M + 127) / 128, batch);
+    simt_gemm128_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
   dim3 grid((N + 63) / 64, (M + 63) / 64, batch);
   simt_gemm_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
   POETX_LAUNCHED();
@@ -550,6 +559,40 @@ poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, con
   const int tps = sb / 128;
   a.num_tiles = sp.splits * nsb * tps * tps;
   return launch_tc<128, true, true, TileMode::GradRed, float>(st, ta, tb, ta, a);
+}
+
+// Fused block transform + token reduction for 128-wide super-blocks:
+// out = in S^T per super-block and partial slots of in^T C (see tc_bdgr.cuh).
+bool bdgr_ok(const SideLayout& S) { return S.sb == 128 && S.nsb <= launch_sms(); }
+
+poetx_status tc_bdgr(cudaStream_t st, const SideLayout& S, const void* in, const void* Ssb,
+                     void* out, const void* Cm, float* partial, int64_t T, int* slots) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_BLOCKDIAG, st);
+  const int d = S.g.d;
+  CUtensorMap ta, tsb, tc, to;
+  POETX_TRY(tmap_bf16(&ta, in, T, d, d, 128));
+  POETX_TRY(tmap_bf16(&tsb, Ssb, static_cast<uint64_t>(S.nsb) * 128, 128, 128, 128));
+  POETX_TRY(tmap_bf16(&tc, Cm, T, d, d, 128));
+  POETX_TRY(tmap_bf16(&to, out, T, d, d, 128));
+  BdgrArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = d;
+  a.nsb = S.nsb;
+  a.nslots = std::max(1, launch_sms() / S.nsb);
+  a.partial = partial;
+  a.timeout_ns = g_timeout_ns;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(tc_bdgr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    BdgrCfg::SMEM);
+  });
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  tc_bdgr_kernel<<<a.nslots * S.nsb, 320, BdgrCfg::SMEM, st>>>(ta, tsb, tc, to, a);
+  POETX_LAUNCHED();
+  *slots += a.nslots;
+  return POETX_OK;
 }
 
 // ------------------------------------------------------------------ builder
@@ -1249,10 +1292,20 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   if (!pl.piped) {
     POETX_TRY(RA(0, c.st, 0));
     if (recompute) POETX_TRY(RG(0, c.st, 0));
-    POETX_TRY(R1(0, c.st, 0));
-    POETX_TRY(GR(0, c.st, 0));
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
+    if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
+      POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
+    } else {
+      POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
+      POETX_TRY(GR(0, c.st, 0));
+    }
     POETX_TRY(D(0, c.st, 0));
-    POETX_TRY(GPE(0, c.st, 0));
+    if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
+      POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
+      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+    } else {
+      POETX_TRY(GPE(0, c.st, 0));
+    }
   } else {
     const int C = ch.count;
     const cudaStream_t sc = c.st, sg = pl.gp.sg, sm = pl.gp.sm;

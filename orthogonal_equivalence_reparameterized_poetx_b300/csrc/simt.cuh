@@ -103,6 +103,100 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemmArgs g) {
   }
 }
 
+// Same contraction with 128 x 128 output tiles for large M and N: 256 threads,
+// each owning an 8 x 8 sub-tile (rows ty*4 + {0..3} and 64 + ty*4 + {0..3},
+// columns likewise), k-slices of 8 double-buffered in shared memory, so every
+// 64 FMAs cost four 16-byte shared loads.
+template <typename TA, typename TB, typename TC>
+__global__ void __launch_bounds__(256) simt_gemm128_kernel(const SimtGemmArgs g) {
+  __shared__ __align__(16) float As[2][8][128];
+  __shared__ __align__(16) float Bs[2][8][128];
+  const int z = blockIdx.z;
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const TA* A = reinterpret_cast<const TA*>(g.A) + z * g.bsA;
+  const TB* B = reinterpret_cast<const TB*>(g.B) + z * g.bsB;
+  TC* C = reinterpret_cast<TC*>(g.C) + z * g.bsC;
+  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+  const bool a_k_contig = (g.sAk == 1);
+  const bool b_n_contig = (g.sBn == 1);
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  float ra[4], rb[4];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + 256 * e;  // 0..1023 over 128 x 8
+      int mm, kk;
+      if (a_k_contig) mm = idx / 8, kk = idx % 8;
+      else mm = idx % 128, kk = idx / 128;
+      const int gm = m0 + mm, gk = k0 + kk;
+      ra[e] = (gm < g.M && gk < g.K) ? to_f32(A[gm * g.sAm + gk * g.sAk]) : 0.f;
+      int kb, nn;
+      if (b_n_contig) kb = idx / 128, nn = idx % 128;
+      else kb = idx % 8, nn = idx / 8;
+      const int gk2 = k0 + kb, gn = n0 + nn;
+      rb[e] = (gk2 < g.K && gn < g.N) ? to_f32(B[gk2 * g.sBk + gn * g.sBn]) : 0.f;
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + 256 * e;
+      int mm, kk;
+      if (a_k_contig) mm = idx / 8, kk = idx % 8;
+      else mm = idx % 128, kk = idx / 128;
+      As[buf][kk][mm] = ra[e];
+      int kb, nn;
+      if (b_n_contig) kb = idx / 128, nn = idx % 128;
+      else kb = idx % 8, nn = idx / 8;
+      Bs[buf][kb][nn] = rb[e];
+    }
+  };
+  load(0);
+  store(0);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < g.K; k0 += 8) {
+    const bool more = k0 + 8 < g.K;
+    if (more) load(k0 + 8);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (more) {
+      store(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    if (gm >= g.M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+      if (gn >= g.N) continue;
+      TC* c = C + gm * g.sCm + gn * g.sCn;
+      float v = g.alpha * acc[i][j];
+      if (g.beta != 0.f) v = fmaf(g.beta, to_f32(*c), v);
+      *c = from_f32<TC>(v);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ gathers
 // out[r][j] = in[r][idx[j]] for `rows` rows of d elements (row-local feature
 // permutation).  A CTA stages `rows_per_iter` consecutive rows (one
