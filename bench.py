@@ -312,7 +312,10 @@ def main():
         st["X"], st["dY"] = inp.X.to(dev), inp.dY.to(dev)
         st["Y"] = torch.empty(T, lin.m, dtype=dt, device=dev)
         st["dX"] = torch.empty(T, lin.n, dtype=dt, device=dev)
+        # stored-activation workloads keep h and the permuted input u of the
+        # forward; recompute workloads keep neither
         st["h"] = None if wl.recompute else torch.empty(T, lin.m, dtype=dt, device=dev)
+        st["u"] = None if wl.recompute else torch.empty(T, lin.n, dtype=dt, device=dev)
         st["dgR"] = torch.empty(lr, dtype=torch.float32, device=dev)
         st["dgP"] = torch.empty(lp, dtype=torch.float32, device=dev)
         W0 = inp.W0.to(dev)
@@ -384,11 +387,11 @@ def main():
         for li, st in enumerate(layers):
             stream.wait_event(ready[li])
             px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
-                                workspace, stream)
+                                st["u"], workspace, stream)
         for li in reversed(range(len(layers))):
             st = layers[li]
-            px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"], T,
-                                st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
+            px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"],
+                                st["u"], T, st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
             if dist is not None:
                 dist.all_reduce(st["dgR"])
                 dist.all_reduce(st["dgP"])
@@ -540,8 +543,8 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
             stream.wait_event(e)
         for st in layers:
             px.poetx_linear_step_host(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
-                                      st["dY"], st["Y"], st["h"], st["dX"], st["dgR"], st["dgP"],
-                                      ghR[id(st)], ghP[id(st)], workspace, stream)
+                                      st["dY"], st["Y"], st["h"], st["u"], st["dX"], st["dgR"],
+                                      st["dgP"], ghR[id(st)], ghP[id(st)], workspace, stream)
         if wl.merge_each_step:
             for li in range(len(layers)):
                 e = torch.cuda.Event()

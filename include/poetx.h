@@ -137,10 +137,13 @@ size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T);
  *   Y[:, pi_R] = z.
  * X: T x n, Y: T x m (dtype).  saved_h: T x m (dtype) receives h, or NULL
  * for activation recompute in the backward (Methodologie §5, POET-Xmem).
+ * saved_u: T x n (dtype) receives the permuted input u, or NULL; the
+ * backward reads it instead of permuting X again.  Both are caller-owned and
+ * must not alias X, Y or each other.
  * T = 0 is a no-op.  Errors: INVALID_ARG, MISALIGNED, CUDA. */
 poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params,
                               const void* W0p, const void* X, int64_t T, void* Y,
-                              void* saved_h, void* workspace, void* stream);
+                              void* saved_h, void* saved_u, void* workspace, void* stream);
 
 /* Backward of L with upstream gradient dY (T x m):
  *   dz = dY[:, pi_R];  G_R,k = dz_k^T h_k;  dh_k = dz_k B_R,k;
@@ -149,14 +152,19 @@ poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params,
  * then per block the Cayley backward dL/dQ = 2 M^T G M^T with
  * M = (I-Q)^-1 (or the Neumann chain rule) and the packed gradient
  * g_ij = dL/dQ[i][j] - dL/dQ[j][i] for i < j.
- * saved_h: the h written by poetx_linear_fwd, or NULL to recompute v and h
- * from X.  dX: T x n or NULL to skip it.  dGenR/dGenP: fp32 packed
+ * saved_h: the h written by poetx_linear_fwd, or NULL to recompute v and h.
+ * saved_u: the u written by poetx_linear_fwd, or NULL to permute X again;
+ * X may be NULL when saved_u is given (it is then not read).  Whatever is
+ * saved is reused and whatever is not is recomputed, so the four
+ * combinations trade memory (T x m and T x n per saved tensor) against
+ * recompute (a GEMM for h, one permutation pass for u).
+ * dX: T x n or NULL to skip it.  dGenR/dGenP: fp32 packed
  * gradients (lengths as for the generators); accumulate != 0 adds into them.
  * Errors: INVALID_ARG, MISALIGNED, CUDA. */
 poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params,
                               const void* W0p, const void* X, const void* dY,
-                              const void* saved_h, int64_t T, void* dX, float* dGenR,
-                              float* dGenP, int32_t accumulate, void* workspace,
+                              const void* saved_h, const void* saved_u, int64_t T, void* dX,
+                              float* dGenR, float* dGenP, int32_t accumulate, void* workspace,
                               void* stream);
 
 /* Scratch bytes that poetx_merge needs. */
@@ -176,17 +184,17 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
 
 /* One forward+backward step from HOST buffers: copies X_host (T x n) and
  * dY_host (T x m) into the device buffers X_dev / dY_dev, runs
- * poetx_linear_fwd (into Y_dev, saved_h_dev) and poetx_linear_bwd (into
- * dX_dev, dGenR_dev, dGenP_dev, overwriting), and copies the generator
- * gradients back into dGenR_host / dGenP_host.  Host buffers should be
- * pinned for asynchronous copies.  Synchronises `stream` before returning.
- * saved_h_dev may be NULL (recompute). */
+ * poetx_linear_fwd (into Y_dev, saved_h_dev, saved_u_dev) and
+ * poetx_linear_bwd (into dX_dev, dGenR_dev, dGenP_dev, overwriting), and
+ * copies the generator gradients back into dGenR_host / dGenP_host.  Host
+ * buffers should be pinned for asynchronous copies.  Synchronises `stream`
+ * before returning.  saved_h_dev and saved_u_dev may be NULL (recompute). */
 poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params,
                                     const void* W0p, const void* X_host,
                                     const void* dY_host, int64_t T, void* X_dev,
                                     void* dY_dev, void* Y_dev, void* saved_h_dev,
-                                    void* dX_dev, float* dGenR_dev, float* dGenP_dev,
-                                    float* dGenR_host, float* dGenP_host,
+                                    void* saved_u_dev, void* dX_dev, float* dGenR_dev,
+                                    float* dGenP_dev, float* dGenR_host, float* dGenP_host,
                                     void* workspace, void* stream);
 
 /* Reads (and with reset != 0 clears) the device status word that bounded
@@ -234,7 +242,7 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
 #define POETX_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* params,
                                       const void* W0p, const void* X, int64_t T, void* Y,
-                                      void* saved_h, void* stream);
+                                      void* saved_h, void* saved_u, void* stream);
 
 /* Pipelined schedule of the bf16 forward and backward.  With T >=
  * min_tokens the library splits the tokens into `chunks` (2..4) and runs the

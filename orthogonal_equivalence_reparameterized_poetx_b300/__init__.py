@@ -95,11 +95,11 @@ def _load():
         "poetx_params_build": (I32, [D, P, P, P, P]),
         "poetx_weight_premerge": (I32, [D, P, P, P, P]),
         "poetx_workspace_size": (SZ, [D, I64]),
-        "poetx_linear_fwd": (I32, [D, P, P, P, I64, P, P, P, P]),
-        "poetx_linear_bwd": (I32, [D, P, P, P, P, P, I64, P, P, P, I32, P, P]),
+        "poetx_linear_fwd": (I32, [D, P, P, P, I64, P, P, P, P, P]),
+        "poetx_linear_bwd": (I32, [D, P, P, P, P, P, P, I64, P, P, P, I32, P, P]),
         "poetx_merge_workspace_size": (SZ, [D]),
         "poetx_merge": (I32, [D, P, P, U64, U64, P, P]),
-        "poetx_linear_step_host": (I32, [D, P, P, P, P, I64, P, P, P, P, P, P, P, P, P, P, P]),
+        "poetx_linear_step_host": (I32, [D, P, P, P, P, I64, P, P, P, P, P, P, P, P, P, P, P, P]),
         "poetx_device_status": (I32, [I32]),
         "poetx_selftest_bounded_wait": (I32, [U64, P]),
         "poetx_set_wait_timeout_ns": (V, [U64]),
@@ -109,7 +109,7 @@ def _load():
                                      ctypes.POINTER(ctypes.c_double)]),
         "poetx_profile_kind_name": (ctypes.c_char_p, [I32]),
         "poetx_launch_count": (I64, []),
-        "poetx_linear_fwd_noalloc": (I32, [D, P, P, P, I64, P, P, P]),
+        "poetx_linear_fwd_noalloc": (I32, [D, P, P, P, I64, P, P, P, P]),
         "poetx_set_pipeline": (V, [I32, I32, I32, I64]),
         "poetx_pipeline_active": (I32, []),
     }
@@ -186,27 +186,27 @@ def poetx_workspace_size(desc, T: int) -> int:
     return LIB.poetx_workspace_size(ctypes.byref(desc), T)
 
 
-def poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, workspace, stream=None):
+def poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, saved_u, workspace, stream=None):
     _check(LIB.poetx_linear_fwd(ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X), T, _ptr(Y),
-                                _ptr(saved_h), _ptr(workspace), _stream(stream)),
+                                _ptr(saved_h), _ptr(saved_u), _ptr(workspace), _stream(stream)),
            "poetx_linear_fwd")
 
 
-def poetx_linear_bwd(desc, params, W0p, X, dY, saved_h, T, dX, dGenR, dGenP, accumulate,
+def poetx_linear_bwd(desc, params, W0p, X, dY, saved_h, saved_u, T, dX, dGenR, dGenP, accumulate,
                      workspace, stream=None):
     _check(LIB.poetx_linear_bwd(ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X), _ptr(dY),
-                                _ptr(saved_h), T, _ptr(dX), _ptr(dGenR), _ptr(dGenP),
-                                int(accumulate), _ptr(workspace), _stream(stream)),
+                                _ptr(saved_h), _ptr(saved_u), T, _ptr(dX), _ptr(dGenR),
+                                _ptr(dGenP), int(accumulate), _ptr(workspace), _stream(stream)),
            "poetx_linear_bwd")
 
 
-def poetx_linear_fwd_noalloc(desc, params, W0p, X, T, Y, saved_h, stream=None):
+def poetx_linear_fwd_noalloc(desc, params, W0p, X, T, Y, saved_h, saved_u, stream=None):
     """Forward without a workspace argument: the library's fixed device scratch
     of NOALLOC_SCRATCH_BYTES serves as workspace, so the call allocates
     nothing (for callers that cannot allocate device memory).  Calls that
     overlap on the GPU share that scratch and race."""
     _check(LIB.poetx_linear_fwd_noalloc(ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X), T,
-                                        _ptr(Y), _ptr(saved_h), _stream(stream)),
+                                        _ptr(Y), _ptr(saved_h), _ptr(saved_u), _stream(stream)),
            "poetx_linear_fwd_noalloc")
 
 
@@ -220,11 +220,11 @@ def poetx_merge(desc, params, W0p, new_seed_R, new_seed_P, workspace, stream=Non
 
 
 def poetx_linear_step_host(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev, Y_dev,
-                           saved_h_dev, dX_dev, dGenR_dev, dGenP_dev, dGenR_host, dGenP_host,
-                           workspace, stream=None):
+                           saved_h_dev, saved_u_dev, dX_dev, dGenR_dev, dGenP_dev, dGenR_host,
+                           dGenP_host, workspace, stream=None):
     _check(LIB.poetx_linear_step_host(
         ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X_host), _ptr(dY_host), T, _ptr(X_dev),
-        _ptr(dY_dev), _ptr(Y_dev), _ptr(saved_h_dev), _ptr(dX_dev), _ptr(dGenR_dev),
+        _ptr(dY_dev), _ptr(Y_dev), _ptr(saved_h_dev), _ptr(saved_u_dev), _ptr(dX_dev), _ptr(dGenR_dev),
         _ptr(dGenP_dev), _ptr(dGenR_host), _ptr(dGenP_host), _ptr(workspace), _stream(stream)),
         "poetx_linear_step_host")
 
@@ -300,16 +300,18 @@ class Layer:
     def premerge(self, W0, stream=None):
         poetx_weight_premerge(self.desc, self.params, W0, self.W0p, stream)
 
-    def forward(self, X, Y, saved_h=None, stream=None):
+    def forward(self, X, Y, saved_h=None, saved_u=None, stream=None):
         T = X.shape[0]
         assert T <= self.max_tokens
-        poetx_linear_fwd(self.desc, self.params, self.W0p, X, T, Y, saved_h, self.workspace, stream)
+        poetx_linear_fwd(self.desc, self.params, self.W0p, X, T, Y, saved_h, saved_u,
+                         self.workspace, stream)
 
-    def backward(self, X, dY, dX, dGenR, dGenP, saved_h=None, accumulate=False, stream=None):
-        T = X.shape[0]
+    def backward(self, X, dY, dX, dGenR, dGenP, saved_h=None, saved_u=None, accumulate=False,
+                 stream=None):
+        T = dY.shape[0]
         assert T <= self.max_tokens
-        poetx_linear_bwd(self.desc, self.params, self.W0p, X, dY, saved_h, T, dX, dGenR, dGenP,
-                         accumulate, self.workspace, stream)
+        poetx_linear_bwd(self.desc, self.params, self.W0p, X, dY, saved_h, saved_u, T, dX, dGenR,
+                         dGenP, accumulate, self.workspace, stream)
 
     def merge(self, new_seed_R, new_seed_P, stream=None):
         poetx_merge(self.desc, self.params, self.W0p, new_seed_R, new_seed_P, self.workspace,

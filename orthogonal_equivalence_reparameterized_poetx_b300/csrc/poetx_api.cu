@@ -26,6 +26,7 @@
 #include "simt.cuh"
 #include "tc_gemm.cuh"
 #include "tc_bdgr.cuh"
+#include "tc_merge.cuh"
 
 using namespace poetx;
 
@@ -595,6 +596,41 @@ poetx_status tc_bdgr(cudaStream_t st, const SideLayout& S, const void* in, const
   return POETX_OK;
 }
 
+// One tensor-core merge pass (tc_merge.cuh): with A = Ahi (+ Alo), M x N
+// row-major, and the super-blocks D = Dhi + Dlo of B - I over the N columns,
+// writes (A B^T)^T = (A + A D^T)^T as out_hi (+ out_lo), N x M row-major.
+template <bool A_SPLIT>
+poetx_status tc_merge_pass(cudaStream_t st, const __nv_bfloat16* Ahi, const __nv_bfloat16* Alo, int M,
+                           int N, int sb, int nsb, const __nv_bfloat16* Dhi, const __nv_bfloat16* Dlo,
+                           __nv_bfloat16* out_hi, __nv_bfloat16* out_lo) {
+  CUtensorMap tah, tal, tdh, tdl;
+  POETX_TRY(tmap_bf16(&tah, Ahi, M, N, N, 128));
+  POETX_TRY(tmap_bf16(&tal, A_SPLIT ? Alo : Ahi, M, N, N, 128));
+  POETX_TRY(tmap_bf16(&tdh, Dhi, static_cast<uint64_t>(nsb) * sb, sb, sb, 128));
+  POETX_TRY(tmap_bf16(&tdl, Dlo, static_cast<uint64_t>(nsb) * sb, sb, sb, 128));
+  MergeArgs a{};
+  a.M = M;
+  a.N = N;
+  a.sb = sb;
+  a.num_tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  a.res_hi = Ahi;
+  a.res_lo = A_SPLIT ? Alo : nullptr;
+  a.out_hi = out_hi;
+  a.out_lo = out_lo;
+  a.timeout_ns = g_timeout_ns;
+  auto kern = tc_merge_kernel<A_SPLIT>;
+  constexpr int smem = MergeCfg<A_SPLIT>::SMEM;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  kern<<<std::min(a.num_tiles, launch_sms()), 320, smem, st>>>(tah, tal, tdh, tdl, a);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 // ------------------------------------------------------------------ builder
 
 bool fused_cayley_ok(const poetx_layer_desc& d, int b) {
@@ -894,9 +930,10 @@ struct Ctx {
   mutable int slotsR = 0, slotsP = 0;
 };
 
-poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs) {
+poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs,
+                      float* us) {
   const int m = c.d.m, n = c.d.n;
-  float* u = c.w<float>(c.W.off_n1);
+  float* u = us ? us : c.w<float>(c.W.off_n1);
   float* v = c.w<float>(c.W.off_n2);
   float* h = hs ? hs : c.w<float>(c.W.off_m1);
   float* z = c.w<float>(c.W.off_m2);
@@ -1074,9 +1111,9 @@ Plan make_plan(int64_t T, bool backward) {
 // Pipelined order (GEMM partition g, memory partition m, caller stream c):
 //   c: A(0) | g: G(0) G(1) ... G(C-1) | m: A(1), Z(0), A(2), Z(1), ... Z(C-2) | c: Z(C-1)
 poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X, int64_t T,
-                      __nv_bfloat16* Y, __nv_bfloat16* hs) {
+                      __nv_bfloat16* Y, __nv_bfloat16* hs, __nv_bfloat16* us) {
   const int m = c.d.m, n = c.d.n;
-  auto* u = c.w<__nv_bfloat16>(c.W.off_n1);
+  auto* u = us ? us : c.w<__nv_bfloat16>(c.W.off_n1);
   auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
   auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
   auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
@@ -1187,14 +1224,15 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
 }
 
 poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const float* dY,
-                      const float* hs, int64_t T, float* dX) {
+                      const float* hs, const float* us, int64_t T, float* dX) {
   const int m = c.d.m, n = c.d.n;
-  float* u = c.w<float>(c.W.off_n1);
+  float* ubuf = c.w<float>(c.W.off_n1);
   float* v = c.w<float>(c.W.off_n2);
   float* hbuf = c.w<float>(c.W.off_m1);
   float* dz = c.w<float>(c.W.off_m2);
   float* dh = c.w<float>(c.W.off_m3);
-  POETX_TRY(gather_cols<float>(c.st, X, u, c.piP(), T, n));
+  if (!us) POETX_TRY(gather_cols<float>(c.st, X, ubuf, c.piP(), T, n));
+  const float* u = us ? us : ubuf;
   const float* h = hs;
   {
     ProfScope prof(POETX_KIND_SIMT, c.st);
@@ -1207,7 +1245,7 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
   }
   POETX_TRY(gather_cols<float>(c.st, dY, dz, c.piR(), T, m));
   float* dv = v;
-  float* du = u;
+  float* du = ubuf;  // u is dead once the dv^T u reduction has read it (a saved u is not written)
   {
     ProfScope prof(POETX_KIND_SIMT, c.st);
     POETX_TRY(simt_gradblocks(c.st, c.L.R, dz, h, c.w<float>(c.W.off_GR), T, m));
@@ -1230,11 +1268,12 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
 // memory partition; chunk 0's first stages and the last chunk's final
 // stages on the caller's stream with the whole device.
 poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X,
-                      const __nv_bfloat16* dY, const __nv_bfloat16* hs, int64_t T,
-                      __nv_bfloat16* dX) {
+                      const __nv_bfloat16* dY, const __nv_bfloat16* hs, const __nv_bfloat16* us,
+                      int64_t T, __nv_bfloat16* dX) {
   const int m = c.d.m, n = c.d.n;
   const SideLayout &R = c.L.R, &P = c.L.P;
-  auto* u = c.w<__nv_bfloat16>(c.W.off_n1);
+  auto* ubuf = c.w<__nv_bfloat16>(c.W.off_n1);
+  const __nv_bfloat16* u = us ? us : ubuf;
   auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
   auto* hbuf = c.w<__nv_bfloat16>(c.W.off_m1);
   auto* dz = c.w<__nv_bfloat16>(c.W.off_m2);
@@ -1246,8 +1285,8 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   const auto* BsbPT = c.p<__nv_bfloat16>(P.off_BsbT);
   const bool recompute = (hs == nullptr);
   const __nv_bfloat16* h = recompute ? hbuf : hs;
-  auto* dv = v;   // v of a chunk is dead once its h is formed
-  auto* du = u;   // u of a chunk is dead once its dv^T u partials are formed
+  auto* dv = v;     // v of a chunk is dead once its h is formed
+  auto* du = ubuf;  // u of a chunk is dead once its dv^T u partials are formed (a saved u is not written)
   const int64_t strideR = static_cast<int64_t>(R.nsb) * R.sb * R.sb;
   const int64_t strideP = static_cast<int64_t>(P.nsb) * P.sb * P.sb;
   c.slotsR = c.slotsP = 0;
@@ -1256,7 +1295,7 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   auto RA = [&](int k, cudaStream_t st, int budget) -> poetx_status {
     CtaBudget bg(budget);
     const int64_t t0 = ch.t0[k], len = ch.len[k];
-    POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, u + t0 * n, c.piP(), len, n));
+    if (!us) POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, ubuf + t0 * n, c.piP(), len, n));
     if (!recompute) return POETX_OK;
     return tc_blockdiag(st, u + t0 * n, BsbP, v + t0 * n, len, n, P.sb, P.nsb);
   };
@@ -1364,6 +1403,42 @@ poetx_status check_tensor(const void* p) {
   return POETX_OK;
 }
 
+// Merge scratch.  fp32 layers: T1 = W0' B_P and K = B_R T1 (fp32, m x n).
+// bf16 layers (tensor-core passes): W1 = (W0' B_P)^T as a bf16 hi/lo pair
+// (n x m each), K = B_R W0' B_P in bf16 (m x n), and the hi/lo super-block
+// arrays of B_P^T - I and B_R - I.  Both: the re-basing index maps rho.
+struct MergeLayout {
+  size_t off_T1, off_K;              // fp32
+  size_t off_W1hi, off_W1lo, off_Kb;  // bf16
+  size_t off_DPhi, off_DPlo, off_DRhi, off_DRlo;
+  size_t off_rhoR, off_rhoP;
+  size_t total;
+};
+
+MergeLayout merge_layout(const poetx_layer_desc& d, const ParamsLayout& L) {
+  MergeLayout M{};
+  const size_t mn = static_cast<size_t>(d.m) * d.n;
+  size_t off = 0;
+  if (d.dtype == POETX_DTYPE_FP32) {
+    M.off_T1 = off; off = align_up(off + mn * 4);
+    M.off_K = off;  off = align_up(off + mn * 4);
+  } else {
+    const size_t dp = static_cast<size_t>(L.P.nsb) * L.P.sb * L.P.sb * 2;
+    const size_t dr = static_cast<size_t>(L.R.nsb) * L.R.sb * L.R.sb * 2;
+    M.off_W1hi = off; off = align_up(off + mn * 2);
+    M.off_W1lo = off; off = align_up(off + mn * 2);
+    M.off_Kb = off;   off = align_up(off + mn * 2);
+    M.off_DPhi = off; off = align_up(off + dp);
+    M.off_DPlo = off; off = align_up(off + dp);
+    M.off_DRhi = off; off = align_up(off + dr);
+    M.off_DRlo = off; off = align_up(off + dr);
+  }
+  M.off_rhoR = off; off = align_up(off + static_cast<size_t>(d.m) * 4);
+  M.off_rhoP = off; off = align_up(off + static_cast<size_t>(d.n) * 4);
+  M.total = off;
+  return M;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -1460,8 +1535,8 @@ size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T) {
 }
 
 poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params, const void* W0p,
-                              const void* X, int64_t T, void* Y, void* saved_h, void* workspace,
-                              void* stream) {
+                              const void* X, int64_t T, void* Y, void* saved_h, void* saved_u,
+                              void* workspace, void* stream) {
   POETX_TRY(check_desc(desc));
   if (T < 0) return POETX_ERR_INVALID_ARG;
   if (T == 0) return POETX_OK;
@@ -1470,6 +1545,8 @@ poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params, 
   POETX_TRY(check_tensor(X));
   POETX_TRY(check_tensor(Y));
   if (saved_h) POETX_TRY(check_tensor(saved_h));
+  if (saved_u) POETX_TRY(check_tensor(saved_u));
+  if (saved_u && (saved_u == X || saved_u == Y || saved_u == saved_h)) return POETX_ERR_INVALID_ARG;
   if (!aligned(params, kAlign) || !aligned(workspace, kAlign)) return POETX_ERR_MISALIGNED;
   if (T > (int64_t(1) << 31) - 256) return POETX_ERR_UNSUPPORTED;
   const ParamsLayout L = params_layout(*desc);
@@ -1478,16 +1555,17 @@ poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params, 
         reinterpret_cast<cudaStream_t>(stream)};
   if (desc->dtype == POETX_DTYPE_FP32)
     return fwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X), T,
-                    reinterpret_cast<float*>(Y), reinterpret_cast<float*>(saved_h));
+                    reinterpret_cast<float*>(Y), reinterpret_cast<float*>(saved_h),
+                    reinterpret_cast<float*>(saved_u));
   return fwd_bf16(c, reinterpret_cast<const __nv_bfloat16*>(W0p),
                   reinterpret_cast<const __nv_bfloat16*>(X), T, reinterpret_cast<__nv_bfloat16*>(Y),
-                  reinterpret_cast<__nv_bfloat16*>(saved_h));
+                  reinterpret_cast<__nv_bfloat16*>(saved_h), reinterpret_cast<__nv_bfloat16*>(saved_u));
 }
 
 poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params, const void* W0p,
-                              const void* X, const void* dY, const void* saved_h, int64_t T, void* dX,
-                              float* dGenR, float* dGenP, int32_t accumulate, void* workspace,
-                              void* stream) {
+                              const void* X, const void* dY, const void* saved_h,
+                              const void* saved_u, int64_t T, void* dX, float* dGenR, float* dGenP,
+                              int32_t accumulate, void* workspace, void* stream) {
   POETX_TRY(check_desc(desc));
   if (T < 0) return POETX_ERR_INVALID_ARG;
   if (!params || !workspace) return POETX_ERR_INVALID_ARG;
@@ -1506,7 +1584,8 @@ poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params, 
     return POETX_OK;
   }
   POETX_TRY(check_tensor(W0p));
-  POETX_TRY(check_tensor(X));
+  if (saved_u) POETX_TRY(check_tensor(saved_u));
+  else POETX_TRY(check_tensor(X));  // X is read only to form u
   POETX_TRY(check_tensor(dY));
   if (saved_h) POETX_TRY(check_tensor(saved_h));
   if (dX) POETX_TRY(check_tensor(dX));
@@ -1518,22 +1597,21 @@ poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params, 
         reinterpret_cast<const uint8_t*>(params), reinterpret_cast<uint8_t*>(workspace), st};
   if (desc->dtype == POETX_DTYPE_FP32)
     POETX_TRY(bwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X),
-                       reinterpret_cast<const float*>(dY), reinterpret_cast<const float*>(saved_h), T,
-                       reinterpret_cast<float*>(dX)));
+                       reinterpret_cast<const float*>(dY), reinterpret_cast<const float*>(saved_h),
+                       reinterpret_cast<const float*>(saved_u), T, reinterpret_cast<float*>(dX)));
   else
     POETX_TRY(bwd_bf16(c, reinterpret_cast<const __nv_bfloat16*>(W0p),
                        reinterpret_cast<const __nv_bfloat16*>(X),
                        reinterpret_cast<const __nv_bfloat16*>(dY),
-                       reinterpret_cast<const __nv_bfloat16*>(saved_h), T,
+                       reinterpret_cast<const __nv_bfloat16*>(saved_h),
+                       reinterpret_cast<const __nv_bfloat16*>(saved_u), T,
                        reinterpret_cast<__nv_bfloat16*>(dX)));
   return bwd_common_tail(c, dGenR, dGenP, accumulate);
 }
 
 size_t poetx_merge_workspace_size(const poetx_layer_desc* desc) {
   if (check_desc(desc) != POETX_OK) return 0;
-  const size_t mn = static_cast<size_t>(desc->m) * desc->n * 4;
-  return align_up(mn) * 2 + align_up(static_cast<size_t>(desc->m) * 4) +
-         align_up(static_cast<size_t>(desc->n) * 4);
+  return merge_layout(*desc, params_layout(*desc)).total;
 }
 
 poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void* W0p,
@@ -1545,23 +1623,41 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int m = desc->m, n = desc->n;
   const ParamsLayout L = params_layout(*desc);
+  const MergeLayout ML = merge_layout(*desc, L);
   const uint8_t* pb = reinterpret_cast<const uint8_t*>(params);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  const size_t mn = align_up(static_cast<size_t>(m) * n * 4);
-  float* T1 = reinterpret_cast<float*>(ws);
-  float* K = reinterpret_cast<float*>(ws + mn);
-  int32_t* rhoR = reinterpret_cast<int32_t*>(ws + 2 * mn);
-  int32_t* rhoP = reinterpret_cast<int32_t*>(ws + 2 * mn + align_up(static_cast<size_t>(m) * 4));
+  int32_t* rhoR = reinterpret_cast<int32_t*>(ws + ML.off_rhoR);
+  int32_t* rhoP = reinterpret_cast<int32_t*>(ws + ML.off_rhoP);
   ProfScope prof(POETX_KIND_MERGE, st);
-  // T1 = W0' blockdiag(B_P): row-local blocks along n (not transposed).
-  if (desc->dtype == POETX_DTYPE_BF16)
-    POETX_TRY(simt_blocks<__nv_bfloat16, float>(st, L.P, pb, reinterpret_cast<const __nv_bfloat16*>(W0p),
-                                                T1, m, n, false));
-  else
+  const bool bf16 = desc->dtype == POETX_DTYPE_BF16;
+  float* T1 = reinterpret_cast<float*>(ws + ML.off_T1);
+  float* K = reinterpret_cast<float*>(ws + ML.off_K);
+  auto* Kb = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_Kb);
+  if (bf16) {
+    // Tensor-core passes with the identity split (tc_merge.cuh):
+    //   W1 = (W0' B_P)^T as hi/lo, then K = (W1 B_R^T)^T = B_R W0' B_P.
+    auto* W1hi = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_W1hi);
+    auto* W1lo = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_W1lo);
+    auto* DPhi = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_DPhi);
+    auto* DPlo = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_DPlo);
+    auto* DRhi = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_DRhi);
+    auto* DRlo = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_DRlo);
+    const float* BP = reinterpret_cast<const float*>(pb + L.P.off_B);
+    const float* BR = reinterpret_cast<const float*>(pb + L.R.off_B);
+    delta_superblock_kernel<<<grid_for(static_cast<int64_t>(L.P.nsb) * L.P.sb * L.P.sb), 256, 0, st>>>(
+        BP, L.P.g, L.P.sb, L.P.nsb, 1, DPhi, DPlo);
+    POETX_LAUNCHED();
+    delta_superblock_kernel<<<grid_for(static_cast<int64_t>(L.R.nsb) * L.R.sb * L.R.sb), 256, 0, st>>>(
+        BR, L.R.g, L.R.sb, L.R.nsb, 0, DRhi, DRlo);
+    POETX_LAUNCHED();
+    POETX_TRY(tc_merge_pass<false>(st, reinterpret_cast<const __nv_bfloat16*>(W0p), nullptr, m, n,
+                                   L.P.sb, L.P.nsb, DPhi, DPlo, W1hi, W1lo));
+    POETX_TRY(tc_merge_pass<true>(st, W1hi, W1lo, n, m, L.R.sb, L.R.nsb, DRhi, DRlo, Kb, nullptr));
+  } else {
+    // T1 = W0' blockdiag(B_P): row-local blocks along n (not transposed).
     POETX_TRY(simt_blocks<float, float>(st, L.P, pb, reinterpret_cast<const float*>(W0p), T1, m, n,
                                         false));
-  // K = blockdiag(B_R) T1: block k of rows is B_R,k (b x b) times T1[rows of k, :].
-  {
+    // K = blockdiag(B_R) T1: block k of rows is B_R,k (b x b) times T1[rows of k, :].
     const SideLayout& S = L.R;
     const int b = S.g.b;
     const int64_t bb = static_cast<int64_t>(b) * b;
@@ -1587,9 +1683,9 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
   for (int j = 0; j < n; ++j) rP[j] = oPi[nP[j]];
   POETX_TRY(ring_upload(st, {{rR.data(), rR.size()}, {rP.data(), rP.size()}}, {rhoR, rhoP}));
   const int grid = std::min(m, device_sm_count() * 8);
-  if (desc->dtype == POETX_DTYPE_BF16)
-    gather2d_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(
-        K, reinterpret_cast<__nv_bfloat16*>(W0p), rhoR, rhoP, m, n);
+  if (bf16)
+    gather2d_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(
+        Kb, reinterpret_cast<__nv_bfloat16*>(W0p), rhoR, rhoP, m, n);
   else
     gather2d_kernel<float, float><<<grid, 256, 0, st>>>(K, reinterpret_cast<float*>(W0p), rhoR, rhoP,
                                                         m, n);
@@ -1599,9 +1695,10 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
 
 poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params, const void* W0p,
                                     const void* X_host, const void* dY_host, int64_t T, void* X_dev,
-                                    void* dY_dev, void* Y_dev, void* saved_h_dev, void* dX_dev,
-                                    float* dGenR_dev, float* dGenP_dev, float* dGenR_host,
-                                    float* dGenP_host, void* workspace, void* stream) {
+                                    void* dY_dev, void* Y_dev, void* saved_h_dev, void* saved_u_dev,
+                                    void* dX_dev, float* dGenR_dev, float* dGenP_dev,
+                                    float* dGenR_host, float* dGenP_host, void* workspace,
+                                    void* stream) {
   POETX_TRY(check_desc(desc));
   if (T < 0 || !X_host || !dY_host || !X_dev || !dY_dev || !dGenR_host || !dGenP_host)
     return POETX_ERR_INVALID_ARG;
@@ -1611,9 +1708,10 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
                              cudaMemcpyHostToDevice, st));
   POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
                              cudaMemcpyHostToDevice, st));
-  POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, workspace, stream));
-  POETX_TRY(poetx_linear_bwd(desc, params, W0p, X_dev, dY_dev, saved_h_dev, T, dX_dev, dGenR_dev,
-                             dGenP_dev, 0, workspace, stream));
+  POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, saved_u_dev, workspace,
+                             stream));
+  POETX_TRY(poetx_linear_bwd(desc, params, W0p, X_dev, dY_dev, saved_h_dev, saved_u_dev, T, dX_dev,
+                             dGenR_dev, dGenP_dev, 0, workspace, stream));
   const int64_t lr = poetx_gen_length(desc->m, desc->b_R), lp = poetx_gen_length(desc->n, desc->b_P);
   if (lr > 0)
     POETX_CUDA(cudaMemcpyAsync(dGenR_host, dGenR_dev, lr * 4, cudaMemcpyDeviceToHost, st));
@@ -1731,7 +1829,7 @@ void* g_noalloc_addr[kNoAllocMaxDevices] = {};
 
 extern "C" poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* params,
                                                  const void* W0p, const void* X, int64_t T, void* Y,
-                                                 void* saved_h, void* stream) {
+                                                 void* saved_h, void* saved_u, void* stream) {
   POETX_TRY(check_desc(desc));
   if (T < 0) return POETX_ERR_INVALID_ARG;
   if (T == 0) return POETX_OK;
@@ -1750,7 +1848,7 @@ extern "C" poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, c
     }
     scratch = g_noalloc_addr[dev];
   }
-  return poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, scratch, stream);
+  return poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, saved_u, scratch, stream);
 }
 
 extern "C" {

@@ -680,6 +680,34 @@ __global__ void __launch_bounds__(256) superblock_kernel(const float* __restrict
   }
 }
 
+// Super-block array of the blocks minus the identity, D = B - I (or
+// B^T - I with `transpose`), each entry split into two bf16 terms hi + lo
+// with hi = bf16(v) and lo = bf16(v - hi), for the tensor-core merge.  The
+// layout is that of superblock_kernel; entries outside the d x d matrix are 0.
+__global__ void __launch_bounds__(256) delta_superblock_kernel(const float* __restrict__ B, SideGeom s,
+                                                               int sb, int nsb, int transpose,
+                                                               __nv_bfloat16* __restrict__ hi,
+                                                               __nv_bfloat16* __restrict__ lo) {
+  const int64_t bb = static_cast<int64_t>(s.b) * s.b;
+  const int64_t total = static_cast<int64_t>(nsb) * sb * sb;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(e / sb), c = static_cast<int>(e % sb);
+    const int f = (r / sb) * sb + c;
+    const int k = r / s.b;
+    float v = 0.f;
+    if (r < s.d && f < s.d && f / s.b == k) {
+      const int i = r - k * s.b, j = f - k * s.b;
+      v = transpose ? B[k * bb + static_cast<int64_t>(j) * s.b + i]
+                    : B[k * bb + static_cast<int64_t>(i) * s.b + j];
+      if (r == f) v -= 1.f;
+    }
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[e] = h;
+    lo[e] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
 // ------------------------------------------------------------------ gradients
 // G[k](i,j) = sum over splits p of partial[p][s][(a - s*sb)][(c - s*sb)],
 // a = k*b + i, c = k*b + j, s = a / sb, in a fixed order (deterministic).

@@ -26,8 +26,12 @@ def make_inputs(m, n, bR, bP, T, dtype, index=0, t0=0, t1=None, gstd=synth.STD_G
     return inp
 
 
-def run_gpu(px, desc, inp, recompute: bool, want_dX=True, dev="cuda"):
-    """Forward + backward through the C ABI; returns CPU float64 numpy arrays."""
+def run_gpu(px, desc, inp, recompute: bool, want_dX=True, dev="cuda", save_u=False):
+    """Forward + backward through the C ABI; returns CPU float64 numpy arrays.
+
+    recompute: h is not saved by the forward.  save_u: the forward saves the
+    permuted input u and the backward gets it instead of X (X is passed as
+    NULL there, so the backward cannot read it)."""
     T = inp.X.shape[0]
     layer = px.Layer(desc, max(T, 1), device=dev)
     layer.build(inp.genR.to(dev), inp.genP.to(dev))
@@ -37,16 +41,17 @@ def run_gpu(px, desc, inp, recompute: bool, want_dX=True, dev="cuda"):
     dY = inp.dY.to(dev)
     Y = torch.empty(T, desc.m, dtype=layer.dtype, device=dev)
     h = None if recompute else torch.empty(T, desc.m, dtype=layer.dtype, device=dev)
-    layer.forward(X, Y, saved_h=h)
+    u = torch.empty(T, desc.n, dtype=layer.dtype, device=dev) if save_u else None
+    layer.forward(X, Y, saved_h=h, saved_u=u)
     dX = torch.empty(T, desc.n, dtype=layer.dtype, device=dev) if want_dX else None
     dgR = torch.empty(layer.len_R, dtype=torch.float32, device=dev)
     dgP = torch.empty(layer.len_P, dtype=torch.float32, device=dev)
-    layer.backward(X, dY, dX, dgR, dgP, saved_h=h)
+    layer.backward(None if save_u else X, dY, dX, dgR, dgP, saved_h=h, saved_u=u)
     torch.cuda.synchronize()
     st = px.poetx_device_status(reset=True)
     assert st == px.POETX_OK, px.poetx_status_string(st)
     f = lambda t: None if t is None else t.double().cpu().numpy()
-    return dict(Y=f(Y), dX=f(dX), dgR=f(dgR), dgP=f(dgP), W0p=f(layer.W0p), layer=layer)
+    return dict(Y=f(Y), dX=f(dX), dgR=f(dgR), dgP=f(dgP), W0p=f(layer.W0p), u=f(u), layer=layer)
 
 
 def run_oracle(spec: O.LayerSpec, inp):

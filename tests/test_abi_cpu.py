@@ -93,17 +93,23 @@ def test_argument_errors_return_before_launch():
     L = px.LIB
     D = ctypes.byref(d)
     # null params / workspace
-    assert L.poetx_linear_fwd(D, None, 256, 256, 4, 256, None, 256, None) == px.POETX_ERR_INVALID_ARG
+    assert L.poetx_linear_fwd(D, None, 256, 256, 4, 256, None, None, 256, None) == px.POETX_ERR_INVALID_ARG
     # misaligned tensor pointer (not 16-byte aligned)
-    assert L.poetx_linear_fwd(D, 256, 264 + 2, 256, 4, 256, None, 256, None) == px.POETX_ERR_MISALIGNED
+    assert L.poetx_linear_fwd(D, 256, 264 + 2, 256, 4, 256, None, None, 256, None) == px.POETX_ERR_MISALIGNED
     # misaligned params buffer (not 256-byte aligned)
-    assert L.poetx_linear_fwd(D, 272, 256, 256, 4, 256, None, 256, None) == px.POETX_ERR_MISALIGNED
+    assert L.poetx_linear_fwd(D, 272, 256, 256, 4, 256, None, None, 256, None) == px.POETX_ERR_MISALIGNED
     # negative token count
-    assert L.poetx_linear_fwd(D, 256, 256, 256, -1, 256, None, 256, None) == px.POETX_ERR_INVALID_ARG
+    assert L.poetx_linear_fwd(D, 256, 256, 256, -1, 256, None, None, 256, None) == px.POETX_ERR_INVALID_ARG
     # T == 0 is a no-op
-    assert L.poetx_linear_fwd(D, 256, 256, 256, 0, 256, None, 256, None) == px.POETX_OK
+    assert L.poetx_linear_fwd(D, 256, 256, 256, 0, 256, None, None, 256, None) == px.POETX_OK
     # backward needs generator-gradient outputs
-    assert L.poetx_linear_bwd(D, 256, 256, 256, 256, None, 4, None, None, None, 0, 256,
+    assert L.poetx_linear_bwd(D, 256, 256, 256, 256, None, None, 4, None, None, None, 0, 256,
+                              None) == px.POETX_ERR_INVALID_ARG
+    # a saved u must not alias the input or the output
+    assert L.poetx_linear_fwd(D, 256, 256, 512, 4, 768, None, 512, 256, None) == px.POETX_ERR_INVALID_ARG
+    assert L.poetx_linear_fwd(D, 256, 256, 512, 4, 768, None, 768, 256, None) == px.POETX_ERR_INVALID_ARG
+    # the backward needs X or a saved u
+    assert L.poetx_linear_bwd(D, 256, 256, None, 256, None, None, 4, None, 256, 256, 0, 256,
                               None) == px.POETX_ERR_INVALID_ARG
     # invalid descriptor
     bad = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32")

@@ -49,12 +49,14 @@ def _run(px, desc, params, W0p, X, dY, T, recompute, dgR, dgP, accumulate=False,
     dt = torch.bfloat16
     ws = torch.empty(px.poetx_workspace_size(desc, T), dtype=torch.uint8, device=dev)
     Y = torch.empty(T, m, dtype=dt, device=dev) if want_out else None
+    # as in the benchmark: stored-activation workloads keep h and u, recompute ones neither
     h = None if recompute else torch.empty(T, m, dtype=dt, device=dev)
+    u = None if recompute else torch.empty(T, n, dtype=dt, device=dev)
     dX = torch.empty(T, n, dtype=dt, device=dev) if want_out else None
     if want_out or not recompute:
         Yb = Y if Y is not None else torch.empty(T, m, dtype=dt, device=dev)
-        px.poetx_linear_fwd(desc, params, W0p, X, T, Yb, h, ws)
-    px.poetx_linear_bwd(desc, params, W0p, X, dY, h, T, dX, dgR, dgP, accumulate, ws)
+        px.poetx_linear_fwd(desc, params, W0p, X, T, Yb, h, u, ws)
+    px.poetx_linear_bwd(desc, params, W0p, X, dY, h, u, T, dX, dgR, dgP, accumulate, ws)
     return Y, dX
 
 

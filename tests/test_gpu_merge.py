@@ -79,3 +79,33 @@ def test_premerge_is_an_exact_permutation_copy(px):
     piR, piP = O.permutation(inp.seed_R, m), O.permutation(inp.seed_P, n)
     want = inp.W0.float().numpy()[piR][:, piP]
     assert np.array_equal(layer.W0p.float().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("m,n,b", [(384, 256, 32), (512, 640, 128), (768, 512, 256)])
+def test_bf16_merge_is_rounded_once_from_a_near_exact_product(px, m, n, b):
+    """The bf16 merge runs on the tensor cores with bf16 operands, splitting
+    B - I and the intermediate into hi + lo bf16 pairs; the result must still
+    be the exact R W0 P (re-based) rounded once to bf16: every element within
+    half a bf16 ulp of the fp64 oracle's value, plus slack at the fp32 level
+    (the blocks themselves are built in fp32)."""
+    inp = make_inputs(m, n, b, b, 1, "bf16", index=7, gstd=0.05)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16")
+    layer = px.Layer(desc, 1)
+    layer.build(inp.genR.cuda(), inp.genP.cuda())
+    layer.premerge(inp.W0.cuda())
+    new_R, new_P = 8303, 9304
+    layer.merge(new_R, new_P)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+    got = layer.W0p.double().cpu().numpy()
+    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P)
+    want = O.merge(spec, inp.W0.double().numpy(), inp.genR.double().numpy(),
+                   inp.genP.double().numpy(), new_R, new_P)
+    a = np.abs(want)
+    tiny = np.finfo(np.float64).tiny
+    half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, tiny))) - 8)   # bf16: 8 significant bits
+    slack = 2e-5 * a + 1e-5 * a.max()
+    err = np.abs(got - want)
+    bad = err > half_ulp + slack
+    assert not bad.any(), (f"{bad.sum()} elements beyond half an ulp; worst excess "
+                           f"{(err - half_ulp - slack).max():.3e}")

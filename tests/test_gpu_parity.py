@@ -31,14 +31,19 @@ def px():
     return m
 
 
-def _case(px, m, n, bR, bP, T, dtype, mode="cayley", k=3, recompute=False, index=0, gstd=0.01):
+def _case(px, m, n, bR, bP, T, dtype, mode="cayley", k=3, recompute=False, index=0, gstd=0.01,
+          save_u=False):
     inp = make_inputs(m, n, bR, bP, T, dtype, index=index, gstd=gstd)
     desc = px.make_desc(m, n, bR, bP, inp.seed_R, inp.seed_P, dtype=dtype, mode=mode, neumann_k=k)
     spec = O.LayerSpec(m, n, bR, bP, inp.seed_R, inp.seed_P,
                        "neumann" if mode == "neumann" else "exact", k)
-    g = run_gpu(px, desc, inp, recompute)
+    g = run_gpu(px, desc, inp, recompute, save_u=save_u)
     o = run_oracle(spec, inp)
     assert np.array_equal(g["W0p"], o["W0p"]), "pre-merged weight must be a bit-exact copy"
+    if save_u:
+        # u = X[:, pi_P] is a permutation copy of the input: bit-exact
+        u_o = inp.X.double().numpy()[:, O.permutation(inp.seed_P, n)]
+        assert np.array_equal(g["u"], u_o), "saved u must be the permuted input, bit for bit"
     tol = TOL[dtype]
     errs = {k_: rel_fro(g[k_], o[k_]) for k_ in ("Y", "dX", "dgR", "dgP") if o[k_].size}
     for k_, e in errs.items():
@@ -70,6 +75,15 @@ def test_fp32_blocked_builder_b256(px):
 @pytest.mark.parametrize("recompute", [False, True])
 def test_bf16_b32_ragged_tokens(px, recompute):
     _case(px, 384, 256, 32, 32, 1000, "bf16", recompute=recompute)
+
+
+@pytest.mark.parametrize("dtype,recompute", [("fp32", False), ("fp32", True),
+                                             ("bf16", False), ("bf16", True)])
+def test_saved_u_replaces_the_input_in_the_backward(px, dtype, recompute):
+    """The forward keeps u = X[:, pi_P]; the backward gets it instead of X
+    (X is NULL there), with h saved or recomputed."""
+    bs = 32 if dtype == "fp32" else 128
+    _case(px, 384, 256, bs, bs, 300, dtype, recompute=recompute, save_u=True)
 
 
 def test_bf16_b64(px):

@@ -47,7 +47,7 @@ def test_noalloc_forward_matches_workspace_forward_twice(px, keep_h):
     for call in range(2):
         Y = torch.full((T, m), float("nan"), dtype=torch.bfloat16, device="cuda")
         h = torch.empty(T, m, dtype=torch.bfloat16, device="cuda") if keep_h else None
-        px.poetx_linear_fwd_noalloc(desc, layer.params, layer.W0p, X, T, Y, h)
+        px.poetx_linear_fwd_noalloc(desc, layer.params, layer.W0p, X, T, Y, h, None)
         torch.cuda.synchronize()
         assert px.poetx_device_status(reset=True) == px.POETX_OK
         y, yr = Y.double().cpu().numpy(), Y_ref.double().cpu().numpy()
@@ -68,5 +68,5 @@ def test_noalloc_forward_refuses_oversized_requests(px):
     T = 65536
     assert px.poetx_workspace_size(desc, T) > px.NOALLOC_SCRATCH_BYTES
     with pytest.raises(px.PoetxError) as ei:
-        px.poetx_linear_fwd_noalloc(desc, 256, 256, 256, T, 256, None)
+        px.poetx_linear_fwd_noalloc(desc, 256, 256, 256, T, 256, None, None)
     assert ei.value.status == px.POETX_ERR_UNSUPPORTED
