@@ -1186,15 +1186,22 @@ poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_
   const size_t smem = 3 * static_cast<size_t>(b) * (b + 4) * 4;
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(cayley_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         3 * 128 * 132 * 4);
     cudaFuncSetAttribute(cayley_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          3 * 64 * 68 * 4);
   });
   const float* M = reinterpret_cast<const float*>(params + S.off_M);
   const int64_t stride = static_cast<int64_t>(S.nsb) * S.sb * S.sb;
-  auto kern = b == 128 ? cayley_bwd_kernel<128> : b == 64 ? cayley_bwd_kernel<64> : cayley_bwd_kernel<32>;
-  const int threads = (b / 4) * (b / 4);
+  if (b == 128) {  // four CTAs (one cluster) per block
+    static cudaError_t attr_err = cudaFuncSetAttribute(
+        cayley_bwd_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCbwdSmem);
+    if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+    cayley_bwd_cluster_kernel<<<S.g.nblk * 4, 256, kCbwdSmem, st>>>(partial, stride, splits, S.g, M,
+                                                                  dGen, accumulate);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
+  auto kern = b == 64 ? cayley_bwd_kernel<64> : cayley_bwd_kernel<32>;
+  const int threads = b == 64 ? cbwd_threads<64>() : cbwd_threads<32>();
   kern<<<S.g.nblk, threads, smem, st>>>(partial, stride, splits, S.g, S.sb, M, dGen, accumulate);
   POETX_LAUNCHED();
   return POETX_OK;

@@ -758,74 +758,116 @@ __global__ void __launch_bounds__(256) pack_grad_kernel(const float* __restrict_
 // shared memory with rows padded to P + 4 floats so 16-byte loads stay
 // aligned.  The second product reads T^T and M^T so both operands are
 // contiguous along the loop.
+// Threads of cayley_bwd_kernel<P>: the (P/4)^2 that hold a 4 x 4 tile of the
+// matrix products, and at least 256 so the split reduction has enough loads
+// in flight.
 template <int P>
-__global__ void __launch_bounds__((P / 4) * (P / 4)) cayley_bwd_kernel(
+__host__ __device__ constexpr int cbwd_threads() {
+  return (P / 4) * (P / 4) > 256 ? (P / 4) * (P / 4) : 256;
+}
+
+template <int P>
+__global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
     const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s, int sb,
     const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
   constexpr int LD = P + 4;
-  constexpr int NT = (P / 4) * (P / 4);
+  constexpr int NT = cbwd_threads<P>();
+  constexpr int CT = (P / 4) * (P / 4);  // threads of the matrix products
   extern __shared__ __align__(16) float cbs[];
   float* Gs = cbs;             // G, then T^T
   float* Ms = cbs + P * LD;    // M, then GQ
   float* Mt = Ms + P * LD;     // M^T
   const int k = blockIdx.x;
   const float* Mk = Mall + static_cast<int64_t>(k) * P * P;
-  for (int e = threadIdx.x; e < P * P; e += NT) {
-    const int i = e / P, j = e % P;
-    const int a = k * P + i, c = k * P + j;   // features of this block
-    const int sbi = a / sb;
-    const int64_t off = static_cast<int64_t>(sbi) * sb * sb +
-                        static_cast<int64_t>(a - sbi * sb) * sb + (c - sbi * sb);
-    float v = 0.f;
-    for (int p = 0; p < splits; ++p) v += partial[p * split_stride + off];
-    Gs[i * LD + j] = v;
-    const float m = Mk[e];
-    Ms[i * LD + j] = m;
-    Mt[j * LD + i] = m;
+  // block k (P <= sb) lies inside super-block (k * P) / sb at offset o0 on the diagonal
+  const int sbi = (k * P) / sb, o0 = k * P - sbi * sb;
+  const float* Pk = partial + static_cast<int64_t>(sbi) * sb * sb + static_cast<int64_t>(o0) * sb + o0;
+  // G (summed over splits in a fixed order) and M: PER float4 of each per
+  // thread, the loads of one split all in flight together
+  constexpr int PER = P * P / 4 / NT;
+  static_assert(PER * NT == P * P / 4, "threads must tile the block");
+  float4 g[PER], mv[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = threadIdx.x + NT * u;
+    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
+    g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    mv[u] = *reinterpret_cast<const float4*>(Mk + i * P + j4);
+  }
+  for (int p = 0; p < splits; ++p) {
+    float4 w[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = threadIdx.x + NT * u;
+      const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
+      w[u] = *reinterpret_cast<const float4*>(Pk + p * split_stride + static_cast<int64_t>(i) * sb + j4);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      g[u].x += w[u].x; g[u].y += w[u].y; g[u].z += w[u].z; g[u].w += w[u].w;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = threadIdx.x + NT * u;
+    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
+    *reinterpret_cast<float4*>(Gs + i * LD + j4) = g[u];
+    *reinterpret_cast<float4*>(Ms + i * LD + j4) = mv[u];
+    Mt[(j4 + 0) * LD + i] = mv[u].x;
+    Mt[(j4 + 1) * LD + i] = mv[u].y;
+    Mt[(j4 + 2) * LD + i] = mv[u].z;
+    Mt[(j4 + 3) * LD + i] = mv[u].w;
   }
   __syncthreads();
-  const int tr = threadIdx.x / (P / 4), tc = threadIdx.x % (P / 4);
+  const bool mm = threadIdx.x < CT;  // holds a tile of the products
+  const int tr = (threadIdx.x % CT) / (P / 4), tc = threadIdx.x % (P / 4);
   float acc[4][4];
   // T = M^T G: T[i][j] = sum_q M[q][i] G[q][j]
 #pragma unroll
   for (int x = 0; x < 4; ++x)
 #pragma unroll
     for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+  if (mm) {
 #pragma unroll 4
-  for (int q = 0; q < P; ++q) {
-    const float4 a = *reinterpret_cast<const float4*>(Ms + q * LD + 4 * tr);
-    const float4 g = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
-    const float av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+    for (int q = 0; q < P; ++q) {
+      const float4 a = *reinterpret_cast<const float4*>(Ms + q * LD + 4 * tr);
+      const float4 g = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
+      const float av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], gv[y], acc[x][y]);
+    }
+  }
+  __syncthreads();
+  if (mm) {
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
-      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], gv[y], acc[x][y]);
+      for (int y = 0; y < 4; ++y) Gs[(4 * tc + y) * LD + 4 * tr + x] = acc[x][y];  // T^T
   }
-  __syncthreads();
-#pragma unroll
-  for (int x = 0; x < 4; ++x)
-#pragma unroll
-    for (int y = 0; y < 4; ++y) Gs[(4 * tc + y) * LD + 4 * tr + x] = acc[x][y];  // T^T
   __syncthreads();
   // GQ = 2 T M^T: GQ[i][j] = 2 sum_q T^T[q][i] M^T[q][j]
-#pragma unroll
-  for (int x = 0; x < 4; ++x)
-#pragma unroll
-    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
-#pragma unroll 4
-  for (int q = 0; q < P; ++q) {
-    const float4 t = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tr);
-    const float4 m = *reinterpret_cast<const float4*>(Mt + q * LD + 4 * tc);
-    const float tv[4] = {t.x, t.y, t.z, t.w}, mv[4] = {m.x, m.y, m.z, m.w};
+  if (mm) {
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
-      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mv[y], acc[x][y]);
-  }
+      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < P; ++q) {
+      const float4 t = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tr);
+      const float4 m = *reinterpret_cast<const float4*>(Mt + q * LD + 4 * tc);
+      const float tv[4] = {t.x, t.y, t.z, t.w}, mv[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-  for (int x = 0; x < 4; ++x)
-    *reinterpret_cast<float4*>(Ms + (4 * tr + x) * LD + 4 * tc) =
-        make_float4(2.f * acc[x][0], 2.f * acc[x][1], 2.f * acc[x][2], 2.f * acc[x][3]);
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mv[y], acc[x][y]);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      *reinterpret_cast<float4*>(Ms + (4 * tr + x) * LD + 4 * tc) =
+          make_float4(2.f * acc[x][0], 2.f * acc[x][1], 2.f * acc[x][2], 2.f * acc[x][3]);
+  }
   __syncthreads();
   // pack: one warp per row
   const int sz = block_size(s, k);
@@ -839,6 +881,152 @@ __global__ void __launch_bounds__((P / 4) * (P / 4)) cayley_bwd_kernel(
       else oi[j] = v;
     }
   }
+}
+
+// The same computation for 128 x 128 blocks on a cluster of four CTAs per
+// block: CTA r owns rows [32r, 32r + 32) of G, T = M^T G and GQ = 2 T M^T.
+//   1. reduce its rows of G from the partials; load its rows of M
+//   2. cluster barrier; copy the other CTAs' rows of G and M over
+//      distributed shared memory; cluster barrier (after it G's storage is
+//      reused)
+//   3. its rows of T (needs all of G and its columns of M), stored as T^T
+//   4. its rows of GQ (needs its rows of T and all of M, read as M^T)
+//   5. cluster barrier; pack its rows, reading GQ[j][i] from the CTA that
+//      owns row j; cluster barrier so no CTA exits while another reads it.
+// Every CTA runs every cluster barrier (no early exit).  256 threads, each
+// holding a 4 x 4 tile of the 32 x 128 output rows.
+constexpr int kCbwdLD = 132;        // padded row of a 128-wide fp32 matrix
+constexpr int kCbwdTLD = 36;        // padded row of T^T (32 wide)
+constexpr int kCbwdSmem = (2 * 128 * kCbwdLD + 128 * kCbwdTLD + 32 * kCbwdLD) * 4;
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(256) cayley_bwd_cluster_kernel(
+    const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s,
+    const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
+  constexpr int P = 128, LD = kCbwdLD, TLD = kCbwdTLD;
+  extern __shared__ __align__(16) float cbs[];
+  float* Gs = cbs;               // G (all rows), then M^T
+  float* Ms = Gs + P * LD;       // M
+  float* Tt = Ms + P * LD;       // T^T: Tt[q][i - r0]
+  float* Qs = Tt + P * TLD;      // GQ rows [r0, r0 + 32)
+  const uint32_t rank = cluster_ctarank();
+  const int k = blockIdx.x / 4;
+  const int r0 = 32 * static_cast<int>(rank);
+  const int tid = threadIdx.x;
+  const float* Mk = Mall + static_cast<int64_t>(k) * P * P;
+  const float* Pk = partial + static_cast<int64_t>(k) * P * P;  // super-block k (sb = 128)
+
+  // 1. own rows of G (summed over splits in a fixed order) and of M: four
+  //    float4 of each per thread, all loads of one split in flight together
+  {
+    constexpr int PER = 32 * P / 4 / 256;  // 4
+    float4 g[PER], m[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + 256 * u;
+      const int i = r0 + e / (P / 4), j4 = 4 * (e % (P / 4));
+      g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      m[u] = *reinterpret_cast<const float4*>(Mk + i * P + j4);
+    }
+    for (int p = 0; p < splits; ++p) {
+      float4 w[PER];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int e = tid + 256 * u;
+        const int i = r0 + e / (P / 4), j4 = 4 * (e % (P / 4));
+        w[u] = *reinterpret_cast<const float4*>(Pk + p * split_stride + i * P + j4);
+      }
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        g[u].x += w[u].x; g[u].y += w[u].y; g[u].z += w[u].z; g[u].w += w[u].w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + 256 * u;
+      const int i = r0 + e / (P / 4), j4 = 4 * (e % (P / 4));
+      *reinterpret_cast<float4*>(Gs + i * LD + j4) = g[u];
+      *reinterpret_cast<float4*>(Ms + i * LD + j4) = m[u];
+    }
+  }
+  cluster_sync();
+  // 2. the other CTAs' rows of G and M over distributed shared memory
+#pragma unroll 4
+  for (int e = tid; e < 3 * 32 * P / 4; e += 256) {
+    const uint32_t other = (rank + 1 + e / (32 * P / 4)) & 3u;
+    const int f = e % (32 * P / 4);
+    const int o = (32 * static_cast<int>(other) + f / (P / 4)) * LD + 4 * (f % (P / 4));
+    const float4 gv = dsmem_ld_f4(dsmem_addr(Gs + o, other));
+    const float4 mv = dsmem_ld_f4(dsmem_addr(Ms + o, other));
+    *reinterpret_cast<float4*>(Gs + o) = gv;
+    *reinterpret_cast<float4*>(Ms + o) = mv;
+  }
+  cluster_sync();
+  // 3. T[i][j] = sum_q M[q][i] G[q][j] for i in [r0, r0 + 32)
+  const int tr = tid / 32, tc = tid % 32;  // rows 4tr.., columns 4tc..
+  float acc[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < P; ++q) {
+    const float4 a = *reinterpret_cast<const float4*>(Ms + q * LD + r0 + 4 * tr);
+    const float4 g = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
+    const float av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], gv[y], acc[x][y]);
+  }
+#pragma unroll
+  for (int y = 0; y < 4; ++y)
+    *reinterpret_cast<float4*>(Tt + (4 * tc + y) * TLD + 4 * tr) =
+        make_float4(acc[0][y], acc[1][y], acc[2][y], acc[3][y]);
+  __syncthreads();
+  // G is no longer needed (and no other CTA reads it after step 2): M^T in its place
+  for (int e = tid; e < P * P; e += 256) {
+    const int i = e / P, j = e % P;
+    Gs[j * LD + i] = Ms[i * LD + j];
+  }
+  __syncthreads();
+  // 4. GQ[i][j] = 2 sum_q T[i][q] M[j][q] = 2 sum_q T^T[q][i] M^T[q][j]
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
+  for (int q = 0; q < P; ++q) {
+    const float4 t = *reinterpret_cast<const float4*>(Tt + q * TLD + 4 * tr);
+    const float4 m = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
+    const float tv[4] = {t.x, t.y, t.z, t.w}, mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mv[y], acc[x][y]);
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    *reinterpret_cast<float4*>(Qs + (4 * tr + x) * LD + 4 * tc) =
+        make_float4(2.f * acc[x][0], 2.f * acc[x][1], 2.f * acc[x][2], 2.f * acc[x][3]);
+  cluster_sync();
+  // 5. pack rows i in [r0, r0 + 32): g_ij = GQ[i][j] - GQ[j][i], j > i
+  const int sz = block_size(s, k);
+  float* o = out + static_cast<int64_t>(k) * P * (P - 1) / 2;
+  const int warp = tid / 32, lane = tid % 32;
+  for (int il = warp; il < 32; il += 8) {
+    const int i = r0 + il;
+    if (i >= sz - 1) continue;
+    float* oi = o + (i * sz - i * (i + 1) / 2 - i - 1);
+    for (int j = i + 1 + lane; j < sz; j += 32) {
+      const uint32_t owner = static_cast<uint32_t>(j / 32);
+      const float* src = Qs + (j % 32) * LD + i;
+      const float gji = owner == rank ? *src : dsmem_ld_f(dsmem_addr(src, owner));
+      const float v = Qs[il * LD + j] - gji;
+      if (accumulate) oi[j] += v;
+      else oi[j] = v;
+    }
+  }
+  cluster_sync();
 }
 
 // ------------------------------------------------------------------ self-test

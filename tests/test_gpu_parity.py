@@ -94,6 +94,12 @@ def test_bf16_b128(px):
     _case(px, 512, 512, 128, 128, 513, "bf16")
 
 
+def test_bf16_b128_ragged_last_blocks(px):
+    # 456 = 3 x 128 + 72 and 328 = 2 x 128 + 72: a short last block on both
+    # sides in the fused transform + reduction and the clustered Cayley backward
+    _case(px, 456, 328, 128, 128, 300, "bf16", gstd=0.03)
+
+
 def test_bf16_b512_ragged_block_and_b256(px):
     # 768 = 512 + ragged 256 on the R side; P side b = 256
     _case(px, 768, 512, 512, 256, 260, "bf16", recompute=True)
