@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--mode", default="cayley", choices=["cayley", "neumann"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overhead", action="store_true",
+                    help="skip the plain-bf16-linear comparison and the per-linear breakdown")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample tokens per linear")
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="oracle tokens per linear per step of the reference arm")
@@ -498,6 +500,11 @@ def main():
         "device_status": px.poetx_status_string(status),
     }
 
+    # ---- per-linear times and the plain-linear comparison
+    if not args.no_overhead:
+        line["per_linear"], line["overhead"] = overhead_and_breakdown(
+            args, wl, b, layers, workspace, stream, dev, px, torch, ms_per_step)
+
     # ---- end to end through the C ABI from pinned host buffers
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
@@ -515,6 +522,87 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def flush_l2(torch, buf):
+    buf.add_(1)  # a write pass over a buffer larger than L2
+
+
+def overhead_and_breakdown(args, wl, b, layers, workspace, stream, dev, px, torch, ms_per_step):
+    """Per-linear POET-X fwd+bwd times, and the same layers as plain bf16
+    linears (cuBLAS through torch.matmul: forward Y = X W^T, dgrad dX = dY W,
+    wgrad dW = dY^T X) and as only the GEMMs POET-X itself runs (forward and
+    dgrad, plus the recomputed forward in recompute mode).  Each repetition is
+    timed alone with CUDA events after an L2 flush."""
+    T = wl.tokens
+    reps = 5
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
+    Ws = {id(st): st["W0p"] for st in layers}
+    dWs = {id(st): torch.empty_like(st["W0p"]) for st in layers}
+
+    def timed(fn):
+        tot = 0.0
+        with torch.cuda.stream(stream):
+            fn()   # warm-up
+            for _ in range(reps):
+                flush_l2(torch, flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+        return tot / reps
+
+    per = []
+    plain_total = gemm_total = 0.0
+    for st in layers:
+        lin = st["lin"]
+
+        def poetx_fb(st=st):
+            px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
+                                st["u"], workspace, stream)
+            px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"],
+                                st["u"], T, st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
+
+        def plain(st=st):
+            W = Ws[id(st)]
+            torch.matmul(st["X"], W.t(), out=st["Y"])
+            torch.matmul(st["dY"], W, out=st["dX"])
+            torch.matmul(st["dY"].t(), st["X"], out=dWs[id(st)])
+
+        def same_gemms(st=st):
+            W = Ws[id(st)]
+            torch.matmul(st["X"], W.t(), out=st["Y"])
+            if wl.recompute:
+                torch.matmul(st["X"], W.t(), out=st["Y"])
+            torch.matmul(st["dY"], W, out=st["dX"])
+
+        t_p = timed(poetx_fb)
+        t_l = timed(plain)
+        t_g = timed(same_gemms)
+        sR, sP = block_square_sum(lin.m, b), block_square_sum(lin.n, b)
+        fl = 4.0 * T * lin.m * lin.n + 6.0 * T * (sR + sP)
+        if wl.recompute:
+            fl += 2.0 * T * lin.m * lin.n + 2.0 * T * sP
+        per.append({"linear": f"{lin.name}:{lin.n}->{lin.m}", "ms": t_p,
+                    "tflops": fl / (t_p / 1e3) / 1e12, "plain_linear_ms": t_l,
+                    "same_gemms_ms": t_g})
+        plain_total += t_l
+        gemm_total += t_g
+    torch.cuda.synchronize(dev)
+    sum_linears = sum(p["ms"] for p in per)
+    return per, {
+        "reading": ("primary: POET-X fwd+bwd vs a plain bf16 linear layer of the same shapes "
+                    "(forward, dgrad and wgrad GEMMs via cuBLAS); secondary: vs only the GEMMs "
+                    "POET-X runs (forward, dgrad, recomputed forward)"),
+        "poetx_linears_ms": sum_linears, "poetx_step_ms": ms_per_step,
+        "plain_linear_ms": plain_total, "same_gemms_ms": gemm_total,
+        "vs_plain_linear": sum_linears / plain_total - 1.0,
+        "vs_same_gemms": sum_linears / gemm_total - 1.0,
+        "note": ("per-linear sums exclude the block builds and merges, which the step also runs; "
+                 "each linear timed alone after an L2 flush"),
+    }
 
 
 def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist, build_all,

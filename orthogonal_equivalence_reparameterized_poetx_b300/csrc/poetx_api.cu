@@ -27,6 +27,7 @@
 #include "tc_gemm.cuh"
 #include "tc_bdgr.cuh"
 #include "tc_merge.cuh"
+#include "tc_f32gemm.cuh"
 
 using namespace poetx;
 
@@ -631,6 +632,103 @@ poetx_status tc_merge_pass(cudaStream_t st, const __nv_bfloat16* Ahi, const __nv
   return POETX_OK;
 }
 
+// An fp32 operand of tc_f32_gemm: element (r, k) of batch z at
+// p[z * bs + r * rs + k * cs]; rs == 1 or cs == 1.
+struct F32Operand {
+  const float* p;
+  int64_t rs, cs, bs;
+};
+
+// 3-D fp32 tensor map (contiguous index, other index, batch), no swizzle.
+poetx_status tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t s1_bytes, uint64_t s2_bytes, uint32_t box0, uint32_t box1) {
+  PFN_encodeTiled enc = get_encode_fn();
+  if (!enc) return POETX_ERR_CUDA;
+  if (!aligned(base, 16) || s1_bytes % 16 != 0 || s2_bytes % 16 != 0) return POETX_ERR_MISALIGNED;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? POETX_OK : POETX_ERR_CUDA;
+}
+
+// Tensor map of an operand with `rows` rows and K columns per batch; sets
+// *kcontig.  UNSUPPORTED when neither stride is 1 or the strides are not
+// multiples of 16 bytes.
+poetx_status f32_operand_map(CUtensorMap* map, const F32Operand& o, int rows, int K, int batch,
+                             bool* kcontig) {
+  const uint64_t s2 = static_cast<uint64_t>(std::max<int64_t>(o.bs, 1)) * 4;
+  if (o.cs == 1 && (o.rs * 4) % 16 == 0 && s2 % 16 == 0) {
+    *kcontig = true;
+    return tmap_f32_3d(map, o.p, K, rows, batch, o.rs * 4, s2, 64, 128);
+  }
+  if (o.rs == 1 && (o.cs * 4) % 16 == 0 && s2 % 16 == 0) {
+    *kcontig = false;
+    return tmap_f32_3d(map, o.p, rows, K, batch, o.cs * 4, s2, 128, 64);
+  }
+  return POETX_ERR_UNSUPPORTED;
+}
+
+template <bool AK, bool BK>
+poetx_status launch_f32gemm(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const F32GemmArgs& a, int tiles, int batch) {
+  auto kern = tc_f32gemm_kernel<AK, BK>;
+  static cudaError_t attr_err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F32GemmCfg::SMEM);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  kern<<<dim3(tiles, batch), 320, F32GemmCfg::SMEM, st>>>(ta, tb, a);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+// Batched C = alpha A B^T + beta C on the tensor cores with fp32-grade
+// products (tc_f32gemm.cuh); A is M x K, B is N x K, C row-major (unit
+// column stride) with row stride c_rs and batch stride c_bs.
+poetx_status tc_f32_gemm(cudaStream_t st, int M, int N, int K, int batch, const F32Operand& A,
+                         const F32Operand& B, float* C, int64_t c_rs, int64_t c_bs, float alpha,
+                         float beta) {
+  if (M <= 0 || N <= 0 || batch <= 0) return POETX_OK;
+  if (K <= 0) return POETX_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  bool ak = false, bk = false;
+  POETX_TRY(f32_operand_map(&ta, A, M, K, batch, &ak));
+  POETX_TRY(f32_operand_map(&tb, B, N, K, batch, &bk));
+  F32GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.c = C;
+  a.c_rs = c_rs;
+  a.c_bs = c_bs;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.timeout_ns = g_timeout_ns;
+  const int tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  if (ak && bk) return launch_f32gemm<true, true>(st, ta, tb, a, tiles, batch);
+  if (ak) return launch_f32gemm<true, false>(st, ta, tb, a, tiles, batch);
+  if (bk) return launch_f32gemm<false, true>(st, ta, tb, a, tiles, batch);
+  return launch_f32gemm<false, false>(st, ta, tb, a, tiles, batch);
+}
+
+// C = alpha A B + beta C with the strides of simt_gemm (A(i,k) = A[i sAm +
+// k sAk], B(k,j) = B[k sBk + j sBn]): on the tensor cores when `tc` (bf16
+// layers, fp32-grade products) and on the CUDA cores otherwise.
+poetx_status dense_f32_gemm(bool tc, cudaStream_t st, int M, int N, int K, int batch, const float* A,
+                            int64_t sAm, int64_t sAk, int64_t bsA, const float* B, int64_t sBk,
+                            int64_t sBn, int64_t bsB, float* C, int64_t sCm, int64_t sCn, int64_t bsC,
+                            float alpha, float beta) {
+  if (tc && M >= 64 && N >= 64 && K >= 64 && sCn == 1) {
+    const F32Operand a{A, sAm, sAk, bsA}, b{B, sBn, sBk, bsB};
+    const poetx_status r = tc_f32_gemm(st, M, N, K, batch, a, b, C, sCm, bsC, alpha, beta);
+    if (r != POETX_ERR_UNSUPPORTED && r != POETX_ERR_MISALIGNED) return r;
+  }
+  return simt_gemm<float, float, float>(st, M, N, K, batch, A, sAm, sAk, bsA, B, sBk, sBn, bsB, C, sCm,
+                                        sCn, bsC, alpha, beta);
+}
+
 // ------------------------------------------------------------------ builder
 
 bool fused_cayley_ok(const poetx_layer_desc& d, int b) {
@@ -690,6 +788,9 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
     POETX_TRY(launch_cayley_blocks(st, d, cayley_side(d, S, gen, params), nullptr));
     return POETX_OK;
   }
+  // bf16 layers run the dense products of the build on the tensor cores
+  // with fp32-grade (split bf16) operands; fp32 layers keep fp32 CUDA cores
+  const bool tcg = d.dtype == POETX_DTYPE_BF16;
   unpack_kernel<<<dim3(nb, (b + 7) / 8), 256, 0, st>>>(gen, S.g, Q, M);
   POETX_LAUNCHED();
   if (d.mode == POETX_MODE_CAYLEY) {
@@ -709,16 +810,16 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
         gj_invert128_kernel<<<nb, 1024, 0, st>>>(M + static_cast<int64_t>(o) * b + o, bb, b, D,
                                                  static_cast<int64_t>(P) * P, P);
         POETX_LAUNCHED();
-        POETX_TRY(simt_gemm<float, float, float>(st, P, b, P, nb, D, P, 1, static_cast<int64_t>(P) * P,
+        POETX_TRY(dense_f32_gemm(tcg, st, P, b, P, nb, D, P, 1, static_cast<int64_t>(P) * P,
                                                  M + static_cast<int64_t>(o) * b, b, 1, bb, Rr, b, 1,
                                                  static_cast<int64_t>(P) * b, 1.f, 0.f));
-        POETX_TRY(simt_gemm<float, float, float>(st, b, b, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
+        POETX_TRY(dense_f32_gemm(tcg, st, b, b, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
                                                  Rr, b, 1, static_cast<int64_t>(P) * b, M, b, 1, bb,
                                                  -1.f, 1.f));
         copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(b) * P), nb), 256, 0, st>>>(
             Rr, static_cast<int64_t>(P) * b, b, M + static_cast<int64_t>(o) * b, bb, b, P, b, 1.f, 0.f);
         POETX_LAUNCHED();
-        POETX_TRY(simt_gemm<float, float, float>(st, b, P, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
+        POETX_TRY(dense_f32_gemm(tcg, st, b, P, P, nb, Cc, P, 1, static_cast<int64_t>(b) * P,
                                                  D, P, 1, static_cast<int64_t>(P) * P, M + o, b, 1, bb,
                                                  -1.f, 0.f));
         copy2d_kernel<<<dim3(grid_for(static_cast<int64_t>(P) * P), nb), 256, 0, st>>>(
@@ -739,13 +840,13 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
     for (int i = 1; i <= d.neumann_k; ++i) {
       copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(Q, bb, b, Sb, bb, b, b, b, 0.f, 1.f);
       POETX_LAUNCHED();
-      POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, Sb, b, 1,
+      POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, Sb, b, 1,
                                                bb, 1.f, 1.f));
       std::swap(Sa, Sb);
     }
     copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(Sa, bb, b, B, bb, b, b, b, 1.f, 0.f);
     POETX_LAUNCHED();
-    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, B, b, 1, bb,
+    POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, Q, b, 1, bb, Sa, b, 1, bb, B, b, 1, bb,
                                              1.f, 1.f));
   }
   if (d.dtype == POETX_DTYPE_BF16) {
@@ -768,11 +869,12 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
   const float* M = reinterpret_cast<const float*>(params + S.off_M);
   const float* Q = reinterpret_cast<const float*>(params + S.off_Q);
   float* GQ = t2;
+  const bool tcg = d.dtype == POETX_DTYPE_BF16;  // tensor-core products for bf16 layers
   if (d.mode == POETX_MODE_CAYLEY) {
     // dL/dQ = 2 M^T G M^T
-    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, M, 1, b, bb, G, b, 1, bb, t1, b, 1, bb,
+    POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, M, 1, b, bb, G, b, 1, bb, t1, b, 1, bb,
                                              1.f, 0.f));
-    POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, t1, b, 1, bb, M, 1, b, bb, GQ, b, 1,
+    POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, t1, b, 1, bb, M, 1, b, bb, GQ, b, 1,
                                              bb, 2.f, 0.f));
   } else {
     // B = sum_p c_p Q^p (c_0 = 1, c_1..c_k = 2, c_{k+1} = 1), so
@@ -786,7 +888,7 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
     copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(G, bb, b, R, bb, b, b, b, 1.f, 0.f);
     POETX_LAUNCHED();
     for (int c = 1; c <= k; ++c)  // R_c = R_{c-1} Qt
-      POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, R + (c - 1) * tstride, b, 1, bb, Q,
+      POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, R + (c - 1) * tstride, b, 1, bb, Q,
                                                1, b, bb, R + c * tstride, b, 1, bb, 1.f, 0.f));
     auto coef = [&](int p) { return (p == 0 || p == k + 1) ? 1.f : 2.f; };
     for (int a = k; a >= 0; --a) {
@@ -799,7 +901,7 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
         POETX_LAUNCHED();
       }
       if (a != k) {  // nxt = T_a + Qt cur
-        POETX_TRY(simt_gemm<float, float, float>(st, b, b, b, nb, Q, 1, b, bb, cur, b, 1, bb, nxt, b,
+        POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, Q, 1, b, bb, cur, b, 1, bb, nxt, b,
                                                  1, bb, 1.f, 1.f));
         std::swap(cur, nxt);
       }
@@ -1175,12 +1277,14 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
 }
 
 bool fused_cayley_bwd_ok(const poetx_layer_desc& d, int b) {
-  return d.dtype == POETX_DTYPE_BF16 && d.mode == POETX_MODE_CAYLEY && (b == 32 || b == 64 || b == 128);
+  return d.dtype == POETX_DTYPE_BF16 && d.mode == POETX_MODE_CAYLEY &&
+         (b == 32 || b == 64 || b == 128 || b == 256 || b == 512);
 }
 
 // Fused reduction + Cayley backward + packing for one side (see cayley_bwd_kernel).
 poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_t* params,
-                              const float* partial, int splits, float* dGen, int accumulate) {
+                              const float* partial, int splits, float* t1, float* t2, float* dGen,
+                              int accumulate) {
   ProfScope prof(POETX_KIND_GENBWD, st);
   const int b = S.g.b;
   const size_t smem = 3 * static_cast<size_t>(b) * (b + 4) * 4;
@@ -1191,6 +1295,24 @@ poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_
   });
   const float* M = reinterpret_cast<const float*>(params + S.off_M);
   const int64_t stride = static_cast<int64_t>(S.nsb) * S.sb * S.sb;
+  if (b >= 256) {
+    // G = sum of the split partials (super-block k is block k), then on the
+    // tensor cores with fp32-grade products T = M^T G and GQ = 2 T M^T,
+    // then the pack
+    const int nb = S.g.nblk;
+    const int64_t bb = static_cast<int64_t>(b) * b;
+    gradred_reduce_kernel<<<grid_for(nb * bb), 256, 0, st>>>(partial, stride, splits, S.g, S.sb, t2);
+    POETX_LAUNCHED();
+    const F32Operand mt{M, 1, b, bb};   // A(i, q) = M[q][i]
+    const F32Operand g{t2, 1, b, bb};   // B(j, q) = G[q][j]
+    POETX_TRY(tc_f32_gemm(st, b, b, b, nb, mt, g, t1, b, bb, 1.f, 0.f));
+    const F32Operand t{t1, b, 1, bb};   // A(i, q) = T[i][q]
+    const F32Operand m{M, b, 1, bb};    // B(j, q) = M[j][q]
+    POETX_TRY(tc_f32_gemm(st, b, b, b, nb, t, m, t2, b, bb, 2.f, 0.f));
+    pack_grad_kernel<<<dim3(nb, (b + 7) / 8), 256, 0, st>>>(t2, S.g, dGen, accumulate);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
   if (b == 128) {  // four CTAs (one cluster) per block
     static cudaError_t attr_err = cudaFuncSetAttribute(
         cayley_bwd_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCbwdSmem);
@@ -1215,15 +1337,15 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
   float* nsc = c.w<float>(c.W.off_nsc);
   if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_R))
-      POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.slotsR, dGenR,
-                                 accumulate));
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.slotsR, t1, t2,
+                                 dGenR, accumulate));
     else
       POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
   }
   if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_P))
-      POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.slotsP, dGenP,
-                                 accumulate));
+      POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.slotsP, t1, t2,
+                                 dGenP, accumulate));
     else
       POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
   }

@@ -100,6 +100,17 @@ def test_bf16_b128_ragged_last_blocks(px):
     _case(px, 456, 328, 128, 128, 300, "bf16", gstd=0.03)
 
 
+def test_bf16_neumann_b256_tensor_core_builder(px):
+    # Neumann blocks of 256 (built and differentiated with tensor-core products)
+    _case(px, 512, 640, 256, 256, 200, "bf16", mode="neumann", gstd=0.02)
+
+
+def test_bf16_b256_ragged_last_blocks(px):
+    # 640 = 2 x 256 + 128 and 328 = 256 + 72: short last blocks on both sides
+    # in the clustered 256-wide Cayley backward
+    _case(px, 640, 328, 256, 256, 300, "bf16", gstd=0.02)
+
+
 def test_bf16_b512_ragged_block_and_b256(px):
     # 768 = 512 + ragged 256 on the R side; P side b = 256
     _case(px, 768, 512, 512, 256, 260, "bf16", recompute=True)
