@@ -28,6 +28,7 @@
 #include "tc_bdgr.cuh"
 #include "tc_merge.cuh"
 #include "tc_f32gemm.cuh"
+#include "tc_gemm2.cuh"
 
 using namespace poetx;
 
@@ -474,11 +475,41 @@ poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap
   return POETX_OK;
 }
 
+// Dense GEMM on CTA pairs (tc_gemm2.cuh) with 256 x 256 tiles.
+template <bool B_MN>
+poetx_status launch_pair(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const CUtensorMap& tc, int64_t T, int N, int K) {
+  TcPairArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.num_tiles = static_cast<int>((T + 255) / 256) * ((N + 255) / 256);
+  a.timeout_ns = g_timeout_ns;
+  auto kern = tc_gemm_pair_kernel<B_MN>;
+  static cudaError_t attr_err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcPairCfg::SMEM_BYTES);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  const int pairs = std::max(1, std::min(a.num_tiles, launch_sms() / 2));
+  kern<<<2 * pairs, 320, TcPairCfg::SMEM_BYTES, st>>>(ta, tb, tc, a);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+// Wide outputs (N >= 1024) run on CTA pairs, narrower ones on single CTAs.
+bool use_pair(int64_t T, int N) { return N >= 1024 && T >= 256 && launch_sms() >= 2; }
+
 // h (T x N) = A (T x K) * W^T, W row-major N x K (both K-major).
 poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
                          int K) {
   if (T <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_GEMM_FWD, st);
+  if (use_pair(T, N)) {
+    CUtensorMap ta, tb, tc;
+    POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
+    POETX_TRY(tmap_bf16(&tb, W, N, K, K, 128));
+    POETX_TRY(tmap_bf16(&tc, C, T, N, N, 128));
+    return launch_pair<false>(st, ta, tb, tc, T, N, K);
+  }
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
   CUtensorMap ta, tb, tc;
@@ -501,6 +532,13 @@ poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C,
                          int K) {
   if (T <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_GEMM_DGRAD, st);
+  if (use_pair(T, N)) {
+    CUtensorMap ta, tb, tc;
+    POETX_TRY(tmap_bf16(&ta, A, T, K, K, 128));
+    POETX_TRY(tmap_bf16(&tb, W, K, N, N, 64));
+    POETX_TRY(tmap_bf16(&tc, C, T, N, N, 128));
+    return launch_pair<true>(st, ta, tb, tc, T, N, K);
+  }
   const bool wide = N >= 1024;
   const int BN = wide ? 256 : 128;
   CUtensorMap ta, tb, tc;

@@ -90,6 +90,13 @@ def test_bf16_b64(px):
     _case(px, 256, 640, 64, 64, 300, "bf16")
 
 
+def test_bf16_cta_pair_gemms_with_ragged_tiles(px):
+    # m = 1376 and n = 1032 are wide enough for the CTA-pair GEMMs (256 x 256
+    # tiles split over two CTAs) in the forward and the dgrad; neither they nor
+    # T = 777 are multiples of 256, and b = 64 leaves a ragged last block
+    _case(px, 1376, 1032, 64, 64, 777, "bf16")
+
+
 def test_bf16_b128(px):
     _case(px, 512, 512, 128, 128, 513, "bf16")
 
