@@ -115,6 +115,33 @@ def kind_flops_per_step(wl, b: int, kind: str) -> float:
     return f
 
 
+def kind_bytes_per_step(wl, b: int, kind: str) -> float:
+    """Algorithmic DRAM bytes of one step for the memory-bound kernel classes
+    (each T x d activation operand read or written once per pass).
+
+    gather: X -> u and z -> Y in the forward, dY -> dz and du -> dX in the
+    backward, plus X -> u again when u is recomputed.  blockdiag: forward
+    u -> v and h -> z; backward dz -> dh and dv -> du, which for b <= 128 also
+    read h and u (the fused transform + reduction); plus u -> v when
+    recomputing.  gradred (b >= 256 only): dz^T h and dv^T u read two operands.
+    """
+    T = wl.tokens
+    e = 2 if wl.dtype == "bf16" else 4
+    r = 1 if wl.recompute else 0
+    fused = b <= 128
+    by = 0
+    for lin in wl.linears:
+        n, m = lin.n, lin.m
+        if kind == "gather":
+            by += 2 * T * ((2 + r) * n + 2 * m) * e
+        elif kind == "blockdiag":
+            bwd = (3 * m + 3 * n) if fused else (2 * m + 2 * n)
+            by += T * (2 * n + 2 * m + bwd + 2 * n * r) * e
+        elif kind == "gradred" and not fused:
+            by += T * (2 * m + 2 * n) * e
+    return float(by)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -294,7 +321,12 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream(dev)
+    # the forward/backward stream runs at high priority and the per-layer
+    # build/merge side streams at the default (lowest) priority, so the block
+    # scheduler serves the critical path first when both have work queued
+    lo, hi = torch.cuda.Stream.priority_range()
+    stream = torch.cuda.Stream(dev, priority=hi)
+    torch.cuda.set_stream(stream)
     pipe_info = {"active": px.poetx_pipeline_active(), "setting": args.pipeline or "library default"}
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     T = wl.tokens
@@ -337,7 +369,7 @@ def main():
     # backward is done and its next build follows on the same side stream,
     # while the main stream runs the other layers' forward and backward.
     # Each merge has its own scratch so concurrent merges do not share it.
-    side = [torch.cuda.Stream(dev) for _ in layers]
+    side = [torch.cuda.Stream(dev, priority=lo) for _ in layers]
     merge_ws = ([torch.empty(px.poetx_merge_workspace_size(st["desc"]), dtype=torch.uint8,
                              device=dev) for st in layers] if wl.merge_each_step else None)
     bwd_done = [None] * len(layers)    # event after layer l's backward in the previous step
@@ -458,7 +490,7 @@ def main():
     serial = {k: v for k, v in kinds.items() if k not in ("build", "merge")}
     top = max(serial, key=lambda k: serial[k]["ms"])
     roof = None
-    if top in ("gemm_fwd", "gemm_dgrad", "blockdiag", "gradred"):
+    if top in ("gemm_fwd", "gemm_dgrad"):
         per_step = kind_flops_per_step(wl, b, top)
         launches_top = kinds[top]["groups"]
         achieved = per_step * args.steps / (kinds[top]["ms"] / 1e3) / 1e12
@@ -470,13 +502,8 @@ def main():
                 "avg_launch_ms": kinds[top]["ms"] / launches_top,
                 "flops_per_launch": per_step * args.steps / launches_top,
                 "traffic": measured_traffic(top, wl.key, b)}
-    elif top == "gather":
-        # algorithmic bytes: read + write of every gathered activation
-        # per layer: X -> u in the forward and again in the backward, z -> Y,
-        # dY -> dz and du -> dX; each reads and writes T x d elements
-        by = 0
-        for lin in wl.linears:
-            by += 2 * T * (3 * lin.n + 2 * lin.m) * (2 if wl.dtype == "bf16" else 4)
+    elif top in ("gather", "blockdiag", "gradred"):
+        by = kind_bytes_per_step(wl, b, top)
         achieved = by * args.steps / (kinds[top]["ms"] / 1e3) / 1e9
         launches_top = kinds[top]["groups"]
         roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"],

@@ -381,6 +381,25 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
   }
   const size_t row_bytes = static_cast<size_t>(d) * sizeof(T);
   if constexpr (sizeof(T) == 2) {
+    // rows of at least 4 KB: persistent CTAs with two blocks of rows (about
+    // 48 KB each) in flight per CTA.  Narrower rows keep the pair-interleaved
+    // kernel below, whose short per-CTA iterations suit the smaller passes
+    // (measured on B300: the pipelined kernel is 18% faster at d = 2048 and
+    // 5% slower at d = 1024).
+    const int rb = static_cast<int>(std::max<size_t>(1, std::min<size_t>(32, (48 * 1024) / row_bytes)));
+    const size_t psmem = 2 * rb * row_bytes + 64;
+    if (row_bytes >= 4096 && psmem <= 200 * 1024) {
+      static cudaError_t attr_err = cudaFuncSetAttribute(
+          gather_rows_pipelined_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+      const int64_t nblocks = (rows + rb - 1) / rb;
+      const int grid = static_cast<int>(std::min<int64_t>(nblocks, launch_sms() * 2));
+      gather_rows_pipelined_kernel<<<grid, 256, psmem, st>>>(
+          reinterpret_cast<const uint16_t*>(in), reinterpret_cast<uint4*>(out), idx, rows, d, rb,
+          g_timeout_ns);
+      POETX_LAUNCHED();
+      return POETX_OK;
+    }
     // interleaved row pairs, about 32 KB staged per iteration (at least one pair)
     const int ppi = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (16 * 1024) / row_bytes)));
     const size_t smem = 2 * row_bytes * ppi;

@@ -246,6 +246,114 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const T* __restrict__ 
   }
 }
 
+// bf16 gather on persistent CTAs with rows staged by bulk copies:
+// out[r][j] = in[r][idx[j]].  CTA c takes blocks of `rb` rows c, c + G, ...
+// (G = gridDim.x) and keeps two blocks in flight: while its 256 threads
+// gather block k from one shared buffer (random 2-byte reads, 16-byte
+// coalesced stores), block k + 1 is landing in the other.  Thread t always
+// produces the 16-byte output chunks t, t + 256, ... of a row, so it keeps
+// their indices in registers when a row has at most 4 * 256 chunks.
+// Waits are bounded; on a timeout the CTA records it and returns.
+__global__ void __launch_bounds__(256) gather_rows_pipelined_kernel(const uint16_t* __restrict__ in,
+                                                                    uint4* __restrict__ out,
+                                                                    const int32_t* __restrict__ idx,
+                                                                    int64_t rows, int d, int rb,
+                                                                    uint64_t timeout_ns) {
+  extern __shared__ __align__(16) uint8_t gsm[];
+  const size_t buf_bytes = static_cast<size_t>(rb) * d * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(gsm + 2 * buf_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+  const int vpr = d / 8;  // 16-byte output chunks per row
+  const int64_t nblocks = (rows + rb - 1) / rb;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int64_t k, int s) {
+    const int64_t b = blockIdx.x + k * gridDim.x;
+    if (b >= nblocks) return;
+    const int nr = static_cast<int>(min(static_cast<int64_t>(rb), rows - b * rb));
+    const uint32_t rowb = static_cast<uint32_t>(d) * 2;
+    mbar_arrive_expect_tx(&full[s], rowb * nr);
+    uint8_t* dst = gsm + s * buf_bytes;
+    for (int r = 0; r < nr; ++r)
+      bulk_load(dst + static_cast<size_t>(r) * rowb, in + (b * rb + r) * static_cast<int64_t>(d), rowb,
+                &full[s]);
+  };
+  if (tid == 0) {
+    issue(0, 0);
+    issue(1, 1);
+  }
+  // this thread's chunk indices
+  constexpr int KREG = 4;
+  const bool in_regs = vpr <= KREG * 256;
+  int4 ia[KREG], ib[KREG];
+#pragma unroll
+  for (int q = 0; q < KREG; ++q) {
+    const int c = tid + 256 * q;
+    if (in_regs && c < vpr) {
+      ia[q] = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c);
+      ib[q] = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c + 1);
+    } else {
+      ia[q] = ib[q] = make_int4(0, 0, 0, 0);
+    }
+  }
+  int64_t kfail = -1;
+  for (int64_t k = 0;; ++k) {
+    const int64_t b = blockIdx.x + k * gridDim.x;
+    if (b >= nblocks) break;
+    const int s = static_cast<int>(k & 1);
+    const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((k >> 1) & 1), timeout_ns, abort_flag);
+    if (__syncthreads_or(!ok)) {  // every thread leaves at the same block
+      kfail = k;
+      break;
+    }
+    const int nr = static_cast<int>(min(static_cast<int64_t>(rb), rows - b * rb));
+    const uint16_t* buf = reinterpret_cast<const uint16_t*>(gsm + s * buf_bytes);
+    for (int r = 0; r < nr; ++r) {
+      const uint16_t* row = buf + static_cast<size_t>(r) * d;
+      uint4* orow = out + (b * rb + r) * static_cast<int64_t>(vpr);
+      if (in_regs) {
+#pragma unroll
+        for (int q = 0; q < KREG; ++q) {
+          const int c = tid + 256 * q;
+          if (c < vpr) {
+            const int4 i0 = ia[q], i1 = ib[q];
+            orow[c] = make_uint4(row[i0.x] | (static_cast<uint32_t>(row[i0.y]) << 16),
+                                 row[i0.z] | (static_cast<uint32_t>(row[i0.w]) << 16),
+                                 row[i1.x] | (static_cast<uint32_t>(row[i1.y]) << 16),
+                                 row[i1.z] | (static_cast<uint32_t>(row[i1.w]) << 16));
+          }
+        }
+      } else {
+        for (int c = tid; c < vpr; c += 256) {
+          const int4 i0 = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c);
+          const int4 i1 = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c + 1);
+          orow[c] = make_uint4(row[i0.x] | (static_cast<uint32_t>(row[i0.y]) << 16),
+                               row[i0.z] | (static_cast<uint32_t>(row[i0.w]) << 16),
+                               row[i1.x] | (static_cast<uint32_t>(row[i1.y]) << 16),
+                               row[i1.z] | (static_cast<uint32_t>(row[i1.w]) << 16));
+        }
+      }
+    }
+    __syncthreads();  // every thread is done with buffer s
+    if (tid == 0) issue(k + 2, s);
+  }
+  // after a timeout, blocks kfail and kfail + 1 may still be landing: wait
+  // for them (bounded) before the CTA's shared memory is released
+  if (tid == 0 && kfail >= 0) {
+    volatile int never = 0;
+    for (int64_t k = kfail; k < kfail + 2; ++k)
+      if (blockIdx.x + k * gridDim.x < nblocks)
+        mbar_wait(&full[k & 1], static_cast<uint32_t>((k >> 1) & 1), timeout_ns, &never);
+  }
+  __syncthreads();
+}
+
 // bf16 version with rows staged in interleaved pairs: shared word c of pair p
 // holds (row 2p)[c] in its low half and (row 2p+1)[c] in its high half, so one
 // random 4-byte shared-memory read serves both rows (half the bank-conflicted
