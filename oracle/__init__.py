@@ -43,6 +43,12 @@ Readings where the pages are silent (each is listed in the design notes):
   highest terms, as [X-nl] §4 names them.
 * Merge folds R and P into the base weight and moves it to fresh
   permutations; the caller then resets the generators to zero.
+* POET-XQ ([X-nl] Methodologie §5: base weights stored quantized, e.g. INT8,
+  and dequantized on the fly; the scheme is not given): symmetric int8 per
+  output row, scale = max|row| / 127, code = round-half-to-even(w / scale)
+  clamped to [-127, 127], computed in float32 (the arithmetic that decides
+  an integer code is the kernel's); an all-zero row has scale 0 and codes 0.
+  The dequantized weight is scale * code.
 
 Every function here is the plain definition: dense matrices, library
 matmuls as single steps, no blocking or fusion beyond what the definition
@@ -61,6 +67,7 @@ __all__ = [
     "inverse_gauss_jordan", "cayley", "neumann", "LayerSpec", "blocks_of",
     "orthogonal_factor", "dense_weight", "premerged_weight", "forward_dense",
     "forward_input_centric", "backward", "merge", "loss_for_fd",
+    "quantize_rows_int8", "dequantize_rows_int8",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -400,3 +407,24 @@ def merge(spec: LayerSpec, W0, genR, genP, new_seed_R: int, new_seed_P: int,
     Wn = dense_weight(spec, W0, genR, genP, piR, piP)
     return premerged_weight(Wn, permutation(new_seed_R, spec.m),
                             permutation(new_seed_P, spec.n))
+
+
+def quantize_rows_int8(W) -> Tuple[np.ndarray, np.ndarray]:
+    """POET-XQ storage of a weight ([X-nl] Methodologie §5): per row i,
+    scale_i = max_j |W[i, j]| / 127 and code_ij = round-half-to-even(
+    W[i, j] / scale_i), clamped to [-127, 127].  All of it in float32, the
+    precision in which the integer decision is taken; a zero row gets scale 0
+    and codes 0.  Returns (codes int8 m x n, scales float32 m)."""
+    W32 = np.asarray(W, dtype=np.float32)
+    amax = np.max(np.abs(W32), axis=1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    q = np.rint(W32 / safe[:, None])          # float32 division; rint rounds half to even
+    q = np.clip(q, -127, 127)
+    q[scale == 0, :] = 0
+    return q.astype(np.int8), scale
+
+
+def dequantize_rows_int8(codes, scales) -> np.ndarray:
+    """The weight a POET-XQ layer computes with: scale_i * code_ij (exact)."""
+    return np.asarray(scales, dtype=np.float64)[:, None] * np.asarray(codes, dtype=np.float64)

@@ -284,6 +284,41 @@ def test_merge_preserves_the_layer_map(spec):
 
 # ---------------------------------------------------------------- planted mistakes
 
+# ------------------------------------------------------------------ POET-XQ int8 rows
+
+def test_int8_quantization_golden_rows():
+    rows = read_golden("quant_int8_rows.txt")
+    ws = [np.array([float(x) for x in r[1:]]) for r in rows if r[0] == "w:"]
+    qs = [np.array([int(x) for x in r[1:]]) for r in rows if r[0] == "q:"]
+    W = np.stack(ws)
+    codes, scales = O.quantize_rows_int8(W)
+    assert codes.dtype == np.int8
+    assert np.array_equal(codes.astype(np.int64), np.stack(qs))
+    amax = np.abs(W.astype(np.float32)).max(axis=1)
+    assert np.array_equal(scales, (amax / np.float32(127)).astype(np.float32))
+
+
+def test_int8_quantization_properties():
+    rng = np.random.default_rng(11)
+    W = (rng.standard_normal((37, 53)) * 0.02).astype(np.float32)
+    W[5] = 0.0                      # an all-zero row
+    W[7, 3] = 0.5                   # a row dominated by one entry
+    codes, scales = O.quantize_rows_int8(W)
+    deq = O.dequantize_rows_int8(codes, scales)
+    # within half a quantization step of the input (plus float32 round-off)
+    err = np.abs(deq - W.astype(np.float64))
+    assert np.all(err <= scales[:, None].astype(np.float64) * (0.5 + 1e-5) + 1e-12)
+    # every nonzero row reaches the full code range at its largest entry
+    nz = scales > 0
+    assert np.all(np.abs(codes[nz]).max(axis=1) == 127)
+    assert np.all(codes[~nz] == 0) and np.all(scales[~nz] == 0)
+    assert np.all(np.abs(codes.astype(np.int64)) <= 127)
+    # per-row: permuting rows permutes the result; permuting columns permutes codes
+    pr, pc = rng.permutation(37), rng.permutation(53)
+    c2, s2 = O.quantize_rows_int8(W[pr][:, pc])
+    assert np.array_equal(c2, codes[pr][:, pc]) and np.array_equal(s2, scales[pr])
+
+
 def _pins_fail(monkeypatch, name, replacement, checks):
     monkeypatch.setattr(O, name, replacement)
     failed = 0
@@ -300,6 +335,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     orig_cayley, orig_neumann = O.cayley, O.neumann
     orig_unpack, orig_apply = O.unpack_skew, O._apply_blocks
     orig_ggrad = O._generator_grad
+    orig_quant = O.quantize_rows_int8
     orig_perm = O.permutation
 
     def cayley_transposed(Q):
@@ -348,3 +384,20 @@ def test_planted_mistakes_are_caught(monkeypatch):
     assert _pins_fail(monkeypatch, "_apply_blocks", apply_blocks_untransposed, [dense, fd]) >= 1
     assert _pins_fail(monkeypatch, "_generator_grad", ggrad_dropped_two, [fd, fdn]) >= 1
     assert _pins_fail(monkeypatch, "permutation", perm_reversed_loop, [permk]) >= 1
+
+    def quant_per_column(W):
+        c, s_ = orig_quant(np.asarray(W).T)
+        return c.T, s_
+    def quant_over_128(W):
+        W32 = np.asarray(W, dtype=np.float32)
+        sc = (np.abs(W32).max(axis=1) / np.float32(128)).astype(np.float32)
+        safe = np.where(sc > 0, sc, np.float32(1))
+        return np.clip(np.rint(W32 / safe[:, None]), -127, 127).astype(np.int8), sc
+    def quant_truncating(W):
+        W32 = np.asarray(W, dtype=np.float32)
+        sc = (np.abs(W32).max(axis=1) / np.float32(127)).astype(np.float32)
+        safe = np.where(sc > 0, sc, np.float32(1))
+        return np.clip(np.trunc(W32 / safe[:, None]), -127, 127).astype(np.int8), sc
+    qgold = lambda: test_int8_quantization_golden_rows()
+    for bad in (quant_per_column, quant_over_128, quant_truncating):
+        assert _pins_fail(monkeypatch, "quantize_rows_int8", bad, [qgold]) >= 1
