@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--b", type=int, default=None, help="block size (default: first of the workload)")
     ap.add_argument("--mode", default="cayley", choices=["cayley", "neumann"])
+    ap.add_argument("--weight", default="dense", choices=["dense", "int8"],
+                    help="storage of the base weight: layer dtype, or int8 rows (POET-XQ)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overhead", action="store_true",
@@ -286,7 +288,8 @@ def workload_config(wl, b, args, pipeline=None):
         "pipeline": pipeline,
         "workload": wl.key, "description": wl.description,
         "linears": [f"{l.name}:{l.n}->{l.m}" for l in wl.linears],
-        "tokens": wl.tokens, "b": b, "mode": args.mode, "recompute": wl.recompute,
+        "tokens": wl.tokens, "b": b, "mode": args.mode, "weight": args.weight,
+        "recompute": wl.recompute,
         "merge_each_step": wl.merge_each_step,
         "l2": "inputs larger than L2 (activations of all linears, several GB per step)",
         "parallelism": f"dp{args.gpus}",
@@ -336,12 +339,15 @@ def main():
     ws_bytes = 0
     for li, lin in enumerate(wl.linears):
         desc = px.make_desc(lin.m, lin.n, b, b, synth.SEED_PERM_R + li, synth.SEED_PERM_P + li,
-                            dtype=wl.dtype, mode=args.mode)
+                            dtype=wl.dtype, mode=args.mode, weight=args.weight)
         lr, lp = px.poetx_gen_length(lin.m, b), px.poetx_gen_length(lin.n, b)
         inp = synth.layer_inputs(lin, li, T, wl.dtype, lr, lp)
         st = dict(lin=lin, desc=desc, lr=lr, lp=lp)
         st["params"] = torch.empty(px.poetx_params_size(desc), dtype=torch.uint8, device=dev)
-        st["W0p"] = torch.empty(lin.m, lin.n, dtype=dt, device=dev)
+        if args.weight == "int8":   # int8 codes and row scales, poetx_weight_size bytes
+            st["W0p"] = torch.empty(px.poetx_weight_size(desc), dtype=torch.uint8, device=dev)
+        else:
+            st["W0p"] = torch.empty(lin.m, lin.n, dtype=dt, device=dev)
         st["genR"], st["genP"] = inp.genR.to(dev), inp.genP.to(dev)
         st["X"], st["dY"] = inp.X.to(dev), inp.dY.to(dev)
         st["Y"] = torch.empty(T, lin.m, dtype=dt, device=dev)
@@ -564,7 +570,11 @@ def overhead_and_breakdown(args, wl, b, layers, workspace, stream, dev, px, torc
     T = wl.tokens
     reps = 5
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
-    Ws = {id(st): st["W0p"] for st in layers}
+    # the plain linear keeps a dense weight of the layer dtype (an int8 layer's
+    # weight buffer holds codes and scales)
+    Ws = {id(st): (st["W0p"] if st["W0p"].dtype != torch.uint8 else
+                   torch.zeros(st["lin"].m, st["lin"].n, dtype=st["X"].dtype, device=dev))
+          for st in layers}
     dWs = {id(st): torch.empty_like(st["W0p"]) for st in layers}
 
     def timed(fn):

@@ -74,11 +74,23 @@ typedef enum poetx_status {
 enum { POETX_MODE_CAYLEY = 0, POETX_MODE_NEUMANN = 1 };
 enum { POETX_DTYPE_FP32 = 0, POETX_DTYPE_BF16 = 1 };
 
+/* Storage of the pre-merged base weight W0p.
+ *   POETX_WEIGHT_DENSE: m x n values of the layer dtype.
+ *   POETX_WEIGHT_INT8:  POET-XQ (Methodologie §5: the base weights are stored
+ *     quantized, e.g. INT8, and dequantized on the fly).  The scheme is a
+ *     reading, as the pages give none: symmetric per row, scale_i =
+ *     max_j |W0p[i][j]| / 127 and code_ij = round-half-to-even(W0p[i][j] /
+ *     scale_i) clamped to [-127, 127], computed in float32; a zero row has
+ *     scale 0.  The layer computes with scale_i * code_ij.  Buffer layout:
+ *     m x n int8 codes (row-major), then, at the next multiple of 256 bytes,
+ *     m float32 scales; poetx_weight_size gives the total.  bf16 layers only. */
+enum { POETX_WEIGHT_DENSE = 0, POETX_WEIGHT_INT8 = 1 };
+
 /* Geometry and options of one layer.  m, n >= 1; 1 <= b_R <= m and
  * 1 <= b_P <= n.  BF16 additionally needs m and n multiples of 8 (16-byte
  * rows for the tensor-memory-accelerator copies) and b_R, b_P in
  * {32, 64, 128, 256, 512}.  neumann_k >= 1 is read in Neumann mode only.
- * reserved must be 0. */
+ * weight_format is POETX_WEIGHT_DENSE or (bf16 only) POETX_WEIGHT_INT8. */
 typedef struct poetx_layer_desc {
   int32_t m, n;
   int32_t b_R, b_P;
@@ -86,7 +98,7 @@ typedef struct poetx_layer_desc {
   int32_t mode;
   int32_t neumann_k;
   int32_t dtype;
-  int32_t reserved;
+  int32_t weight_format;
 } poetx_layer_desc;
 
 /* Human-readable name of a status code (static storage). */
@@ -120,11 +132,17 @@ size_t poetx_params_size(const poetx_layer_desc* desc);
 poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR,
                                 const float* genP, void* params, void* stream);
 
+/* Bytes of the pre-merged weight buffer W0p in the desc's weight format
+ * (0 for an invalid desc). */
+size_t poetx_weight_size(const poetx_layer_desc* desc);
+
 /* Pre-merges the two permutations adjacent to W0 into it:
- * W0p[i][j] = W0[pi_R(i)][pi_P(j)] (row-major m x n, dtype of desc).
- * W0 and W0p must not overlap.  params must come from poetx_params_build
- * with the same desc.  Source: Methodologie §2 (two of the four forward
- * permutations merged into the weight ahead of time). */
+ * W0p[i][j] = W0[pi_R(i)][pi_P(j)].  W0 is row-major m x n of the layer
+ * dtype; W0p is in the desc's weight format (for POETX_WEIGHT_INT8 the
+ * permuted rows are quantized as described there; the codes depend only on
+ * W0 and the permutations).  W0 and W0p must not overlap.  params must come
+ * from poetx_params_build with the same desc.  Source: Methodologie §2 (two
+ * of the four forward permutations merged into the weight ahead of time). */
 poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* params,
                                    const void* W0, void* W0p, void* stream);
 
@@ -135,6 +153,8 @@ size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T);
  * never forming R W0 P (Methodologie §1, §2, §3):
  *   u = X[:, pi_P];  v_k = u_k B_P,k^T;  h = v W0'^T;  z_k = h_k B_R,k^T;
  *   Y[:, pi_R] = z.
+ * W0p is in the desc's weight format; an int8 weight is dequantized into the
+ * workspace (scale_i * code_ij rounded to bf16) at the start of each call.
  * X: T x n, Y: T x m (dtype).  saved_h: T x m (dtype) receives h, or NULL
  * for activation recompute in the backward (Methodologie §5, POET-Xmem).
  * saved_u: T x n (dtype) receives the permuted input u, or NULL; the
@@ -174,7 +194,9 @@ size_t poetx_merge_workspace_size(const poetx_layer_desc* desc);
  * base weight and re-expresses it under the permutations of
  * (new_seed_R, new_seed_P): with K = blockdiag(B_R) W0p blockdiag(B_P),
  * W0p_new[i][j] = K[pi_R^-1(pi'_R(i))][pi_P^-1(pi'_P(j))], accumulated in fp32
- * and rounded once to dtype.  W0p is updated in place.  The caller then
+ * and rounded once to dtype.  An int8 weight (POET-XQ) is dequantized, merged
+ * and quantized again per row from the fp32-grade K (each code then lies
+ * within one step of the exact result).  W0p is updated in place.  The caller then
  * resets the generators to zero and rebuilds params with the new seeds;
  * the layer then computes the same map as before the merge.
  * Errors: INVALID_ARG, MISALIGNED, CUDA. */
@@ -273,7 +295,8 @@ enum {
   POETX_KIND_GENBWD = 6,      /* partial reduction, Cayley backward, packing       */
   POETX_KIND_MERGE = 7,       /* merge and weight pre-merge                        */
   POETX_KIND_SIMT = 8,        /* fp32 CUDA-core path of the layer                  */
-  POETX_NUM_KINDS = 9
+  POETX_KIND_DEQUANT = 9,     /* int8 weight dequantization (POET-XQ)              */
+  POETX_NUM_KINDS = 10
 };
 
 /* Profiling.  While enabled, each group of launches of one kernel class is

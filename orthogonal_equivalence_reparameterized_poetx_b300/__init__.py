@@ -21,7 +21,8 @@ from . import build as _build
 __all__ = [
     "PoetxError", "poetx_layer_desc", "LIB", "lib_path", "POETX_OK", "POETX_ERR_INVALID_ARG",
     "POETX_ERR_UNSUPPORTED", "POETX_ERR_MISALIGNED", "POETX_ERR_CUDA", "POETX_ERR_TIMEOUT",
-    "MODE_CAYLEY", "MODE_NEUMANN", "DTYPE_FP32", "DTYPE_BF16", "make_desc",
+    "MODE_CAYLEY", "MODE_NEUMANN", "DTYPE_FP32", "DTYPE_BF16", "WEIGHT_DENSE", "WEIGHT_INT8",
+    "make_desc", "poetx_weight_size",
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
@@ -36,6 +37,7 @@ POETX_OK, POETX_ERR_INVALID_ARG, POETX_ERR_UNSUPPORTED = 0, 1, 2
 POETX_ERR_MISALIGNED, POETX_ERR_CUDA, POETX_ERR_TIMEOUT = 3, 4, 5
 MODE_CAYLEY, MODE_NEUMANN = 0, 1
 DTYPE_FP32, DTYPE_BF16 = 0, 1
+WEIGHT_DENSE, WEIGHT_INT8 = 0, 1
 
 EXPORTED_SYMBOLS = [
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
@@ -45,13 +47,14 @@ EXPORTED_SYMBOLS = [
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "poetx_linear_fwd_noalloc", "poetx_set_pipeline", "poetx_pipeline_active",
+    "poetx_weight_size",
 ]
 
 # Size of the library's fixed forward scratch (POETX_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KIND_NAMES = ["gemm_fwd", "gemm_dgrad", "blockdiag", "gradred", "gather", "build", "genbwd",
-              "merge", "simt"]
+              "merge", "simt", "dequant"]
 
 
 class PoetxError(RuntimeError):
@@ -64,19 +67,23 @@ class poetx_layer_desc(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("b_R", ctypes.c_int32),
                 ("b_P", ctypes.c_int32), ("seed_R", ctypes.c_uint64), ("seed_P", ctypes.c_uint64),
                 ("mode", ctypes.c_int32), ("neumann_k", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("weight_format", ctypes.c_int32)]
 
     def __repr__(self):
         return (f"poetx_layer_desc(m={self.m}, n={self.n}, b_R={self.b_R}, b_P={self.b_P}, "
                 f"seed_R={self.seed_R}, seed_P={self.seed_P}, mode={self.mode}, "
-                f"neumann_k={self.neumann_k}, dtype={self.dtype})")
+                f"neumann_k={self.neumann_k}, dtype={self.dtype}, "
+                f"weight_format={self.weight_format})")
 
 
-def make_desc(m, n, b_R, b_P, seed_R, seed_P, dtype="bf16", mode="cayley", neumann_k=3):
+def make_desc(m, n, b_R, b_P, seed_R, seed_P, dtype="bf16", mode="cayley", neumann_k=3,
+              weight="dense"):
+    """weight: "dense" (W0' in the layer dtype) or "int8" (POET-XQ storage)."""
     return poetx_layer_desc(
         m, n, b_R, b_P, seed_R, seed_P,
         MODE_NEUMANN if mode in ("neumann", MODE_NEUMANN) else MODE_CAYLEY, neumann_k,
-        DTYPE_BF16 if dtype in ("bf16", DTYPE_BF16) else DTYPE_FP32, 0)
+        DTYPE_BF16 if dtype in ("bf16", DTYPE_BF16) else DTYPE_FP32,
+        WEIGHT_INT8 if weight in ("int8", WEIGHT_INT8) else WEIGHT_DENSE)
 
 
 def _load():
@@ -95,6 +102,7 @@ def _load():
         "poetx_params_build": (I32, [D, P, P, P, P]),
         "poetx_weight_premerge": (I32, [D, P, P, P, P]),
         "poetx_workspace_size": (SZ, [D, I64]),
+        "poetx_weight_size": (SZ, [D]),
         "poetx_linear_fwd": (I32, [D, P, P, P, I64, P, P, P, P, P]),
         "poetx_linear_bwd": (I32, [D, P, P, P, P, P, P, I64, P, P, P, I32, P, P]),
         "poetx_merge_workspace_size": (SZ, [D]),
@@ -184,6 +192,10 @@ def poetx_weight_premerge(desc, params, W0, W0p, stream=None):
 
 def poetx_workspace_size(desc, T: int) -> int:
     return LIB.poetx_workspace_size(ctypes.byref(desc), T)
+
+
+def poetx_weight_size(desc) -> int:
+    return LIB.poetx_weight_size(ctypes.byref(desc))
 
 
 def poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, saved_u, workspace, stream=None):
@@ -287,7 +299,10 @@ class Layer:
         self.device = torch.device(device)
         self.dtype = torch.bfloat16 if desc.dtype == DTYPE_BF16 else torch.float32
         self.params = torch.empty(poetx_params_size(desc), dtype=torch.uint8, device=self.device)
-        self.W0p = torch.empty(desc.m, desc.n, dtype=self.dtype, device=self.device)
+        if desc.weight_format == WEIGHT_INT8:   # codes, then row scales (poetx_weight_size bytes)
+            self.W0p = torch.empty(poetx_weight_size(desc), dtype=torch.uint8, device=self.device)
+        else:
+            self.W0p = torch.empty(desc.m, desc.n, dtype=self.dtype, device=self.device)
         self.max_tokens = max_tokens
         ws = max(poetx_workspace_size(desc, max_tokens), poetx_merge_workspace_size(desc))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)

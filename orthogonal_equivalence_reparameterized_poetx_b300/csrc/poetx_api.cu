@@ -220,7 +220,7 @@ Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
 
 struct WorkLayout {
   size_t off_n1, off_n2, off_m1, off_m2, off_m3;
-  size_t off_partR, off_partP, off_GR, off_GP, off_t1, off_t2, off_nsc;
+  size_t off_partR, off_partP, off_GR, off_GP, off_t1, off_t2, off_nsc, off_wdq;
   int splitsR, splitsP;
   size_t total;
 };
@@ -262,6 +262,17 @@ int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
   return std::max(smax * kMaxChunks, fused);
 }
 
+// Pre-merged weight buffer: m x n of the dtype, or (POET-XQ) m x n int8
+// codes followed, at the next 256-byte boundary, by m float32 row scales.
+bool weight_int8(const poetx_layer_desc& d) { return d.weight_format == POETX_WEIGHT_INT8; }
+size_t weight_codes_bytes(const poetx_layer_desc& d) {
+  return align_up(static_cast<size_t>(d.m) * d.n);
+}
+size_t weight_bytes(const poetx_layer_desc& d) {
+  if (weight_int8(d)) return weight_codes_bytes(d) + align_up(static_cast<size_t>(d.m) * 4);
+  return static_cast<size_t>(d.m) * d.n * (d.dtype == POETX_DTYPE_BF16 ? 2 : 4);
+}
+
 WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t T, int nsm) {
   WorkLayout W{};
   const size_t e = d.dtype == POETX_DTYPE_BF16 ? 2 : 4;
@@ -293,6 +304,8 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   W.off_t2 = off; off = align_up(off + gmax);
   W.off_nsc = off;
   if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * (d.neumann_k + 3));
+  W.off_wdq = off;  // dequantized int8 weight (bf16 m x n)
+  if (weight_int8(d)) off = align_up(off + static_cast<size_t>(d.m) * d.n * 2);
   W.total = off;
   return W;
 }
@@ -307,7 +320,9 @@ poetx_status check_desc(const poetx_layer_desc* d) {
   if (d->mode == POETX_MODE_NEUMANN && (d->neumann_k < 1 || d->neumann_k > 6))
     return POETX_ERR_INVALID_ARG;
   if (d->dtype != POETX_DTYPE_FP32 && d->dtype != POETX_DTYPE_BF16) return POETX_ERR_INVALID_ARG;
-  if (d->reserved != 0) return POETX_ERR_INVALID_ARG;
+  if (d->weight_format != POETX_WEIGHT_DENSE && d->weight_format != POETX_WEIGHT_INT8)
+    return POETX_ERR_INVALID_ARG;
+  if (d->weight_format == POETX_WEIGHT_INT8 && d->dtype != POETX_DTYPE_BF16) return POETX_ERR_UNSUPPORTED;
   auto b_ok_fp32 = [](int b) { return b <= 128 || (b % 128 == 0 && b <= 1024); };
   auto b_ok_bf16 = [](int b) { return b == 32 || b == 64 || b == 128 || b == 256 || b == 512; };
   if (d->dtype == POETX_DTYPE_FP32) {
@@ -1589,6 +1604,37 @@ poetx_status check_tensor(const void* p) {
   return POETX_OK;
 }
 
+// POET-XQ: an int8 weight buffer (codes, then row scales) to bf16 m x n,
+// with `lo` also the bf16 remainder (out + lo = scale * code to 2^-17).
+poetx_status dequant_weight(cudaStream_t st, const poetx_layer_desc& d, const void* W0p,
+                            __nv_bfloat16* out, __nv_bfloat16* lo = nullptr) {
+  ProfScope prof(POETX_KIND_DEQUANT, st);
+  const auto* codes = reinterpret_cast<const int8_t*>(W0p);
+  const auto* scales =
+      reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(W0p) + weight_codes_bytes(d));
+  dequant_int8_kernel<<<grid_for(static_cast<int64_t>(d.m) * d.n / 8), 256, 0, st>>>(codes, scales, out,
+                                                                                     lo, d.m, d.n);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+// POET-XQ: quantizes row i from S[row_map[i]][col_map[j]], S = hi (+ lo), into
+// the int8 weight buffer (quantize_rows_kernel).
+poetx_status quantize_weight(cudaStream_t st, const poetx_layer_desc& d, const __nv_bfloat16* hi,
+                             const __nv_bfloat16* lo, const int32_t* row_map, const int32_t* col_map,
+                             void* W0p) {
+  const size_t smem = static_cast<size_t>(d.n) * 4;
+  if (smem > 200 * 1024) return POETX_ERR_UNSUPPORTED;
+  static cudaError_t attr_err =
+      cudaFuncSetAttribute(quantize_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  auto* codes = reinterpret_cast<int8_t*>(W0p);
+  auto* scales = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(W0p) + weight_codes_bytes(d));
+  quantize_rows_kernel<<<d.m, 256, smem, st>>>(hi, lo, row_map, col_map, d.n, codes, scales);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 // Merge scratch.  fp32 layers: T1 = W0' B_P and K = B_R T1 (fp32, m x n).
 // bf16 layers (tensor-core passes): W1 = (W0' B_P)^T as a bf16 hi/lo pair
 // (n x m each), K = B_R W0' B_P in bf16 (m x n), and the hi/lo super-block
@@ -1596,6 +1642,7 @@ poetx_status check_tensor(const void* p) {
 struct MergeLayout {
   size_t off_T1, off_K;              // fp32
   size_t off_W1hi, off_W1lo, off_Kb;  // bf16
+  size_t off_Wdq, off_Wdqlo, off_Klo;  // int8 weights: dequantized input (hi, lo), low half of K
   size_t off_DPhi, off_DPlo, off_DRhi, off_DRlo;
   size_t off_rhoR, off_rhoP;
   size_t total;
@@ -1618,6 +1665,11 @@ MergeLayout merge_layout(const poetx_layer_desc& d, const ParamsLayout& L) {
     M.off_DPlo = off; off = align_up(off + dp);
     M.off_DRhi = off; off = align_up(off + dr);
     M.off_DRlo = off; off = align_up(off + dr);
+    if (weight_int8(d)) {
+      M.off_Wdq = off; off = align_up(off + mn * 2);
+      M.off_Wdqlo = off; off = align_up(off + mn * 2);
+      M.off_Klo = off; off = align_up(off + mn * 2);
+    }
   }
   M.off_rhoR = off; off = align_up(off + static_cast<size_t>(d.m) * 4);
   M.off_rhoP = off; off = align_up(off + static_cast<size_t>(d.n) * 4);
@@ -1703,6 +1755,8 @@ poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* par
   const int32_t* piP = reinterpret_cast<const int32_t*>(pb + L.off_piP);
   const int grid = std::min(desc->m, device_sm_count() * 8);
   ProfScope prof(POETX_KIND_MERGE, st);
+  if (weight_int8(*desc))
+    return quantize_weight(st, *desc, reinterpret_cast<const __nv_bfloat16*>(W0), nullptr, piR, piP, W0p);
   if (desc->dtype == POETX_DTYPE_BF16)
     gather2d_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(
         reinterpret_cast<const __nv_bfloat16*>(W0), reinterpret_cast<__nv_bfloat16*>(W0p), piR, piP,
@@ -1713,6 +1767,11 @@ poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* par
                                                         desc->m, desc->n);
   POETX_LAUNCHED();
   return POETX_OK;
+}
+
+size_t poetx_weight_size(const poetx_layer_desc* desc) {
+  if (check_desc(desc) != POETX_OK) return 0;
+  return weight_bytes(*desc);
 }
 
 size_t poetx_workspace_size(const poetx_layer_desc* desc, int64_t T) {
@@ -1739,6 +1798,11 @@ poetx_status poetx_linear_fwd(const poetx_layer_desc* desc, const void* params, 
   Ctx c{*desc, L, work_layout(*desc, L, T, device_sm_count()),
         reinterpret_cast<const uint8_t*>(params), reinterpret_cast<uint8_t*>(workspace),
         reinterpret_cast<cudaStream_t>(stream)};
+  if (weight_int8(*desc)) {
+    auto* wdq = c.w<__nv_bfloat16>(c.W.off_wdq);
+    POETX_TRY(dequant_weight(c.st, *desc, W0p, wdq));
+    W0p = wdq;
+  }
   if (desc->dtype == POETX_DTYPE_FP32)
     return fwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X), T,
                     reinterpret_cast<float*>(Y), reinterpret_cast<float*>(saved_h),
@@ -1781,6 +1845,11 @@ poetx_status poetx_linear_bwd(const poetx_layer_desc* desc, const void* params, 
   const ParamsLayout L = params_layout(*desc);
   Ctx c{*desc, L, work_layout(*desc, L, T, device_sm_count()),
         reinterpret_cast<const uint8_t*>(params), reinterpret_cast<uint8_t*>(workspace), st};
+  if (weight_int8(*desc)) {
+    auto* wdq = c.w<__nv_bfloat16>(c.W.off_wdq);
+    POETX_TRY(dequant_weight(c.st, *desc, W0p, wdq));
+    W0p = wdq;
+  }
   if (desc->dtype == POETX_DTYPE_FP32)
     POETX_TRY(bwd_fp32(c, reinterpret_cast<const float*>(W0p), reinterpret_cast<const float*>(X),
                        reinterpret_cast<const float*>(dY), reinterpret_cast<const float*>(saved_h),
@@ -1836,9 +1905,20 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
     delta_superblock_kernel<<<grid_for(static_cast<int64_t>(L.R.nsb) * L.R.sb * L.R.sb), 256, 0, st>>>(
         BR, L.R.g, L.R.sb, L.R.nsb, 0, DRhi, DRlo);
     POETX_LAUNCHED();
-    POETX_TRY(tc_merge_pass<false>(st, reinterpret_cast<const __nv_bfloat16*>(W0p), nullptr, m, n,
-                                   L.P.sb, L.P.nsb, DPhi, DPlo, W1hi, W1lo));
-    POETX_TRY(tc_merge_pass<true>(st, W1hi, W1lo, n, m, L.R.sb, L.R.nsb, DRhi, DRlo, Kb, nullptr));
+    const bool q8 = weight_int8(*desc);
+    auto* Klo = q8 ? reinterpret_cast<__nv_bfloat16*>(ws + ML.off_Klo) : nullptr;
+    if (q8) {
+      // the exact scale * code as a hi + lo pair: the first pass then splits A too
+      auto* Wdq = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_Wdq);
+      auto* Wdqlo = reinterpret_cast<__nv_bfloat16*>(ws + ML.off_Wdqlo);
+      POETX_TRY(dequant_weight(st, *desc, W0p, Wdq, Wdqlo));
+      POETX_TRY(tc_merge_pass<true>(st, Wdq, Wdqlo, m, n, L.P.sb, L.P.nsb, DPhi, DPlo, W1hi, W1lo));
+    } else {
+      POETX_TRY(tc_merge_pass<false>(st, reinterpret_cast<const __nv_bfloat16*>(W0p), nullptr, m, n,
+                                     L.P.sb, L.P.nsb, DPhi, DPlo, W1hi, W1lo));
+    }
+    // int8 weights keep K as hi + lo so the codes come from the fp32-grade K
+    POETX_TRY(tc_merge_pass<true>(st, W1hi, W1lo, n, m, L.R.sb, L.R.nsb, DRhi, DRlo, Kb, Klo));
   } else {
     // T1 = W0' blockdiag(B_P): row-local blocks along n (not transposed).
     POETX_TRY(simt_blocks<float, float>(st, L.P, pb, reinterpret_cast<const float*>(W0p), T1, m, n,
@@ -1869,6 +1949,9 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
   for (int j = 0; j < n; ++j) rP[j] = oPi[nP[j]];
   POETX_TRY(ring_upload(st, {{rR.data(), rR.size()}, {rP.data(), rP.size()}}, {rhoR, rhoP}));
   const int grid = std::min(m, device_sm_count() * 8);
+  if (weight_int8(*desc))  // re-basing copy and row quantization in one pass
+    return quantize_weight(st, *desc, Kb, reinterpret_cast<const __nv_bfloat16*>(ws + ML.off_Klo), rhoR,
+                           rhoP, W0p);
   if (bf16)
     gather2d_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(
         Kb, reinterpret_cast<__nv_bfloat16*>(W0p), rhoR, rhoP, m, n);
@@ -1993,7 +2076,8 @@ poetx_status poetx_profile_read(int32_t kind, int64_t* groups, double* total_ms)
 
 const char* poetx_profile_kind_name(int32_t kind) {
   static const char* names[POETX_NUM_KINDS] = {"gemm_fwd", "gemm_dgrad", "blockdiag", "gradred",
-                                               "gather", "build", "genbwd", "merge", "simt"};
+                                               "gather", "build", "genbwd", "merge", "simt",
+                                               "dequant"};
   return (kind >= 0 && kind < POETX_NUM_KINDS) ? names[kind] : "unknown";
 }
 

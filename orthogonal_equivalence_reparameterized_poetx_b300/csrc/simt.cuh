@@ -816,6 +816,78 @@ __global__ void __launch_bounds__(256) delta_superblock_kernel(const float* __re
   }
 }
 
+// ------------------------------------------------------------------ POET-XQ
+// int8 base weights with a float32 scale per row.
+
+// out[i][j] = bf16(scale_i * code_ij), and with `lo` also the remainder
+// lo[i][j] = bf16(scale_i * code_ij - out[i][j]) (out + lo is the product to
+// 2^-17); eight codes per step (n % 8 == 0, so they share a row).
+__global__ void __launch_bounds__(256) dequant_int8_kernel(const int8_t* __restrict__ codes,
+                                                           const float* __restrict__ scales,
+                                                           __nv_bfloat16* __restrict__ out,
+                                                           __nv_bfloat16* __restrict__ lo, int m, int n) {
+  const int64_t chunks = static_cast<int64_t>(m) * n / 8;
+  for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < chunks;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = c * 8;
+    const float sc = scales[e / n];
+    const uint2 q = *reinterpret_cast<const uint2*>(codes + e);
+    uint32_t w[4], r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t word = k < 2 ? q.x : q.y;
+      const int sh = 16 * (k & 1);
+      const float a = sc * static_cast<float>(static_cast<int8_t>((word >> sh) & 0xFFu));
+      const float b = sc * static_cast<float>(static_cast<int8_t>((word >> (sh + 8)) & 0xFFu));
+      w[k] = pack_bf16x2(a, b);
+      const float ah = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w[k] & 0xFFFFu)));
+      const float bh = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w[k] >> 16)));
+      r[k] = pack_bf16x2(a - ah, b - bh);
+    }
+    *reinterpret_cast<uint4*>(out + e) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (lo) *reinterpret_cast<uint4*>(lo + e) = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+// Row i of a quantized weight: its values are v_j = S[row_map[i]][col_map[j]]
+// of a row-major source S with n columns, S = hi (+ lo when given, in fp32).
+// scale_i = max_j |v_j| / 127 and code_ij = round-half-to-even(v_j / scale_i)
+// clamped to [-127, 127], in float32 (IEEE division); a zero row gets scale 0
+// and codes 0.  One CTA per row; the source row is staged in shared memory
+// (its maximum is the maximum of the permuted row).
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16* __restrict__ hi,
+                                                            const __nv_bfloat16* __restrict__ lo,
+                                                            const int32_t* __restrict__ row_map,
+                                                            const int32_t* __restrict__ col_map, int n,
+                                                            int8_t* __restrict__ codes,
+                                                            float* __restrict__ scales) {
+  extern __shared__ float qrow[];
+  __shared__ float wmax[8];
+  const int i = blockIdx.x;
+  const int64_t src = static_cast<int64_t>(row_map[i]) * n;
+  float mx = 0.f;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    float v = __bfloat162float(hi[src + j]);
+    if (lo) v += __bfloat162float(lo[src + j]);
+    qrow[j] = v;
+    mx = fmaxf(mx, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (threadIdx.x % 32 == 0) wmax[threadIdx.x / 32] = mx;
+  __syncthreads();
+  mx = wmax[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x) / 32; ++w) mx = fmaxf(mx, wmax[w]);
+  const float sc = mx / 127.f;
+  int8_t* out = codes + static_cast<int64_t>(i) * n;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    int q = 0;
+    if (sc > 0.f) q = static_cast<int>(fminf(fmaxf(rintf(qrow[col_map[j]] / sc), -127.f), 127.f));
+    out[j] = static_cast<int8_t>(q);
+  }
+  if (threadIdx.x == 0) scales[i] = sc;
+}
+
 // ------------------------------------------------------------------ gradients
 // G[k](i,j) = sum over splits p of partial[p][s][(a - s*sb)][(c - s*sb)],
 // a = k*b + i, c = k*b + j, s = a / sb, in a fixed order (deterministic).

@@ -82,8 +82,17 @@ def test_params_size_validation():
     for d in bad:
         assert px.poetx_params_size(d) == 0
     d = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32")
-    d.reserved = 1
+    d.weight_format = 7
     assert px.poetx_params_size(d) == 0
+    # POET-XQ int8 storage is for bf16 layers only
+    assert px.poetx_params_size(px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32", weight="int8")) == 0
+    q = px.make_desc(96, 64, 32, 32, 1, 2, dtype="bf16", weight="int8")
+    assert px.poetx_params_size(q) > 0
+    # codes padded to 256 bytes, then one float scale per row
+    assert px.poetx_weight_size(q) == 96 * 64 + 512
+    assert px.poetx_weight_size(px.make_desc(96, 64, 32, 32, 1, 2, dtype="bf16")) == 96 * 64 * 2
+    assert px.poetx_workspace_size(q, 10) > px.poetx_workspace_size(
+        px.make_desc(96, 64, 32, 32, 1, 2, dtype="bf16"), 10)
     d = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32", mode="neumann", neumann_k=0)
     assert px.poetx_params_size(d) == 0
 
