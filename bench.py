@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--b", type=int, default=None, help="block size (default: first of the workload)")
     ap.add_argument("--mode", default="cayley", choices=["cayley", "neumann"])
+    ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
+                    help="replay each timed step from a CUDA graph (auto: for workloads "
+                         "without a per-step merge, whose new permutations come from the host)")
     ap.add_argument("--weight", default="dense", choices=["dense", "int8"],
                     help="storage of the base weight: layer dtype, or int8 rows (POET-XQ)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -395,10 +398,16 @@ def main():
         ready = []
         for li, st in enumerate(layers):
             ss = side[li]
-            ss.wait_event(bwd_done[li] if bwd_done[li] is not None else start)
+            # a merge must follow the layer's backward of the previous step;
+            # without merges the build only follows the step's start
+            dep = bwd_done[li] if (wl.merge_each_step and bwd_done[li] is not None) else start
+            ss.wait_event(dep)
             if wl.merge_each_step and bwd_done[li] is not None:
                 merge_one(li, st, ss, tag if tag is not None else step_counter[0])
-            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
+            if wl.merge_each_step:   # new seeds after the merge: permutations and blocks
+                px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
+            else:                    # same seeds: the blocks only (device work only)
+                px.poetx_blocks_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
             e = torch.cuda.Event()
             e.record(ss)
             ready.append(e)
@@ -449,9 +458,26 @@ def main():
     if px.poetx_device_status(reset=True) != px.POETX_OK:
         raise SystemExit("device status reported a timeout during warm-up")
 
+    use_graph = args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step)
+    if use_graph and wl.merge_each_step:
+        raise SystemExit("--graph on needs a workload without a per-step merge")
+    graph = None
+    if use_graph:
+        # one step captured once (the side-stream builds become graph branches);
+        # the library's timing events stay off inside the graph
+        px.poetx_profile_enable(False)
+        graph = torch.cuda.CUDAGraph()
+        l0 = px.poetx_launch_count()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        launches_per_step = px.poetx_launch_count() - l0
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
     # ---- timed region (device-resident inputs)
     px.poetx_profile_reset()
-    px.poetx_profile_enable(True)
+    px.poetx_profile_enable(not use_graph)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
     clocks = ClockSampler(gpu_idx)
@@ -463,13 +489,26 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     drain_merges(step_counter[0])   # the last timed step's merges
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    launches = px.poetx_launch_count() - launches0
+    launches = (launches_per_step * args.steps if graph is not None
+                else px.poetx_launch_count() - launches0)
     clk = clocks.stop()
     px.poetx_profile_enable(False)
+    if graph is not None:
+        # per-class device times (roofline) from the same steps run eagerly,
+        # right after the graph-timed region
+        px.poetx_profile_reset()
+        px.poetx_profile_enable(True)
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+        px.poetx_profile_enable(False)
     elapsed_ms = ev0.elapsed_time(ev1)
     if dist is not None:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -525,10 +564,14 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic: seeded N(0,1) activations, N(0,0.02^2) W0, "
                                    "N(0,0.01^2) packed generators",
-        "config": workload_config(wl, b, args, pipeline=pipe_info),
+        "config": dict(workload_config(wl, b, args, pipeline=pipe_info),
+                       cuda_graph=graph is not None),
         "tflops": tflops, "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
         "tflops_frac_of_bf16_burst": tflops / peaks["bf16"],
         "step_tflop": flops / 1e12, "roofline": roof, "kernels": kinds,
+        "kernels_timing": ("library CUDA events over the timed steps" if graph is None else
+                           "library CUDA events over as many eager steps run right after the "
+                           "graph-timed region"),
         "gpu_launches": launches, "clocks": clk,
         "device_status": px.poetx_status_string(status),
     }

@@ -136,6 +136,17 @@ poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR,
  * (0 for an invalid desc). */
 size_t poetx_weight_size(const poetx_layer_desc* desc);
 
+/* Rebuilds only the block matrices of params from new generators (the
+ * builder step of poetx_params_build), leaving the permutations that
+ * poetx_params_build wrote for the desc's seeds untouched.  It launches
+ * device work only (no host-to-device copies and no host synchronisation),
+ * so a training step that changes the generators but not the seeds can be
+ * captured in a CUDA graph with it.  Arguments and errors as for
+ * poetx_params_build; params must already hold the permutations of the
+ * desc's seeds. */
+poetx_status poetx_blocks_build(const poetx_layer_desc* desc, const float* genR,
+                                const float* genP, void* params, void* stream);
+
 /* Pre-merges the two permutations adjacent to W0 into it:
  * W0p[i][j] = W0[pi_R(i)][pi_P(j)].  W0 is row-major m x n of the layer
  * dtype; W0p is in the desc's weight format (for POETX_WEIGHT_INT8 the

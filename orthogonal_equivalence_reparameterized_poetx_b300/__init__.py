@@ -22,7 +22,7 @@ __all__ = [
     "PoetxError", "poetx_layer_desc", "LIB", "lib_path", "POETX_OK", "POETX_ERR_INVALID_ARG",
     "POETX_ERR_UNSUPPORTED", "POETX_ERR_MISALIGNED", "POETX_ERR_CUDA", "POETX_ERR_TIMEOUT",
     "MODE_CAYLEY", "MODE_NEUMANN", "DTYPE_FP32", "DTYPE_BF16", "WEIGHT_DENSE", "WEIGHT_INT8",
-    "make_desc", "poetx_weight_size",
+    "make_desc", "poetx_weight_size", "poetx_blocks_build",
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
@@ -47,7 +47,7 @@ EXPORTED_SYMBOLS = [
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "poetx_linear_fwd_noalloc", "poetx_set_pipeline", "poetx_pipeline_active",
-    "poetx_weight_size",
+    "poetx_weight_size", "poetx_blocks_build",
 ]
 
 # Size of the library's fixed forward scratch (POETX_NOALLOC_SCRATCH_BYTES).
@@ -100,6 +100,7 @@ def _load():
         "poetx_gen_length": (I64, [I32, I32]),
         "poetx_params_size": (SZ, [D]),
         "poetx_params_build": (I32, [D, P, P, P, P]),
+        "poetx_blocks_build": (I32, [D, P, P, P, P]),
         "poetx_weight_premerge": (I32, [D, P, P, P, P]),
         "poetx_workspace_size": (SZ, [D, I64]),
         "poetx_weight_size": (SZ, [D]),
@@ -183,6 +184,13 @@ def poetx_params_size(desc) -> int:
 def poetx_params_build(desc, genR, genP, params, stream=None):
     _check(LIB.poetx_params_build(ctypes.byref(desc), _ptr(genR), _ptr(genP), _ptr(params),
                                   _stream(stream)), "poetx_params_build")
+
+
+def poetx_blocks_build(desc, genR, genP, params, stream=None):
+    """Rebuild only the blocks of params (device work only; capturable in a
+    CUDA graph).  params must already hold the permutations of desc's seeds."""
+    _check(LIB.poetx_blocks_build(ctypes.byref(desc), _ptr(genR), _ptr(genP), _ptr(params),
+                                  _stream(stream)), "poetx_blocks_build")
 
 
 def poetx_weight_premerge(desc, params, W0, W0p, stream=None):
@@ -311,6 +319,10 @@ class Layer:
 
     def build(self, genR, genP, stream=None):
         poetx_params_build(self.desc, genR, genP, self.params, stream)
+
+    def rebuild(self, genR, genP, stream=None):
+        """New generators, same seeds: blocks only (capturable in a CUDA graph)."""
+        poetx_blocks_build(self.desc, genR, genP, self.params, stream)
 
     def premerge(self, W0, stream=None):
         poetx_weight_premerge(self.desc, self.params, W0, self.W0p, stream)

@@ -1715,6 +1715,27 @@ size_t poetx_params_size(const poetx_layer_desc* d) {
   return params_layout(*d).total;
 }
 
+poetx_status poetx_blocks_build(const poetx_layer_desc* desc, const float* genR, const float* genP,
+                                void* params, void* stream) {
+  POETX_TRY(check_desc(desc));
+  if (!params) return POETX_ERR_INVALID_ARG;
+  if ((poetx_gen_length(desc->m, desc->b_R) > 0 && !genR) ||
+      (poetx_gen_length(desc->n, desc->b_P) > 0 && !genP))
+    return POETX_ERR_INVALID_ARG;
+  if (!aligned(params, kAlign)) return POETX_ERR_MISALIGNED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ParamsLayout L = params_layout(*desc);
+  uint8_t* pb = reinterpret_cast<uint8_t*>(params);
+  if (desc->b_R == desc->b_P && fused_cayley_ok(*desc, desc->b_R)) {
+    ProfScope prof(POETX_KIND_BUILD, st);
+    const CayleySide r = cayley_side(*desc, L.R, genR, pb), p = cayley_side(*desc, L.P, genP, pb);
+    return launch_cayley_blocks(st, *desc, r, &p);
+  }
+  POETX_TRY(build_side(st, *desc, L.R, genR, pb));
+  POETX_TRY(build_side(st, *desc, L.P, genP, pb));
+  return POETX_OK;
+}
+
 poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR, const float* genP,
                                 void* params, void* stream) {
   POETX_TRY(check_desc(desc));
@@ -1733,14 +1754,7 @@ poetx_status poetx_params_build(const poetx_layer_desc* desc, const float* genR,
                         {{piR.data(), piR.size()}, {piRinv.data(), piRinv.size()},
                          {piP.data(), piP.size()}, {piPinv.data(), piPinv.size()}},
                         {pb + L.off_piR, pb + L.off_piRinv, pb + L.off_piP, pb + L.off_piPinv}));
-  if (desc->b_R == desc->b_P && fused_cayley_ok(*desc, desc->b_R)) {
-    ProfScope prof(POETX_KIND_BUILD, st);
-    const CayleySide r = cayley_side(*desc, L.R, genR, pb), p = cayley_side(*desc, L.P, genP, pb);
-    return launch_cayley_blocks(st, *desc, r, &p);
-  }
-  POETX_TRY(build_side(st, *desc, L.R, genR, pb));
-  POETX_TRY(build_side(st, *desc, L.P, genP, pb));
-  return POETX_OK;
+  return poetx_blocks_build(desc, genR, genP, params, stream);
 }
 
 poetx_status poetx_weight_premerge(const poetx_layer_desc* desc, const void* params, const void* W0,
