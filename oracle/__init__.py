@@ -49,6 +49,10 @@ Readings where the pages are silent (each is listed in the design notes):
   clamped to [-127, 127], computed in float32 (the arithmetic that decides
   an integer code is the kernel's); an all-zero row has scale 0 and codes 0.
   The dequantized weight is scale * code.
+* Generator optimizer step (the pages train with an optimizer they do not
+  name): AdamW with decoupled weight decay (Loshchilov & Hutter, "Decoupled
+  Weight Decay Regularization", ICLR 2019, Algorithm 2, with bias-corrected
+  moments as in Adam).
 
 Every function here is the plain definition: dense matrices, library
 matmuls as single steps, no blocking or fusion beyond what the definition
@@ -67,7 +71,7 @@ __all__ = [
     "inverse_gauss_jordan", "cayley", "neumann", "LayerSpec", "blocks_of",
     "orthogonal_factor", "dense_weight", "premerged_weight", "forward_dense",
     "forward_input_centric", "backward", "merge", "loss_for_fd",
-    "quantize_rows_int8", "dequantize_rows_int8",
+    "quantize_rows_int8", "dequantize_rows_int8", "adamw_step",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -428,3 +432,20 @@ def quantize_rows_int8(W) -> Tuple[np.ndarray, np.ndarray]:
 def dequantize_rows_int8(codes, scales) -> np.ndarray:
     """The weight a POET-XQ layer computes with: scale_i * code_ij (exact)."""
     return np.asarray(scales, dtype=np.float64)[:, None] * np.asarray(codes, dtype=np.float64)
+
+
+def adamw_step(theta, grad, m1, m2, step: int, lr: float, beta1: float, beta2: float, eps: float,
+               weight_decay: float):
+    """One AdamW step (decoupled weight decay), step counted from 1:
+        m1 <- beta1 m1 + (1 - beta1) g,     m2 <- beta2 m2 + (1 - beta2) g^2
+        mhat = m1 / (1 - beta1^step),        vhat = m2 / (1 - beta2^step)
+        theta <- theta - lr (mhat / (sqrt(vhat) + eps) + weight_decay theta)
+    Returns (theta, m1, m2) as new float64 arrays."""
+    th = np.asarray(theta, dtype=np.float64)
+    g = np.asarray(grad, dtype=np.float64)
+    m1 = beta1 * np.asarray(m1, dtype=np.float64) + (1.0 - beta1) * g
+    m2 = beta2 * np.asarray(m2, dtype=np.float64) + (1.0 - beta2) * g * g
+    mhat = m1 / (1.0 - beta1 ** step)
+    vhat = m2 / (1.0 - beta2 ** step)
+    th = th - lr * (mhat / (np.sqrt(vhat) + eps) + weight_decay * th)
+    return th, m1, m2

@@ -319,6 +319,37 @@ def test_int8_quantization_properties():
     assert np.array_equal(c2, codes[pr][:, pc]) and np.array_equal(s2, scales[pr])
 
 
+# ------------------------------------------------------------------ AdamW on the generators
+
+def test_adamw_first_step_closed_form():
+    # zero moments: mhat = g and vhat = g^2, so each entry moves by
+    # -lr (g / (|g| + eps) + wd theta): about -lr sign(g) for |g| >> eps
+    th = np.array([0.5, -0.25, 0.0, 1.0])
+    g = np.array([2.0, -1e-3, 0.5, 0.0])
+    lr, wd, eps = 0.1, 0.01, 1e-8
+    t1, m1, m2 = O.adamw_step(th, g, np.zeros(4), np.zeros(4), 1, lr, 0.9, 0.999, eps, wd)
+    want = th - lr * (g / (np.abs(g) + eps) + wd * th)
+    assert np.allclose(t1, want, rtol=0, atol=1e-15)
+    assert np.allclose(m1, 0.1 * g) and np.allclose(m2, 0.001 * g * g)
+
+
+def test_adamw_matches_torch_optim_adamw_over_steps():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    th0 = rng.standard_normal(50) * 0.01
+    grads = [rng.standard_normal(50) for _ in range(6)]
+    hp = dict(lr=3e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    p = torch.nn.Parameter(torch.tensor(th0, dtype=torch.float64))
+    opt = torch.optim.AdamW([p], **hp)
+    th, m1, m2 = th0.copy(), np.zeros(50), np.zeros(50)
+    for t, g in enumerate(grads, start=1):
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        th, m1, m2 = O.adamw_step(th, g, m1, m2, t, hp["lr"], *hp["betas"], hp["eps"],
+                                  hp["weight_decay"])
+    assert np.allclose(th, p.detach().numpy(), rtol=1e-12, atol=1e-15)
+
+
 def _pins_fail(monkeypatch, name, replacement, checks):
     monkeypatch.setattr(O, name, replacement)
     failed = 0
@@ -336,6 +367,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     orig_unpack, orig_apply = O.unpack_skew, O._apply_blocks
     orig_ggrad = O._generator_grad
     orig_quant = O.quantize_rows_int8
+    orig_adamw = O.adamw_step
     orig_perm = O.permutation
 
     def cayley_transposed(Q):
@@ -401,3 +433,14 @@ def test_planted_mistakes_are_caught(monkeypatch):
     qgold = lambda: test_int8_quantization_golden_rows()
     for bad in (quant_per_column, quant_over_128, quant_truncating):
         assert _pins_fail(monkeypatch, "quantize_rows_int8", bad, [qgold]) >= 1
+
+    def adamw_no_bias_correction(th, g, m1, m2, step, lr, b1, b2, eps, wd):
+        m1 = b1 * np.asarray(m1) + (1 - b1) * np.asarray(g)
+        m2 = b2 * np.asarray(m2) + (1 - b2) * np.asarray(g) ** 2
+        return np.asarray(th) - lr * (m1 / (np.sqrt(m2) + eps) + wd * np.asarray(th)), m1, m2
+    def adamw_coupled_decay(th, g, m1, m2, step, lr, b1, b2, eps, wd):
+        return orig_adamw(th, np.asarray(g) + wd * np.asarray(th), m1, m2, step, lr, b1, b2, eps, 0.0)
+    first = lambda: test_adamw_first_step_closed_form()
+    vs_torch = lambda: test_adamw_matches_torch_optim_adamw_over_steps()
+    for bad in (adamw_no_bias_correction, adamw_coupled_decay):
+        assert _pins_fail(monkeypatch, "adamw_step", bad, [first, vs_torch]) >= 1
