@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay each timed step from a CUDA graph (auto: for workloads "
                          "without a per-step merge, whose new permutations come from the host)")
+    ap.add_argument("--optimizer", default="none", choices=["none", "adamw"],
+                    help="end each layer's step with an AdamW update of its generators")
     ap.add_argument("--weight", default="dense", choices=["dense", "int8"],
                     help="storage of the base weight: layer dtype, or int8 rows (POET-XQ)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -292,6 +294,7 @@ def workload_config(wl, b, args, pipeline=None):
         "workload": wl.key, "description": wl.description,
         "linears": [f"{l.name}:{l.n}->{l.m}" for l in wl.linears],
         "tokens": wl.tokens, "b": b, "mode": args.mode, "weight": args.weight,
+        "optimizer": args.optimizer,
         "recompute": wl.recompute,
         "merge_each_step": wl.merge_each_step,
         "l2": "inputs larger than L2 (activations of all linears, several GB per step)",
@@ -361,6 +364,8 @@ def main():
         st["u"] = None if wl.recompute else torch.empty(T, lin.n, dtype=dt, device=dev)
         st["dgR"] = torch.empty(lr, dtype=torch.float32, device=dev)
         st["dgP"] = torch.empty(lp, dtype=torch.float32, device=dev)
+        if args.optimizer == "adamw":   # AdamW moments of the packed generators
+            st["mom"] = [torch.zeros(x, dtype=torch.float32, device=dev) for x in (lr, lr, lp, lp)]
         W0 = inp.W0.to(dev)
         px.poetx_params_build(desc, st["genR"], st["genP"], st["params"], stream)
         px.poetx_weight_premerge(desc, st["params"], W0, st["W0p"], stream)
@@ -444,6 +449,12 @@ def main():
             if dist is not None:
                 dist.all_reduce(st["dgR"])
                 dist.all_reduce(st["dgP"])
+            if args.optimizer == "adamw":
+                mR, vR, mP, vP = st["mom"]
+                px.poetx_generator_adamw(st["genR"], st["dgR"], mR, vR, st["lr"], s + 1, 1e-3,
+                                         0.9, 0.999, 1e-8, 0.0, stream)
+                px.poetx_generator_adamw(st["genP"], st["dgP"], mP, vP, st["lp"], s + 1, 1e-3,
+                                         0.9, 0.999, 1e-8, 0.0, stream)
             e = torch.cuda.Event()
             e.record(stream)
             bwd_done[li] = e
@@ -458,7 +469,9 @@ def main():
     if px.poetx_device_status(reset=True) != px.POETX_OK:
         raise SystemExit("device status reported a timeout during warm-up")
 
-    use_graph = args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step)
+    # (an optimizer step takes its step count from the host, so it stays eager)
+    use_graph = args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step
+                                       and args.optimizer == "none")
     if use_graph and wl.merge_each_step:
         raise SystemExit("--graph on needs a workload without a per-step merge")
     graph = None

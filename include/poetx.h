@@ -230,6 +230,21 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
                                     float* dGenP_dev, float* dGenR_host, float* dGenP_host,
                                     void* workspace, void* stream);
 
+/* One AdamW step on a packed generator array (the step after the backward).
+ * The pages train the generators with an optimizer they do not name; the
+ * reading is AdamW with decoupled weight decay (Loshchilov & Hutter, ICLR
+ * 2019) and bias-corrected moments.  For e < len, in fp32:
+ *   m1 = beta1 m1 + (1 - beta1) g;   m2 = beta2 m2 + (1 - beta2) g^2;
+ *   gen = gen (1 - lr weight_decay)
+ *         - (lr / (1 - beta1^step)) m1 / (sqrt(m2 / (1 - beta2^step)) + eps)
+ * with g = grad[e].  gen, grad, m1, m2: device float arrays of len entries
+ * (m1 and m2 zero before step 1); step >= 1; the bias corrections are
+ * computed on the host in double.  len = 0 is a no-op.
+ * Errors: INVALID_ARG, CUDA. */
+poetx_status poetx_generator_adamw(float* gen, const float* grad, float* m1, float* m2, int64_t len,
+                                   int64_t step, float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, void* stream);
+
 /* Reads (and with reset != 0 clears) the device status word that bounded
  * waits write.  Synchronises the device.  Returns POETX_OK, POETX_ERR_TIMEOUT
  * if any kernel gave up on a wait since the last reset, or POETX_ERR_CUDA. */

@@ -22,7 +22,7 @@ __all__ = [
     "PoetxError", "poetx_layer_desc", "LIB", "lib_path", "POETX_OK", "POETX_ERR_INVALID_ARG",
     "POETX_ERR_UNSUPPORTED", "POETX_ERR_MISALIGNED", "POETX_ERR_CUDA", "POETX_ERR_TIMEOUT",
     "MODE_CAYLEY", "MODE_NEUMANN", "DTYPE_FP32", "DTYPE_BF16", "WEIGHT_DENSE", "WEIGHT_INT8",
-    "make_desc", "poetx_weight_size", "poetx_blocks_build",
+    "make_desc", "poetx_weight_size", "poetx_blocks_build", "poetx_generator_adamw",
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
@@ -47,7 +47,7 @@ EXPORTED_SYMBOLS = [
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "poetx_linear_fwd_noalloc", "poetx_set_pipeline", "poetx_pipeline_active",
-    "poetx_weight_size", "poetx_blocks_build",
+    "poetx_weight_size", "poetx_blocks_build", "poetx_generator_adamw",
 ]
 
 # Size of the library's fixed forward scratch (POETX_NOALLOC_SCRATCH_BYTES).
@@ -110,6 +110,8 @@ def _load():
         "poetx_merge": (I32, [D, P, P, U64, U64, P, P]),
         "poetx_linear_step_host": (I32, [D, P, P, P, P, I64, P, P, P, P, P, P, P, P, P, P, P, P]),
         "poetx_device_status": (I32, [I32]),
+        "poetx_generator_adamw": (I32, [P, P, P, P, I64, I64, ctypes.c_float, ctypes.c_float,
+                                        ctypes.c_float, ctypes.c_float, ctypes.c_float, P]),
         "poetx_selftest_bounded_wait": (I32, [U64, P]),
         "poetx_set_wait_timeout_ns": (V, [U64]),
         "poetx_profile_enable": (V, [I32]),
@@ -247,6 +249,13 @@ def poetx_linear_step_host(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev,
         _ptr(dY_dev), _ptr(Y_dev), _ptr(saved_h_dev), _ptr(saved_u_dev), _ptr(dX_dev), _ptr(dGenR_dev),
         _ptr(dGenP_dev), _ptr(dGenR_host), _ptr(dGenP_host), _ptr(workspace), _stream(stream)),
         "poetx_linear_step_host")
+
+
+def poetx_generator_adamw(gen, grad, m1, m2, length, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                          weight_decay=0.0, stream=None):
+    _check(LIB.poetx_generator_adamw(_ptr(gen), _ptr(grad), _ptr(m1), _ptr(m2), length, step, lr,
+                                     beta1, beta2, eps, weight_decay, _stream(stream)),
+           "poetx_generator_adamw")
 
 
 def poetx_device_status(reset: bool = False) -> int:

@@ -2004,6 +2004,26 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
   return POETX_OK;
 }
 
+poetx_status poetx_generator_adamw(float* gen, const float* grad, float* m1, float* m2, int64_t len,
+                                   int64_t step, float lr, float beta1, float beta2, float eps,
+                                   float weight_decay, void* stream) {
+  if (len < 0 || step < 1) return POETX_ERR_INVALID_ARG;
+  if (len == 0) return POETX_OK;
+  if (!gen || !grad || !m1 || !m2) return POETX_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f && eps >= 0.f))
+    return POETX_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(step));
+  const float step_size = static_cast<float>(static_cast<double>(lr) / bc1);
+  const float inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  const float decay = static_cast<float>(1.0 - static_cast<double>(lr) * weight_decay);
+  adamw_kernel<<<grid_for(len), 256, 0, st>>>(gen, grad, m1, m2, len, beta1, beta2, eps, decay, step_size,
+                                               inv_sqrt_bc2);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 poetx_status poetx_device_status(int32_t reset) {
   POETX_CUDA(cudaDeviceSynchronize());
   unsigned int w = 0;

@@ -888,6 +888,26 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
   if (threadIdx.x == 0) scales[i] = sc;
 }
 
+// ------------------------------------------------------------------ optimizer
+// AdamW on packed generators: see poetx_generator_adamw.  step_size =
+// lr / (1 - beta1^t) and inv_sqrt_bc2 = 1 / sqrt(1 - beta2^t) come from the
+// host (double, rounded once).
+__global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ gen, const float* __restrict__ grad,
+                                                    float* __restrict__ m1, float* __restrict__ m2, int64_t len,
+                                                    float beta1, float beta2, float eps, float decay_factor,
+                                                    float step_size, float inv_sqrt_bc2) {
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < len;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float g = grad[e];
+    const float a = fmaf(beta1, m1[e], (1.f - beta1) * g);
+    const float b = fmaf(beta2, m2[e], (1.f - beta2) * g * g);
+    m1[e] = a;
+    m2[e] = b;
+    const float denom = sqrtf(b) * inv_sqrt_bc2 + eps;
+    gen[e] = gen[e] * decay_factor - step_size * (a / denom);
+  }
+}
+
 // ------------------------------------------------------------------ gradients
 // G[k](i,j) = sum over splits p of partial[p][s][(a - s*sb)][(c - s*sb)],
 // a = k*b + i, c = k*b + j, s = a / sb, in a fixed order (deterministic).
