@@ -396,19 +396,20 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
   }
   const size_t row_bytes = static_cast<size_t>(d) * sizeof(T);
   if constexpr (sizeof(T) == 2) {
-    // rows of at least 4 KB: persistent CTAs with two blocks of rows (about
-    // 48 KB each) in flight per CTA.  Narrower rows keep the pair-interleaved
-    // kernel below, whose short per-CTA iterations suit the smaller passes
-    // (measured on B300: the pipelined kernel is 18% faster at d = 2048 and
-    // 5% slower at d = 1024).
-    const int rb = static_cast<int>(std::max<size_t>(1, std::min<size_t>(32, (48 * 1024) / row_bytes)));
+    // rows of at least 4 KB: persistent CTAs (three per SM) with two blocks
+    // of rows (about 32 KB each) in flight per CTA.  Narrower rows keep the
+    // pair-interleaved kernel below, whose short per-CTA iterations suit the
+    // smaller passes (measured on B300: the pipelined kernel is 18% faster at
+    // d = 2048 and 5% slower at d = 1024; three CTAs of 32 KB blocks beat two
+    // of 48 KB by 2% at d = 2048 and 5% at d = 4096).
+    const int rb = static_cast<int>(std::max<size_t>(1, std::min<size_t>(32, (32 * 1024) / row_bytes)));
     const size_t psmem = 2 * rb * row_bytes + 64;
     if (row_bytes >= 4096 && psmem <= 200 * 1024) {
       static cudaError_t attr_err = cudaFuncSetAttribute(
           gather_rows_pipelined_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
       const int64_t nblocks = (rows + rb - 1) / rb;
-      const int grid = static_cast<int>(std::min<int64_t>(nblocks, launch_sms() * 2));
+      const int grid = static_cast<int>(std::min<int64_t>(nblocks, launch_sms() * 3));
       gather_rows_pipelined_kernel<<<grid, 256, psmem, st>>>(
           reinterpret_cast<const uint16_t*>(in), reinterpret_cast<uint4*>(out), idx, rows, d, rb,
           g_timeout_ns);
@@ -1353,6 +1354,19 @@ bool fused_cayley_bwd_ok(const poetx_layer_desc& d, int b) {
          (b == 32 || b == 64 || b == 128 || b == 256 || b == 512);
 }
 
+// 128-wide blocks of one or two sides on four-CTA clusters (side b may be empty).
+poetx_status launch_cayley_bwd_clusters(cudaStream_t st, const CbwdSide& a, const CbwdSide& b,
+                                        int accumulate) {
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      cayley_bwd_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCbwdSmem);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  const int blocks = a.s.nblk + b.s.nblk;
+  if (blocks == 0) return POETX_OK;
+  cayley_bwd_cluster_kernel<<<blocks * 4, 256, kCbwdSmem, st>>>(a, b, accumulate);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 // Fused reduction + Cayley backward + packing for one side (see cayley_bwd_kernel).
 poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_t* params,
                               const float* partial, int splits, float* t1, float* t2, float* dGen,
@@ -1386,13 +1400,9 @@ poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_
     return POETX_OK;
   }
   if (b == 128) {  // four CTAs (one cluster) per block
-    static cudaError_t attr_err = cudaFuncSetAttribute(
-        cayley_bwd_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCbwdSmem);
-    if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
-    cayley_bwd_cluster_kernel<<<S.g.nblk * 4, 256, kCbwdSmem, st>>>(partial, stride, splits, S.g, M,
-                                                                  dGen, accumulate);
-    POETX_LAUNCHED();
-    return POETX_OK;
+    CbwdSide a{partial, stride, splits, S.g, M, dGen}, none{};
+    none.s.nblk = 0;
+    return launch_cayley_bwd_clusters(st, a, none, accumulate);
   }
   auto kern = b == 64 ? cayley_bwd_kernel<64> : cayley_bwd_kernel<32>;
   const int threads = b == 64 ? cbwd_threads<64>() : cbwd_threads<32>();
@@ -1407,14 +1417,25 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
   float* t1 = c.w<float>(c.W.off_t1);
   float* t2 = c.w<float>(c.W.off_t2);
   float* nsc = c.w<float>(c.W.off_nsc);
-  if (dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0) {
+  const bool doR = dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0;
+  const bool doP = dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0;
+  if (doR && doP && c.d.b_R == 128 && c.d.b_P == 128 && fused_cayley_bwd_ok(c.d, 128)) {
+    // both sides' 128-wide blocks in one launch
+    ProfScope prof(POETX_KIND_GENBWD, c.st);
+    const CbwdSide r{c.w<float>(c.W.off_partR), static_cast<int64_t>(c.L.R.nsb) * c.L.R.sb * c.L.R.sb,
+                     c.slotsR, c.L.R.g, c.p<float>(c.L.R.off_M), dGenR};
+    const CbwdSide p{c.w<float>(c.W.off_partP), static_cast<int64_t>(c.L.P.nsb) * c.L.P.sb * c.L.P.sb,
+                     c.slotsP, c.L.P.g, c.p<float>(c.L.P.off_M), dGenP};
+    return launch_cayley_bwd_clusters(c.st, r, p, accumulate);
+  }
+  if (doR) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_R))
       POETX_TRY(fused_cayley_bwd(c.st, c.L.R, c.params, c.w<float>(c.W.off_partR), c.slotsR, t1, t2,
                                  dGenR, accumulate));
     else
       POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
   }
-  if (dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0) {
+  if (doP) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_P))
       POETX_TRY(fused_cayley_bwd(c.st, c.L.P, c.params, c.w<float>(c.W.off_partP), c.slotsP, t1, t2,
                                  dGenP, accumulate));

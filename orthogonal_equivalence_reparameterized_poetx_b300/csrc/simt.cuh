@@ -1099,17 +1099,38 @@ constexpr int kCbwdLD = 132;        // padded row of a 128-wide fp32 matrix
 constexpr int kCbwdTLD = 36;        // padded row of T^T (32 wide)
 constexpr int kCbwdSmem = (2 * 128 * kCbwdLD + 128 * kCbwdTLD + 32 * kCbwdLD) * 4;
 
+// One side's operands: split partials ([split][block][128][128]), M per
+// block, packed output.
+struct CbwdSide {
+  const float* partial;
+  int64_t split_stride;
+  int splits;
+  SideGeom s;
+  const float* M;
+  float* out;
+};
+
+// Clusters [0, a.s.nblk) work on side a, the rest on side b (both sides of a
+// layer in one launch).
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(256) cayley_bwd_cluster_kernel(
-    const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s,
-    const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
+    const CbwdSide a, const CbwdSide b, int accumulate) {
   constexpr int P = 128, LD = kCbwdLD, TLD = kCbwdTLD;
+  const int kg = blockIdx.x / 4;
+  const bool on_a = kg < a.s.nblk;
+  const CbwdSide& side = on_a ? a : b;
+  const float* __restrict__ partial = side.partial;
+  const int64_t split_stride = side.split_stride;
+  const int splits = side.splits;
+  const SideGeom s = side.s;
+  const float* __restrict__ Mall = side.M;
+  float* __restrict__ out = side.out;
   extern __shared__ __align__(16) float cbs[];
   float* Gs = cbs;               // G (all rows), then M^T
   float* Ms = Gs + P * LD;       // M
   float* Tt = Ms + P * LD;       // T^T: Tt[q][i - r0]
   float* Qs = Tt + P * TLD;      // GQ rows [r0, r0 + 32)
   const uint32_t rank = cluster_ctarank();
-  const int k = blockIdx.x / 4;
+  const int k = on_a ? kg : kg - a.s.nblk;
   const int r0 = 32 * static_cast<int>(rank);
   const int tid = threadIdx.x;
   const float* Mk = Mall + static_cast<int64_t>(k) * P * P;
