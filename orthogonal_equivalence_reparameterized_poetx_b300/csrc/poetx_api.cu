@@ -26,6 +26,7 @@
 #include "simt.cuh"
 #include "tc_gemm.cuh"
 #include "tc_bdgr.cuh"
+#include "tc_bdgr256.cuh"
 #include "tc_merge.cuh"
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
@@ -638,6 +639,16 @@ poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, con
 
 // Fused block transform + token reduction for 128-wide super-blocks:
 // out = in S^T per super-block and partial slots of in^T C (see tc_bdgr.cuh).
+// A fused transform + reduction grid is a whole number of token slots times
+// the CTAs of one slot; true when that covers at least 80% of the SMs.
+bool fused_grid_fills(int ctas_per_slot) {
+  const int sms = launch_sms();
+  return ctas_per_slot <= sms && 5 * (sms / ctas_per_slot) * ctas_per_slot >= 4 * sms;
+}
+
+// 128-wide super-blocks: fused whenever one slot fits (measured on B300 at
+// d = 11008, where one slot covers 86 of 148 SMs, it still beats the separate
+// transform and reduction: 4.19 vs 4.37 ms per step at d = 4096, b = 128).
 bool bdgr_ok(const SideLayout& S) { return S.sb == 128 && S.nsb <= launch_sms(); }
 
 poetx_status tc_bdgr(cudaStream_t st, const SideLayout& S, const void* in, const void* Ssb,
@@ -665,6 +676,39 @@ poetx_status tc_bdgr(cudaStream_t st, const SideLayout& S, const void* in, const
   });
   if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
   tc_bdgr_kernel<<<a.nslots * S.nsb, 320, BdgrCfg::SMEM, st>>>(ta, tsb, tc, to, a);
+  POETX_LAUNCHED();
+  *slots += a.nslots;
+  return POETX_OK;
+}
+
+// 256-wide super-blocks: two CTAs per super-block and token slot (one per
+// half of its output features), tiles of 64 tokens (tc_bdgr256.cuh).  Used
+// only when its grid fills the GPU (measured on B300 at d = 11008, 86 of 148
+// SMs: 5.94 ms per step against 5.16 for the separate passes at d = 4096,
+// b = 256; at d = 2048 it saves 0.3 ms per step).
+bool bdgr256_ok(const SideLayout& S) { return S.sb == 256 && fused_grid_fills(2 * S.nsb); }
+
+poetx_status tc_bdgr256(cudaStream_t st, const SideLayout& S, const void* in, const void* Ssb, void* out,
+                        const void* Cm, float* partial, int64_t T, int* slots) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_BLOCKDIAG, st);
+  const int d = S.g.d;
+  CUtensorMap ta, tsb, tc, to;
+  POETX_TRY(tmap_bf16(&ta, in, T, d, d, 64));
+  POETX_TRY(tmap_bf16(&tsb, Ssb, static_cast<uint64_t>(S.nsb) * 256, 256, 256, 128));
+  POETX_TRY(tmap_bf16(&tc, Cm, T, d, d, 64));
+  POETX_TRY(tmap_bf16(&to, out, T, d, d, 64));
+  Bdgr256Args a{};
+  a.M = static_cast<int>(T);
+  a.N = d;
+  a.nsb = S.nsb;
+  a.nslots = std::max(1, launch_sms() / (2 * S.nsb));
+  a.partial = partial;
+  a.timeout_ns = g_timeout_ns;
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      tc_bdgr256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Bdgr256Cfg::SMEM);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  tc_bdgr256_kernel<<<a.nslots * S.nsb * 2, 320, Bdgr256Cfg::SMEM, st>>>(ta, tsb, tc, to, a);
   POETX_LAUNCHED();
   *slots += a.nslots;
   return POETX_OK;
@@ -1556,6 +1600,8 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
     POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
     if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
       POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
+    } else if (bdgr256_ok(R)) {
+      POETX_TRY(tc_bdgr256(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
     } else {
       POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
       POETX_TRY(GR(0, c.st, 0));
@@ -1563,6 +1609,9 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
     POETX_TRY(D(0, c.st, 0));
     if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
       POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
+      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+    } else if (dX && bdgr256_ok(P)) {
+      POETX_TRY(tc_bdgr256(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
       POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
     } else {
       POETX_TRY(GPE(0, c.st, 0));
