@@ -130,22 +130,34 @@ def kind_bytes_per_step(wl, b: int, kind: str) -> float:
     backward, plus X -> u again when u is recomputed.  blockdiag: forward
     u -> v and h -> z; backward dz -> dh and dv -> du, which for b <= 128 also
     read h and u (the fused transform + reduction); plus u -> v when
-    recomputing.  gradred (b >= 256 only): dz^T h and dv^T u read two operands.
+    recomputing.  gradred (sides whose reduction is not fused): dz^T h and
+    dv^T u read two operands.  The fused kernels are used for b <= 128 and,
+    when their grid fills the GPU, for b = 256 (as the library decides).
     """
     T = wl.tokens
     e = 2 if wl.dtype == "bf16" else 4
     r = 1 if wl.recompute else 0
-    fused = b <= 128
+    sms = 148
+
+    def fused(d):  # the library's choice of the fused transform + reduction for one side
+        if b <= 128:
+            return -(-d // 128) <= sms
+        if b == 256:
+            cps = 2 * -(-d // 256)
+            return cps <= sms and 5 * (sms // cps) * cps >= 4 * sms
+        return False
+
     by = 0
     for lin in wl.linears:
         n, m = lin.n, lin.m
+        fm, fn = fused(m), fused(n)
         if kind == "gather":
             by += 2 * T * ((2 + r) * n + 2 * m) * e
         elif kind == "blockdiag":
-            bwd = (3 * m + 3 * n) if fused else (2 * m + 2 * n)
+            bwd = (3 if fm else 2) * m + (3 if fn else 2) * n
             by += T * (2 * n + 2 * m + bwd + 2 * n * r) * e
-        elif kind == "gradred" and not fused:
-            by += T * (2 * m + 2 * n) * e
+        elif kind == "gradred":
+            by += T * ((0 if fm else 2) * m + (0 if fn else 2) * n) * e
     return float(by)
 
 
