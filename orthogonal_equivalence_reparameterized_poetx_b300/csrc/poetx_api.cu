@@ -30,6 +30,7 @@
 #include "tc_merge.cuh"
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
+#include "cayley_cluster.cuh"
 
 using namespace poetx;
 
@@ -849,7 +850,7 @@ poetx_status dense_f32_gemm(bool tc, cudaStream_t st, int M, int N, int K, int b
 // ------------------------------------------------------------------ builder
 
 bool fused_cayley_ok(const poetx_layer_desc& d, int b) {
-  return d.mode == POETX_MODE_CAYLEY && b <= 128;
+  return d.mode == POETX_MODE_CAYLEY && (b <= 128 || b == 256 || b == 512);
 }
 
 CayleySide cayley_side(const poetx_layer_desc& d, const SideLayout& S, const float* gen,
@@ -873,6 +874,25 @@ CayleySide cayley_side(const poetx_layer_desc& d, const SideLayout& S, const flo
 poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, const CayleySide& a,
                                   const CayleySide* second) {
   const int b = a.s.b;
+  const int grid_blocks = a.s.nblk + (second ? second->s.nblk : 0);
+  if (b == 256 || b == 512) {
+    // one cluster of eight CTAs per block
+    static std::once_flag once_cluster;
+    std::call_once(once_cluster, [] {
+      cudaFuncSetAttribute(cayley_cluster_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(CcCfg<256>::SMEM));
+      cudaFuncSetAttribute(cayley_cluster_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(CcCfg<512>::SMEM));
+    });
+    if (b == 256)
+      cayley_cluster_kernel<256><<<CcCfg<256>::C * grid_blocks, 256, CcCfg<256>::SMEM, st>>>(
+          a, second ? *second : a);
+    else
+      cayley_cluster_kernel<512><<<CcCfg<512>::C * grid_blocks, 512, CcCfg<512>::SMEM, st>>>(
+          a, second ? *second : a);
+    POETX_LAUNCHED();
+    return POETX_OK;
+  }
   static std::once_flag once;
   std::call_once(once, [] {
     const int lim = 128 * 129 * 4;
@@ -883,7 +903,7 @@ poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, co
   });
   const size_t smem = d.dtype == POETX_DTYPE_BF16 ? static_cast<size_t>(b) * (b + 1) * 4 : 0;
   const int R = std::min(b, 1024 / b);
-  const int grid = a.s.nblk + (second ? second->s.nblk : 0);
+  const int grid = grid_blocks;
   auto kern = b == 128 ? cayley_block_kernel<128>
             : b == 64  ? cayley_block_kernel<64>
             : b == 32  ? cayley_block_kernel<32>
@@ -2046,6 +2066,35 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
   return POETX_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// One non-blocking stream per device for the second host-to-device copy of
+// poetx_linear_step_host, created on first use and kept for the process;
+// nullptr if it cannot be created (both copies then go on the caller's
+// stream).
+cudaStream_t step_copy_stream() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    (void)cudaGetLastError();
+    streams[dev] = nullptr;
+  }
+  return streams[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
 poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params, const void* W0p,
                                     const void* X_host, const void* dY_host, int64_t T, void* X_dev,
                                     void* dY_dev, void* Y_dev, void* saved_h_dev, void* saved_u_dev,
@@ -2059,12 +2108,36 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
   const size_t e = desc->dtype == POETX_DTYPE_BF16 ? 2 : 4;
   POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, static_cast<size_t>(T) * desc->n * e,
                              cudaMemcpyHostToDevice, st));
-  POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
-                             cudaMemcpyHostToDevice, st));
-  POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, saved_u_dev, workspace,
-                             stream));
-  POETX_TRY(poetx_linear_bwd(desc, params, W0p, X_dev, dY_dev, saved_h_dev, saved_u_dev, T, dX_dev,
-                             dGenR_dev, dGenP_dev, 0, workspace, stream));
+  // dY is copied on a second stream once X has arrived, so that it crosses
+  // the host link while the forward runs (the two copies would only share
+  // the link if they overlapped each other); the backward waits for it.
+  // The wait on an event of `st` also orders the copy after all earlier
+  // work on `st`, which may still read dY_dev.
+  cudaStream_t cs = step_copy_stream();
+  Ev x_done, dy_done;
+  if (cs) {
+    POETX_TRY(x_done.record(st));
+    POETX_TRY(x_done.wait_on(cs));
+    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
+                               cudaMemcpyHostToDevice, cs));
+    POETX_TRY(dy_done.record(cs));
+  } else {
+    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
+                               cudaMemcpyHostToDevice, st));
+  }
+  auto run = [&]() -> poetx_status {
+    POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, saved_u_dev,
+                               workspace, stream));
+    if (cs) POETX_TRY(dy_done.wait_on(st));
+    return poetx_linear_bwd(desc, params, W0p, X_dev, dY_dev, saved_h_dev, saved_u_dev, T, dX_dev,
+                            dGenR_dev, dGenP_dev, 0, workspace, stream);
+  };
+  const poetx_status rs = run();
+  if (rs != POETX_OK) {
+    // the dY copy may still be reading the caller's host buffer
+    if (cs) (void)cudaStreamSynchronize(cs);
+    return rs;
+  }
   const int64_t lr = poetx_gen_length(desc->m, desc->b_R), lp = poetx_gen_length(desc->n, desc->b_P);
   if (lr > 0)
     POETX_CUDA(cudaMemcpyAsync(dGenR_host, dGenR_dev, lr * 4, cudaMemcpyDeviceToHost, st));

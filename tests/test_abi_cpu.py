@@ -120,6 +120,16 @@ def test_argument_errors_return_before_launch():
     # the backward needs X or a saved u
     assert L.poetx_linear_bwd(D, 256, 256, None, 256, None, None, 4, None, 256, 256, 0, 256,
                               None) == px.POETX_ERR_INVALID_ARG
+    # the host step needs both host inputs, both device input buffers and
+    # both host gradient outputs (checked before any copy)
+    for missing in range(6):
+        ptrs = [256] * 6
+        ptrs[missing] = None
+        xh, dyh, xd, dyd, gh_r, gh_p = ptrs
+        assert L.poetx_linear_step_host(D, 256, 256, xh, dyh, 4, xd, dyd, 256, None, None, None,
+                                        256, 256, gh_r, gh_p, 256, None) == px.POETX_ERR_INVALID_ARG
+    assert L.poetx_linear_step_host(D, 256, 256, 256, 256, -1, 256, 256, 256, None, None, None,
+                                    256, 256, 256, 256, 256, None) == px.POETX_ERR_INVALID_ARG
     # invalid descriptor
     bad = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32")
     bad.mode = 7

@@ -66,8 +66,22 @@ def test_fp32_neumann(px):
     _case(px, 128, 128, 32, 32, 100, "fp32", mode="neumann", gstd=0.05)
 
 
-def test_fp32_blocked_builder_b256(px):
+def test_fp32_cluster_builder_b256(px):
+    # 256-wide blocks: one cluster of eight CTAs per block
     _case(px, 512, 384, 256, 128, 64, "fp32", gstd=0.02)
+
+
+@pytest.mark.parametrize("gstd", [0.02, 0.1])
+def test_fp32_cluster_builder_b512_ragged(px, gstd):
+    # 768 = 512 + 256 and 640 = 512 + 128: ragged last blocks inverted as the
+    # identity-padded 512 x 512 matrix; gstd = 0.1 gives ||Q|| of several units
+    _case(px, 768, 640, 512, 512, 64, "fp32", gstd=gstd)
+
+
+def test_fp32_blocked_builder_b384(px):
+    # a block size that is neither <= 128 nor 256 / 512: the panel-wise
+    # Gauss-Jordan builder with batched products
+    _case(px, 768, 384, 384, 384, 64, "fp32", gstd=0.02)
 
 
 # ------------------------------------------------------------------ bf16 path
