@@ -31,6 +31,7 @@
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
 #include "cayley_cluster.cuh"
+#include "tc_neumann.cuh"
 
 using namespace poetx;
 
@@ -913,6 +914,55 @@ poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, co
   return POETX_OK;
 }
 
+// bf16 layers build 128-, 256- and 512-wide Neumann blocks in one launch
+// with fp32-grade tensor-core products; fp32 layers keep CUDA-core products
+// (the split-bf16 products are not fp32 round-off).
+bool fused_neumann_ok(const poetx_layer_desc& d, int b) {
+  return d.mode == POETX_MODE_NEUMANN && d.dtype == POETX_DTYPE_BF16 &&
+         (b == 128 || b == 256 || b == 512);
+}
+
+NeumannSide neumann_side(const SideLayout& S, const float* gen, uint8_t* params) {
+  NeumannSide n;
+  n.gen = gen;
+  n.s = S.g;
+  n.B = reinterpret_cast<float*>(params + S.off_B);
+  n.Q = reinterpret_cast<float*>(params + S.off_Q);
+  n.S0 = reinterpret_cast<float*>(params + S.off_s1);
+  n.S1 = reinterpret_cast<float*>(params + S.off_s2);
+  n.sb = S.sb;
+  n.Bsb = reinterpret_cast<__nv_bfloat16*>(params + S.off_Bsb);
+  n.BsbT = reinterpret_cast<__nv_bfloat16*>(params + S.off_BsbT);
+  return n;
+}
+
+template <int BS>
+void launch_neumann_kernel(cudaStream_t st, const NeumannSide& a, const NeumannSide& b2, int blocks,
+                           int k) {
+  using Cfg = NeuCfg<BS>;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(tc_neumann_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  });
+  tc_neumann_kernel<BS><<<Cfg::C * blocks, Cfg::THREADS, Cfg::SMEM, st>>>(a, b2, k, g_timeout_ns);
+}
+
+// Neumann blocks of one side, or of both sides at once when `second` is
+// given (same block size), in a single launch.
+poetx_status launch_neumann_blocks(cudaStream_t st, const poetx_layer_desc& d, const NeumannSide& a,
+                                   const NeumannSide* second) {
+  const int blocks = a.s.nblk + (second ? second->s.nblk : 0);
+  const NeumannSide& b2 = second ? *second : a;
+  switch (a.s.b) {
+    case 128: launch_neumann_kernel<128>(st, a, b2, blocks, d.neumann_k); break;
+    case 256: launch_neumann_kernel<256>(st, a, b2, blocks, d.neumann_k); break;
+    case 512: launch_neumann_kernel<512>(st, a, b2, blocks, d.neumann_k); break;
+    default: return POETX_ERR_UNSUPPORTED;
+  }
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLayout& S,
                         const float* gen, uint8_t* params) {
   ProfScope prof(POETX_KIND_BUILD, st);
@@ -925,6 +975,7 @@ poetx_status build_side(cudaStream_t st, const poetx_layer_desc& d, const SideLa
     POETX_TRY(launch_cayley_blocks(st, d, cayley_side(d, S, gen, params), nullptr));
     return POETX_OK;
   }
+  if (fused_neumann_ok(d, b)) return launch_neumann_blocks(st, d, neumann_side(S, gen, params), nullptr);
   // bf16 layers run the dense products of the build on the tensor cores
   // with fp32-grade (split bf16) operands; fp32 layers keep fp32 CUDA cores
   const bool tcg = d.dtype == POETX_DTYPE_BF16;
@@ -1820,6 +1871,11 @@ poetx_status poetx_blocks_build(const poetx_layer_desc* desc, const float* genR,
     ProfScope prof(POETX_KIND_BUILD, st);
     const CayleySide r = cayley_side(*desc, L.R, genR, pb), p = cayley_side(*desc, L.P, genP, pb);
     return launch_cayley_blocks(st, *desc, r, &p);
+  }
+  if (desc->b_R == desc->b_P && fused_neumann_ok(*desc, desc->b_R)) {
+    ProfScope prof(POETX_KIND_BUILD, st);
+    const NeumannSide r = neumann_side(L.R, genR, pb), p = neumann_side(L.P, genP, pb);
+    return launch_neumann_blocks(st, *desc, r, &p);
   }
   POETX_TRY(build_side(st, *desc, L.R, genR, pb));
   POETX_TRY(build_side(st, *desc, L.P, genP, pb));

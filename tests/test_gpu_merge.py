@@ -81,15 +81,25 @@ def test_premerge_is_an_exact_permutation_copy(px):
     assert np.array_equal(layer.W0p.float().cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("m,n,b", [(384, 256, 32), (512, 640, 128), (768, 512, 256)])
-def test_bf16_merge_is_rounded_once_from_a_near_exact_product(px, m, n, b):
+@pytest.mark.parametrize("m,n,b,mode,k", [
+    (384, 256, 32, "cayley", 3), (512, 640, 128, "cayley", 3), (768, 512, 256, "cayley", 3),
+    (768, 512, 512, "cayley", 3),
+    # Neumann blocks built by the fused tensor-core builder: B itself must be
+    # fp32-grade for the merged weight to stay within half an ulp
+    (512, 640, 128, "neumann", 3), (768, 512, 256, "neumann", 2), (768, 512, 512, "neumann", 3),
+    (512, 384, 256, "neumann", 6),
+])
+def test_bf16_merge_is_rounded_once_from_a_near_exact_product(px, m, n, b, mode, k):
     """The bf16 merge runs on the tensor cores with bf16 operands, splitting
     B - I and the intermediate into hi + lo bf16 pairs; the result must still
     be the exact R W0 P (re-based) rounded once to bf16: every element within
     half a bf16 ulp of the fp64 oracle's value, plus slack at the fp32 level
-    (the blocks themselves are built in fp32)."""
-    inp = make_inputs(m, n, b, b, 1, "bf16", index=7, gstd=0.05)
-    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16")
+    (the blocks themselves are built to fp32 accuracy)."""
+    # Neumann blocks with the workloads' generator scale (||Q|| < 1, where the
+    # series is a good orthogonal approximation); Cayley blocks larger
+    gstd = 0.01 if mode == "neumann" else 0.05
+    inp = make_inputs(m, n, b, b, 1, "bf16", index=7, gstd=gstd)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16", mode=mode, neumann_k=k)
     layer = px.Layer(desc, 1)
     layer.build(inp.genR.cuda(), inp.genP.cuda())
     layer.premerge(inp.W0.cuda())
@@ -98,7 +108,8 @@ def test_bf16_merge_is_rounded_once_from_a_near_exact_product(px, m, n, b):
     torch.cuda.synchronize()
     assert px.poetx_device_status(reset=True) == px.POETX_OK
     got = layer.W0p.double().cpu().numpy()
-    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P)
+    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P,
+                       "neumann" if mode == "neumann" else "exact", k)
     want = O.merge(spec, inp.W0.double().numpy(), inp.genR.double().numpy(),
                    inp.genP.double().numpy(), new_R, new_P)
     a = np.abs(want)

@@ -147,6 +147,17 @@ def test_bf16_neumann(px):
     _case(px, 256, 256, 128, 128, 200, "bf16", mode="neumann", gstd=0.05)
 
 
+@pytest.mark.parametrize("k", [1, 2, 6])
+def test_bf16_neumann_fused_builder_orders(px, k):
+    # the fused tensor-core builder runs k products; 384 = 256 + 128 ragged
+    _case(px, 512, 384, 256, 256, 200, "bf16", mode="neumann", k=k, gstd=0.02)
+
+
+def test_bf16_neumann_b512_ragged(px):
+    # eight-CTA clusters per 512-wide block; 768 = 512 + 256 ragged
+    _case(px, 768, 512, 512, 512, 130, "bf16", mode="neumann", gstd=0.01)
+
+
 def test_bf16_single_token_and_single_block(px):
     _case(px, 128, 128, 128, 128, 1, "bf16")
 
