@@ -1,14 +1,14 @@
-// Exact Cayley blocks of size 256 or 512 in one launch: one cluster of eight
-// CTAs per block.
+// Exact Cayley blocks of size 256 or 512 in one launch: one cluster per
+// block (two CTAs of 128 rows at b = 256, eight of 64 rows at b = 512).
 //
 // "POET-X：基于正交变换缩放的内存高效LLM训练方法", 实践 2: B = (I+Q)(I-Q)^-1,
 // which equals 2M - I with M = (I - Q)^-1 (the factors commute).  CTA c of a
 // block's cluster keeps rows [c*RB, c*RB + RB) of the working matrix
-// A = I - Q in shared memory (RB = b / 8) and the cluster inverts A in place
+// A = I - Q in shared memory and the cluster inverts A in place
 // by Gauss-Jordan, W = 32 pivots per panel K = [k0, k0 + W):
 //
 //   D = A_KK^-1                          (every CTA, from the owner's rows)
-//   R = D A_K*                           (each CTA forms b/8 of its columns)
+//   R = D A_K*                           (each CTA forms RB of its columns)
 //   A_ij -= A_iK R_Kj     i, j outside K
 //   A_iK  = -A_iK D       i outside K
 //   A_K*  = R,  A_KK = D  (the owner of the pivot rows)
@@ -31,36 +31,43 @@ namespace poetx {
 
 template <int BS>
 struct CcCfg {
-  static constexpr int C = 8;           // CTAs per block
-  static constexpr int RB = BS / C;     // rows of A per CTA
-  static constexpr int W = 32;          // pivots per panel
-  static constexpr int CS = BS / C;     // columns of R each CTA forms
-  static constexpr int NW = BS / 32;    // warps
-  static constexpr int U = W / NW;      // rows of the pivot block per warp
-  static constexpr int DLD = W + 1;     // leading dimension of the inverted pivot block
-  static constexpr int RLD = W + 4;     // leading dimension of the transposed R slice
+  // b = 256: two CTAs of 1024 threads; b = 512: eight CTAs of 512 threads
+  // (fewer, wider CTAs hold an SM for less time in total; at b = 512 the
+  // 128 KB of rows per CTA allows one CTA per SM and 512 threads keep the
+  // per-pivot barriers cheap)
+  static constexpr int C = BS == 256 ? 2 : 8;  // CTAs per block (one cluster)
+  static constexpr int NT = BS == 256 ? 1024 : 512;  // threads per CTA
+  static constexpr int RB = BS / C;           // rows of A per CTA
+  static constexpr int TPC = NT / BS;         // threads per column
+  static constexpr int RPT = RB / TPC;        // rows per thread
+  static constexpr int W = 32;                // pivots per panel
+  static constexpr int CS = BS / C;           // columns of R each CTA forms
+  static constexpr int NW = NT / 32;          // warps
+  static constexpr int U = W / NW;            // pivot-block rows per warp
+  static constexpr int DLD = W + 1;           // leading dimension of the inverted pivot block
+  static constexpr int RLD = W + 4;           // leading dimension of the transposed R slice
   static constexpr int A_F = RB * BS;
   static constexpr int D_F = W * DLD + 2 * W;  // inverse, then two pivot-row buffers
   static constexpr int CP_F = RB * W;
   static constexpr int AK_F = W * CS;
   static constexpr int RS_F = CS * RLD;
   static constexpr size_t SMEM = static_cast<size_t>(A_F + D_F + CP_F + AK_F + RS_F) * 4;
-  static_assert(RB % W == 0 && RB % 8 == 0 && W % NW == 0, "panel shape");
-  static_assert((W * W) % BS == 0 && (W * CS) % BS == 0 && (RB * W) % BS == 0, "work split");
+  static_assert(W % NW == 0 && RPT % W == 0, "pivot-block rows per warp; whole panels per thread");
+  static_assert((W * CS) % NT == 0 && (RB * W) % NT == 0 && RB % W == 0, "work split");
   static_assert(D_F % 4 == 0 && A_F % 4 == 0, "16-byte alignment of the buffers");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Blocks [0, first.s.nblk) belong to `first`, the rest to `second`; both
-// sides have block size BS.  Grid: 8 CTAs per block, BS threads each
-// (thread j owns column j of the CTA's rows).
+// sides have block size BS.  Grid: C CTAs per block, NT threads each:
+// thread t owns column t % BS of the CTA's rows [RPT (t / BS), RPT (t / BS) + RPT).
 template <int BS>
-__global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
+__global__ void __cluster_dims__(CcCfg<BS>::C, 1, 1) __launch_bounds__(CcCfg<BS>::NT, 1)
     cayley_cluster_kernel(const CayleySide first, const CayleySide second) {
   using Cfg = CcCfg<BS>;
-  constexpr int C = Cfg::C, RB = Cfg::RB, W = Cfg::W, CS = Cfg::CS, NW = Cfg::NW, U = Cfg::U;
-  constexpr int DLD = Cfg::DLD, RLD = Cfg::RLD;
-  constexpr int E_AK = W * CS / BS, E_CP = RB * W / BS;
+  constexpr int C = Cfg::C, RB = Cfg::RB, W = Cfg::W, CS = Cfg::CS, NT = Cfg::NT;
+  constexpr int RPT = Cfg::RPT, DLD = Cfg::DLD, RLD = Cfg::RLD, NW = Cfg::NW, U = Cfg::U;
+  constexpr int E_AK = W * CS / NT, E_CP = RB * W / NT;
   extern __shared__ __align__(16) float ccs[];
   float* A = ccs;                 // own rows of the working matrix, RB x BS
   float* Dinv = A + Cfg::A_F;     // the inverted pivot block, W x DLD
@@ -76,8 +83,10 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
   const uint32_t rank = cluster_ctarank();
   const int r0 = RB * static_cast<int>(rank);
   const int c0 = CS * static_cast<int>(rank);
-  const int j = static_cast<int>(threadIdx.x);
-  const int warp = j / 32, lane = j % 32;
+  const int tid = static_cast<int>(threadIdx.x);
+  const int j = tid % BS;                 // column
+  const int i0 = RPT * (tid / BS);        // first of this thread's rows (within the CTA)
+  const int warp = tid / 32, lane = tid % 32;
   const int sz = block_size(cs.s, k);
   const int64_t base = static_cast<int64_t>(k) * BS * BS;
   const float* g = cs.gen + static_cast<int64_t>(k) * BS * (BS - 1) / 2;
@@ -85,11 +94,11 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
   // 1. own rows of Q (unpacked from the strict upper triangle, entry (i, j),
   //    i < j, at i*sz - i(i+1)/2 + (j-i-1)) and of A = I - Q; eight rows'
   //    loads in flight at a time
-  for (int i0 = 0; i0 < RB; i0 += 8) {
+  for (int t0 = 0; t0 < RPT; t0 += 8) {
     float q[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int gi = r0 + i0 + t;
+      const int gi = r0 + i0 + t0 + t;
       q[t] = 0.f;
       if (gi < sz && j < sz && gi != j)
         q[t] = gi < j ? g[gi * sz - gi * (gi + 1) / 2 + (j - gi - 1)]
@@ -97,9 +106,9 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
     }
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const int gi = r0 + i0 + t;
+      const int gi = r0 + i0 + t0 + t;
       cs.Q[base + static_cast<int64_t>(gi) * BS + j] = q[t];
-      A[(i0 + t) * BS + j] = (gi == j ? 1.f : 0.f) - q[t];
+      A[(i0 + t0 + t) * BS + j] = (gi == j ? 1.f : 0.f) - q[t];
     }
   }
 
@@ -119,22 +128,22 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
       d[u] = dsmem_ld_f(oA + 4u * static_cast<uint32_t>((ok0 + warp + NW * u) * BS + k0 + lane));
 #pragma unroll
     for (int u = 0; u < E_AK; ++u) {
-      const int e = j + BS * u, p = e / CS, jj = e % CS;
+      const int e = tid + NT * u, p = e / CS, jj = e % CS;
       ak[u] = dsmem_ld_f(oA + 4u * static_cast<uint32_t>((ok0 + p) * BS + c0 + jj));
     }
 #pragma unroll
     for (int u = 0; u < E_CP; ++u) {
-      const int e = j + BS * u, i = e / W, p = e % W;
+      const int e = tid + NT * u, i = e / W, p = e % W;
       cp[u] = A[i * BS + k0 + p];
     }
 #pragma unroll
     for (int u = 0; u < E_AK; ++u) {
-      const int e = j + BS * u, p = e / CS, jj = e % CS;
+      const int e = tid + NT * u, p = e / CS, jj = e % CS;
       AK[p * CS + jj] = ak[u];
     }
 #pragma unroll
     for (int u = 0; u < E_CP; ++u) {
-      const int e = j + BS * u, i = e / W, p = e % W;
+      const int e = tid + NT * u, i = e / W, p = e % W;
       Cp[i * W + p] = cp[u];
     }
     if (warp == 0) rowbuf[lane] = d[0];  // pivot row 0 (warp 0, u = 0)
@@ -150,14 +159,11 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float f = __shfl_sync(0xffffffffu, d[u], p);
-        const int i = warp + NW * u;
-        float v;
-        if (i == p) v = (lane == p) ? inv : rq;
-        else v = (lane == p) ? -f * inv : fmaf(-f, rq, d[u]);
-        d[u] = v;
+        if (warp + NW * u == p) d[u] = (lane == p) ? inv : rq;
+        else d[u] = (lane == p) ? -f * inv : fmaf(-f, rq, d[u]);
       }
       const int pn = p + 1;
-      if (pn < W && (pn % NW) == warp) {
+      if (pn < W && pn % NW == warp) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
           if (u == pn / NW) rowbuf[(pn & 1) * W + lane] = d[u];
@@ -167,10 +173,10 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
     for (int u = 0; u < U; ++u) Dinv[(warp + NW * u) * DLD + lane] = d[u];
     __syncthreads();
     // this CTA's columns of R = D A_K* (columns inside K are never read);
-    // thread j forms E_AK entries of one column jj
+    // thread t forms E_AK entries of one column jj
     {
-      const int jj = j % CS, p0 = j / CS;
-      constexpr int PS = BS / CS;  // row stride between a thread's entries
+      const int jj = tid % CS, p0 = tid / CS;
+      constexpr int PS = NT / CS;  // row stride between a thread's entries
       if (!(c0 + jj >= k0 && c0 + jj < k0 + W)) {
         float acc[E_AK];
 #pragma unroll
@@ -186,7 +192,7 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
       }
     }
     cluster_sync();  // every CTA's columns of R are complete
-    // the panel column of thread j
+    // the panel column of thread t's column j
     const bool inK = j >= k0 && j < k0 + W;
     float r[W];
     if (inK) {
@@ -203,28 +209,33 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
         r[4 * q4 + 3] = v.w;
       }
     }
-    // rank-W update of the own rows outside K, four rows at a time
+    // rank-W update of the thread's rows outside K, four at a time; the
+    // pivot rows get R outside K and D inside
+    const bool has_pivots = own_pivots && ok0 >= i0 && ok0 < i0 + RPT;
+    {
 #pragma unroll 1
-    for (int i0 = 0; i0 < RB; i0 += 4) {
-      if (own_pivots && i0 >= ok0 && i0 < ok0 + W) continue;
-      float acc[4];
+      for (int t0 = 0; t0 < RPT; t0 += 4) {
+        const int i = i0 + t0;
+        if (has_pivots && i >= ok0 && i < ok0 + W) continue;
+        float acc[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) acc[t] = inK ? 0.f : A[(i0 + t) * BS + j];
+        for (int t = 0; t < 4; ++t) acc[t] = inK ? 0.f : A[(i + t) * BS + j];
 #pragma unroll
-      for (int q4 = 0; q4 < W / 4; ++q4) {
+        for (int q4 = 0; q4 < W / 4; ++q4) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float4 c = reinterpret_cast<const float4*>(Cp + (i0 + t) * W)[q4];
-          acc[t] = fmaf(-c.x, r[4 * q4], acc[t]);
-          acc[t] = fmaf(-c.y, r[4 * q4 + 1], acc[t]);
-          acc[t] = fmaf(-c.z, r[4 * q4 + 2], acc[t]);
-          acc[t] = fmaf(-c.w, r[4 * q4 + 3], acc[t]);
+          for (int t = 0; t < 4; ++t) {
+            const float4 c = reinterpret_cast<const float4*>(Cp + (i + t) * W)[q4];
+            acc[t] = fmaf(-c.x, r[4 * q4], acc[t]);
+            acc[t] = fmaf(-c.y, r[4 * q4 + 1], acc[t]);
+            acc[t] = fmaf(-c.z, r[4 * q4 + 2], acc[t]);
+            acc[t] = fmaf(-c.w, r[4 * q4 + 3], acc[t]);
+          }
         }
-      }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) A[(i0 + t) * BS + j] = acc[t];
+        for (int t = 0; t < 4; ++t) A[(i + t) * BS + j] = acc[t];
+      }
     }
-    if (own_pivots) {  // pivot rows: R outside K, D inside
+    if (has_pivots) {
 #pragma unroll
       for (int p = 0; p < W; ++p) A[(ok0 + p) * BS + j] = r[p];
     }
@@ -232,11 +243,11 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
   // no CTA leaves while another may still read its shared memory
   cluster_sync();
 
-  // 3. outputs of the own rows: M, B = 2M - I, and for bf16 layers the
+  // 3. outputs of the thread's rows: M, B = 2M - I, and for bf16 layers the
   //    super-block arrays (super-block = block here): Bsb rows are rows of B,
   //    BsbT rows are columns of B
-  for (int i = 0; i < RB; ++i) {
-    const int gi = r0 + i;
+  for (int t = 0; t < RPT; ++t) {
+    const int i = i0 + t, gi = r0 + i;
     const float mv = A[i * BS + j];
     const float bv = 2.f * mv - (gi == j ? 1.f : 0.f);
     cs.M[base + static_cast<int64_t>(gi) * BS + j] = mv;
@@ -245,16 +256,17 @@ __global__ void __cluster_dims__(8, 1, 1) __launch_bounds__(BS, 1)
     A[i * BS + j] = bv;
   }
   if (cs.BsbT) {
-    // thread j writes row k*BS + j of BsbT, columns [r0, r0 + RB), from its
-    // own column of A (no other thread wrote it)
-    __nv_bfloat16* dst = cs.BsbT + (static_cast<int64_t>(k) * BS + j) * cs.sb + r0;
+    // row k*BS + j of BsbT, columns [r0 + i0, r0 + i0 + RPT), from this
+    // thread's own entries of A (no other thread wrote them)
+    __nv_bfloat16* dst = cs.BsbT + (static_cast<int64_t>(k) * BS + j) * cs.sb + r0 + i0;
 #pragma unroll 1
-    for (int i8 = 0; i8 < RB; i8 += 8) {
+    for (int i8 = 0; i8 < RPT; i8 += 8) {
+      const float* a = A + (i0 + i8) * BS + j;
       uint4 v;
-      v.x = pack_bf16x2(A[(i8 + 0) * BS + j], A[(i8 + 1) * BS + j]);
-      v.y = pack_bf16x2(A[(i8 + 2) * BS + j], A[(i8 + 3) * BS + j]);
-      v.z = pack_bf16x2(A[(i8 + 4) * BS + j], A[(i8 + 5) * BS + j]);
-      v.w = pack_bf16x2(A[(i8 + 6) * BS + j], A[(i8 + 7) * BS + j]);
+      v.x = pack_bf16x2(a[0], a[BS]);
+      v.y = pack_bf16x2(a[2 * BS], a[3 * BS]);
+      v.z = pack_bf16x2(a[4 * BS], a[5 * BS]);
+      v.w = pack_bf16x2(a[6 * BS], a[7 * BS]);
       *reinterpret_cast<uint4*>(dst + i8) = v;
     }
   }

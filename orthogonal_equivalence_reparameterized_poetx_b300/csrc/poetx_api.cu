@@ -877,7 +877,7 @@ poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, co
   const int b = a.s.b;
   const int grid_blocks = a.s.nblk + (second ? second->s.nblk : 0);
   if (b == 256 || b == 512) {
-    // one cluster of eight CTAs per block
+    // one cluster per block
     static std::once_flag once_cluster;
     std::call_once(once_cluster, [] {
       cudaFuncSetAttribute(cayley_cluster_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -886,10 +886,10 @@ poetx_status launch_cayley_blocks(cudaStream_t st, const poetx_layer_desc& d, co
                            static_cast<int>(CcCfg<512>::SMEM));
     });
     if (b == 256)
-      cayley_cluster_kernel<256><<<CcCfg<256>::C * grid_blocks, 256, CcCfg<256>::SMEM, st>>>(
+      cayley_cluster_kernel<256><<<CcCfg<256>::C * grid_blocks, CcCfg<256>::NT, CcCfg<256>::SMEM, st>>>(
           a, second ? *second : a);
     else
-      cayley_cluster_kernel<512><<<CcCfg<512>::C * grid_blocks, 512, CcCfg<512>::SMEM, st>>>(
+      cayley_cluster_kernel<512><<<CcCfg<512>::C * grid_blocks, CcCfg<512>::NT, CcCfg<512>::SMEM, st>>>(
           a, second ? *second : a);
     POETX_LAUNCHED();
     return POETX_OK;
