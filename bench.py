@@ -68,6 +68,9 @@ def parse():
                          "(CHUNKS 1 disables it); default: the library's setting")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small profiling cases only)")
+    ap.add_argument("--builds-only", action="store_true",
+                    help="time only the block builds (poetx_blocks_build) of each linear, "
+                         "in isolation, and print one JSON line")
     return ap.parse_args()
 
 
@@ -316,6 +319,36 @@ def workload_config(wl, b, args, pipeline=None):
 
 # ---------------------------------------------------------------- the CUDA path
 
+def run_builds_only(args, wl, b, px, torch, dev):
+    """Isolated device time of poetx_blocks_build (both sides of a layer) per
+    linear: CUDA events around K builds after W warm-up builds."""
+    per = []
+    for li, lin in enumerate(wl.linears):
+        desc = px.make_desc(lin.m, lin.n, b, b, synth.SEED_PERM_R + li, synth.SEED_PERM_P + li,
+                            dtype=wl.dtype, mode=args.mode, weight=args.weight)
+        lr, lp = px.poetx_gen_length(lin.m, b), px.poetx_gen_length(lin.n, b)
+        g = np.random.default_rng([synth.SEED_GEN_R + li, 0])
+        genR = torch.from_numpy((g.standard_normal(lr) * synth.STD_GEN).astype(np.float32)).to(dev)
+        genP = torch.from_numpy((g.standard_normal(lp) * synth.STD_GEN).astype(np.float32)).to(dev)
+        params = torch.empty(px.poetx_params_size(desc), dtype=torch.uint8, device=dev)
+        px.poetx_params_build(desc, genR, genP, params)
+        for _ in range(args.warmup):
+            px.poetx_blocks_build(desc, genR, genP, params)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(args.steps):
+            px.poetx_blocks_build(desc, genR, genP, params)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        per.append({"linear": f"{lin.name}:{lin.n}->{lin.m}", "ms": e0.elapsed_time(e1) / args.steps})
+    st = px.poetx_device_status(reset=True)
+    print(json.dumps({"metric": "block build time per linear (both sides, isolated)", "unit": "ms",
+                      "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+                      "config": {"workload": wl.key, "b": b, "mode": args.mode, "dtype": wl.dtype},
+                      "per_linear": per, "device_status": px.poetx_status_string(st)}))
+
+
 def main():
     args = parse()
     wl = synth.WORKLOADS[args.workload]
@@ -335,6 +368,9 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.builds_only:
+        run_builds_only(args, wl, b, px, torch, dev)
+        return
     if args.pipeline:
         ch, fs, bs = (int(x) for x in args.pipeline.split(","))
         px.poetx_set_pipeline(ch, fs, bs, 0)
