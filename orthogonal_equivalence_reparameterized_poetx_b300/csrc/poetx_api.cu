@@ -32,6 +32,7 @@
 #include "tc_gemm2.cuh"
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
+#include "tc_neumann_bwd.cuh"
 
 using namespace poetx;
 
@@ -306,7 +307,9 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   W.off_t1 = off; off = align_up(off + gmax);
   W.off_t2 = off; off = align_up(off + gmax);
   W.off_nsc = off;
-  if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * (d.neumann_k + 3));
+  // Neumann scratch: the batched chain rule keeps k + 3 matrices per side;
+  // the fused tensor-core backward keeps five per side for both sides
+  if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * std::max(d.neumann_k + 3, 10));
   W.off_wdq = off;  // dequantized int8 weight (bf16 m x n)
   if (weight_int8(d)) off = align_up(off + static_cast<size_t>(d.m) * d.n * 2);
   W.total = off;
@@ -1526,6 +1529,39 @@ poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_
   return POETX_OK;
 }
 
+// bf16 Neumann layers with 128-wide blocks: the chain rule of the
+// polynomial for every block of one side, or of both sides when `second` is
+// given, in one tensor-core launch.  Measured on d2048 (k = 3): at b = 128
+// it cuts the generator backward from 2.05 to 1.36 ms per step; at b = 256
+// and 512 its 2k dependent products per CTA are slower than the batched
+// products over 128 x 128 tiles (3.2 vs 2.5-2.8 ms at b = 256), so those keep
+// the batched chain rule.
+bool fused_neumann_bwd_ok(const poetx_layer_desc& d, int b) { return fused_neumann_ok(d, b) && b == 128; }
+
+template <int BS>
+void launch_neumann_bwd_kernel(cudaStream_t st, const NeumannBwdSide& a, const NeumannBwdSide& b2,
+                               int blocks, int k, int accumulate) {
+  using Cfg = NeuCfg<BS>;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(tc_neumann_bwd_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::SMEM);
+  });
+  tc_neumann_bwd_kernel<BS><<<Cfg::C * blocks, Cfg::THREADS, Cfg::SMEM, st>>>(a, b2, k, accumulate,
+                                                                             g_timeout_ns);
+}
+
+poetx_status launch_neumann_bwd(cudaStream_t st, const poetx_layer_desc& d, const NeumannBwdSide& a,
+                                const NeumannBwdSide* second, int accumulate) {
+  ProfScope prof(POETX_KIND_GENBWD, st);
+  const int blocks = a.s.nblk + (second ? second->s.nblk : 0);
+  const NeumannBwdSide& b2 = second ? *second : a;
+  if (a.s.b != 128) return POETX_ERR_UNSUPPORTED;
+  launch_neumann_bwd_kernel<128>(st, a, b2, blocks, d.neumann_k, accumulate);
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
 poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accumulate) {
   float* GR = c.w<float>(c.W.off_GR);
   float* GP = c.w<float>(c.W.off_GP);
@@ -1542,6 +1578,23 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
     const CbwdSide p{c.w<float>(c.W.off_partP), static_cast<int64_t>(c.L.P.nsb) * c.L.P.sb * c.L.P.sb,
                      c.slotsP, c.L.P.g, c.p<float>(c.L.P.off_M), dGenP};
     return launch_cayley_bwd_clusters(c.st, r, p, accumulate);
+  }
+  if (fused_neumann_bwd_ok(c.d, c.d.b_R) || fused_neumann_bwd_ok(c.d, c.d.b_P)) {
+    // five scratch matrices per side: side R at nsc, side P after them
+    const int64_t gstride = static_cast<int64_t>(std::max(c.L.R.g.nblk * c.L.R.bb(),
+                                                          c.L.P.g.nblk * c.L.P.bb()));
+    const float* Qr = c.p<float>(c.L.R.off_Q);
+    const float* Qp = c.p<float>(c.L.P.off_Q);
+    const NeumannBwdSide r{GR, Qr, nsc, gstride, c.L.R.g, dGenR};
+    const NeumannBwdSide p{GP, Qp, nsc + 5 * gstride, gstride, c.L.P.g, dGenP};
+    const bool fr = doR && fused_neumann_bwd_ok(c.d, c.d.b_R);
+    const bool fp = doP && fused_neumann_bwd_ok(c.d, c.d.b_P);
+    if (fr && fp && c.d.b_R == c.d.b_P) return launch_neumann_bwd(c.st, c.d, r, &p, accumulate);
+    if (fr) POETX_TRY(launch_neumann_bwd(c.st, c.d, r, nullptr, accumulate));
+    else if (doR) POETX_TRY(generator_backward(c.st, c.d, c.L.R, c.params, GR, t1, t2, nsc, dGenR, accumulate));
+    if (fp) POETX_TRY(launch_neumann_bwd(c.st, c.d, p, nullptr, accumulate));
+    else if (doP) POETX_TRY(generator_backward(c.st, c.d, c.L.P, c.params, GP, t1, t2, nsc, dGenP, accumulate));
+    return POETX_OK;
   }
   if (doR) {
     if (fused_cayley_bwd_ok(c.d, c.d.b_R))

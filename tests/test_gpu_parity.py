@@ -164,9 +164,15 @@ def test_bf16_single_token_and_single_block(px):
 
 # ------------------------------------------------------------------ other ABI behaviour
 
-def test_accumulate_adds_into_generator_gradients(px):
-    inp = make_inputs(256, 256, 64, 64, 200, "bf16")
-    desc = px.make_desc(256, 256, 64, 64, inp.seed_R, inp.seed_P, dtype="bf16")
+@pytest.mark.parametrize("m,n,b,mode", [
+    (256, 256, 64, "cayley"),
+    (384, 256, 128, "neumann"),     # fused tensor-core Neumann backward (b = 128)
+    (512, 384, 256, "cayley"),
+    (768, 512, 512, "neumann"),     # batched Neumann chain rule
+])
+def test_accumulate_adds_into_generator_gradients(px, m, n, b, mode):
+    inp = make_inputs(m, n, b, b, 200, "bf16")
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16", mode=mode)
     g = run_gpu(px, desc, inp, recompute=True)
     layer = g["layer"]
     dev = "cuda"
