@@ -24,9 +24,9 @@ def px():
     return m
 
 
-def _setup(px, m, n, b, T, dtype="bf16"):
+def _setup(px, m, n, b, T, dtype="bf16", mode="cayley"):
     inp = make_inputs(m, n, b, b, T, dtype, index=8, gstd=0.02)
-    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype=dtype)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype=dtype, mode=mode)
     layer = px.Layer(desc, T)
     layer.build(inp.genR.cuda(), inp.genP.cuda())
     layer.premerge(inp.W0.cuda())
@@ -48,10 +48,10 @@ def _snapshot(B):
     return [B[k].clone() for k in ("Y", "dX", "dgR", "dgP")]
 
 
-@pytest.mark.parametrize("b", [64, 256])
-def test_blocks_build_equals_params_build(px, b):
+@pytest.mark.parametrize("b,mode", [(64, "cayley"), (256, "cayley"), (128, "neumann"), (256, "neumann")])
+def test_blocks_build_equals_params_build(px, b, mode):
     m, n, T = 512, 384, 200
-    inp, desc, layer, B = _setup(px, m, n, b, T)
+    inp, desc, layer, B = _setup(px, m, n, b, T, mode=mode)
     g2R, g2P = (inp.genR * 1.5).cuda(), (inp.genP * -0.5).cuda()
     _step(layer, g2R, g2P, B)
     torch.cuda.synchronize()
@@ -67,10 +67,15 @@ def test_blocks_build_equals_params_build(px, b):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("m,n,b", [(512, 1376, 32), (2048, 1024, 128)])
-def test_captured_step_replays_bit_identically(px, m, n, b):
+@pytest.mark.parametrize("m,n,b,mode", [
+    (512, 1376, 32, "cayley"), (2048, 1024, 128, "cayley"),
+    (768, 512, 512, "cayley"),      # cluster Gauss-Jordan builder, ragged block
+    (640, 384, 128, "neumann"),     # tensor-core Neumann builder and backward
+    (512, 768, 256, "neumann"),     # tensor-core Neumann builder, batched backward
+])
+def test_captured_step_replays_bit_identically(px, m, n, b, mode):
     T = 1000
-    inp, desc, layer, B = _setup(px, m, n, b, T)
+    inp, desc, layer, B = _setup(px, m, n, b, T, mode=mode)
     genR, genP = inp.genR.cuda().clone(), inp.genP.cuda().clone()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
