@@ -66,6 +66,11 @@ def test_fp32_neumann(px):
     _case(px, 128, 128, 32, 32, 100, "fp32", mode="neumann", gstd=0.05)
 
 
+def test_fp32_neumann_b256_ragged(px):
+    # fp32 layers keep CUDA-core products for the Neumann build and chain rule
+    _case(px, 512, 384, 256, 256, 64, "fp32", mode="neumann", gstd=0.02)
+
+
 def test_fp32_cluster_builder_b256(px):
     # 256-wide blocks: one cluster of eight CTAs per block
     _case(px, 512, 384, 256, 128, 64, "fp32", gstd=0.02)

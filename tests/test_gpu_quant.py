@@ -50,9 +50,9 @@ def _original_basis(Wp, piR, piP):
     return W
 
 
-def _layer(px, m, n, b, T, index, gstd=0.01, tokens=None):
+def _layer(px, m, n, b, T, index, gstd=0.01, tokens=None, mode="cayley"):
     inp = make_inputs(m, n, b, b, T, "bf16", index=index, gstd=gstd)
-    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16", weight="int8")
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16", weight="int8", mode=mode)
     layer = px.Layer(desc, T)
     layer.build(inp.genR.cuda(), inp.genP.cuda())
     layer.premerge(inp.W0.cuda())
@@ -71,12 +71,13 @@ def test_premerge_quantizes_exactly_like_the_oracle(px, m, n, b):
     assert np.array_equal(codes, want_c)
 
 
-@pytest.mark.parametrize("m,n,b,T,recompute", [
-    (512, 384, 128, 300, False),
-    (1376, 1032, 64, 777, True),    # CTA-pair GEMMs, ragged tiles and blocks
+@pytest.mark.parametrize("m,n,b,T,recompute,mode", [
+    (512, 384, 128, 300, False, "cayley"),
+    (1376, 1032, 64, 777, True, "cayley"),    # CTA-pair GEMMs, ragged tiles and blocks
+    (640, 384, 128, 300, False, "neumann"),   # int8 weights with Neumann blocks
 ])
-def test_int8_layer_matches_the_oracle_on_the_dequantized_weight(px, m, n, b, T, recompute):
-    inp, desc, layer = _layer(px, m, n, b, T, index=4)
+def test_int8_layer_matches_the_oracle_on_the_dequantized_weight(px, m, n, b, T, recompute, mode):
+    inp, desc, layer = _layer(px, m, n, b, T, index=4, mode=mode)
     X, dY = inp.X.cuda(), inp.dY.cuda()
     Y = torch.empty(T, m, dtype=torch.bfloat16, device="cuda")
     h = None if recompute else torch.empty(T, m, dtype=torch.bfloat16, device="cuda")
@@ -91,7 +92,7 @@ def test_int8_layer_matches_the_oracle_on_the_dequantized_weight(px, m, n, b, T,
     codes, scales = _split(layer.W0p, m, n)
     piR, piP = O.permutation(inp.seed_R, m), O.permutation(inp.seed_P, n)
     W0q = _original_basis(O.dequantize_rows_int8(codes, scales), piR, piP)
-    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P)
+    spec = O.LayerSpec(m, n, b, b, inp.seed_R, inp.seed_P, "neumann" if mode == "neumann" else "exact", 3)
     dX_o, dgR_o, dgP_o, ex = O.backward(spec, W0q, inp.X.double().numpy(), inp.dY.double().numpy(),
                                         inp.genR.double().numpy(), inp.genP.double().numpy())
     errs = {"Y": rel_fro(Y.double().cpu().numpy(), ex["Y"]),
