@@ -698,12 +698,13 @@ poetx_status tc_bdgr256(cudaStream_t st, const SideLayout& S, const void* in, co
   if (T <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_BLOCKDIAG, st);
   const int d = S.g.d;
-  CUtensorMap ta, tsb, tc, to;
+  CUtensorMap ta, tc, to;
   POETX_TRY(tmap_bf16(&ta, in, T, d, d, 64));
-  POETX_TRY(tmap_bf16(&tsb, Ssb, static_cast<uint64_t>(S.nsb) * 256, 256, 256, 128));
   POETX_TRY(tmap_bf16(&tc, Cm, T, d, d, 64));
   POETX_TRY(tmap_bf16(&to, out, T, d, d, 64));
+  if (!aligned(Ssb, 16)) return POETX_ERR_MISALIGNED;
   Bdgr256Args a{};
+  a.S = reinterpret_cast<const __nv_bfloat16*>(Ssb);
   a.M = static_cast<int>(T);
   a.N = d;
   a.nsb = S.nsb;
@@ -713,7 +714,7 @@ poetx_status tc_bdgr256(cudaStream_t st, const SideLayout& S, const void* in, co
   static cudaError_t attr_err = cudaFuncSetAttribute(
       tc_bdgr256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Bdgr256Cfg::SMEM);
   if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
-  tc_bdgr256_kernel<<<a.nslots * S.nsb * 2, 320, Bdgr256Cfg::SMEM, st>>>(ta, tsb, tc, to, a);
+  tc_bdgr256_kernel<<<a.nslots * S.nsb * 2, 320, Bdgr256Cfg::SMEM, st>>>(ta, tc, to, a);
   POETX_LAUNCHED();
   *slots += a.nslots;
   return POETX_OK;

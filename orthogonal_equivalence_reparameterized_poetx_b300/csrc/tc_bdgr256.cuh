@@ -11,13 +11,16 @@
 //   out[:, s][:, 128r .. 128r+127] = A[:, s] (rows 128r.. of S_s)^T
 //     as a transposed MMA: D (128 output features x 64 tokens) = S_half A_tile^T
 //   G rows 128r .. 128r+127 (all 256 columns) += A[:, s half r]^T C[:, s]
-// keeping its half of S_s resident in shared memory (64 KB, loaded once) and
-// its 128 x 256 reduction rows in TMEM for all its tiles; the rows are written
+// keeping its half of S_s resident in TMEM (loaded once, the A operand of the
+// transform MMAs, so no shared-memory operand traffic for it) and its
+// 128 x 256 reduction rows in TMEM for all its tiles; the rows are written
 // once as partial `slot` (layout [slot][s][256][256] fp32).
-// Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 epilogue.
+// Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 S loader, then
+// epilogue.
 // Stage: A tile and C tile, 64 tokens x 256 features each as four 64-feature
-// boxes with 128-byte swizzle (2 x 32 KB); two stages, plus a 16 KB output
-// tile.  TMEM: [0, 256) reduction, [256, 384) two transform accumulators.
+// boxes with 128-byte swizzle (2 x 32 KB); three stages, plus a 16 KB output
+// tile.  TMEM: [0, 256) reduction, [256, 384) two transform accumulators,
+// [384, 512) the S half (row f in lane f, features 2c, 2c + 1 in column c).
 #pragma once
 
 #include "ptx.cuh"
@@ -30,6 +33,7 @@ struct Bdgr256Args {
   int nsb;        // 256-wide super-blocks
   int nslots;     // CTAs per (super-block, half)
   float* partial; // [nslots][nsb][256][256]
+  const __nv_bfloat16* S;  // super-block matrices: nsb * 256 rows of 256
   uint64_t timeout_ns;
 };
 
@@ -37,25 +41,21 @@ struct Bdgr256Cfg {
   static constexpr int TBOX = 64 * 64 * 2;     // 64 tokens x 64 features: 8 KB
   static constexpr int TILE = 4 * TBOX;        // 64 tokens x 256 features: 32 KB
   static constexpr int STAGE = 2 * TILE;       // A and C
-  static constexpr int STAGES = 2;
-  static constexpr int SBOX = 128 * 64 * 2;    // 128 rows x 64 k: 16 KB
-  static constexpr int SHALF = 4 * SBOX;       // 128 rows x 256 k: 64 KB
+  static constexpr int STAGES = 3;
   static constexpr int OUT = 2 * TBOX;         // 64 tokens x 128 features: 16 KB
-  static constexpr int SMEM = 1024 + SHALF + STAGES * STAGE + OUT + 256;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + OUT + 256;
   static_assert(SMEM <= 232448, "shared memory");
 };
 
 __global__ void __launch_bounds__(320, 1)
-    tc_bdgr256_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
-                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmOut,
-                      const Bdgr256Args args) {
+    tc_bdgr256_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmOut, const Bdgr256Args args) {
   using Cfg = Bdgr256Cfg;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* s_half = smem;                                  // resident half of S_s
-  uint8_t* stages = smem + Cfg::SHALF;
+  uint8_t* stages = smem;
   uint8_t* out_stage = stages + STAGES * Cfg::STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT);
   uint64_t* empty = full + STAGES;
@@ -85,12 +85,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 256);
     }
-    mbar_init(sfull, 1);
+    mbar_init(sfull, 256);  // the S loader threads
     mbar_init(gdone, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmS);
     tma_prefetch_desc(&tmC);
     tma_prefetch_desc(&tmOut);
   }
@@ -106,19 +105,11 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      bool s_issued = false;
-      if (ntiles > 0) {
-        // rows f0 + 128 r .. +127 of the S array, 256 k in four 64-wide boxes
-        mbar_arrive_expect_tx(sfull, Cfg::SHALF);
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-          tma_load_2d(s_half + kb * Cfg::SBOX, &tmS, sfull, 64 * kb, f0 + 128 * r);
-        s_issued = true;
-      }
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[STAGES] = {0, 0};
-      bool issued[STAGES] = {false, false};
+      uint32_t issued_phase[STAGES];
+      bool issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued[i] = false, issued_phase[i] = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int m0 = (slot + i * args.nslots) * 64;
         if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) break;
@@ -135,20 +126,20 @@ __global__ void __launch_bounds__(320, 1)
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
       volatile int never = 0;
-      if (s_issued) mbar_wait(sfull, 0, tmo, &never);
       for (int i = 0; i < STAGES; ++i)
         if (issued[i]) mbar_wait(&full[i], issued_phase[i], tmo, &never);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      // transform: D (128 features x 64 tokens) = S_half (K-major) x A_tile^T (K-major)
+      // transform: D (128 features x 64 tokens) = S_half (TMEM) x A_tile^T (K-major)
       constexpr uint32_t idesc_t = idesc_bf16_f32(128, 64, false, false);
       // reduction: G (128 features x 256 features) += A_half^T (MN-major) x C (MN-major)
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, 256, true, true);
       const uint32_t d_g = tmem_base;
-      const uint32_t sh = smem_u32(s_half);
+      const uint32_t s_tmem = tmem_base + 384;
       bool ok = ntiles == 0 || mbar_wait(sfull, 0, tmo, abort_flag);
+      if (ok) tc_fence_after();
       int stage = 0;
       uint32_t phase = 0;
       for (int i = 0; i < ntiles && ok; ++i) {
@@ -163,10 +154,9 @@ __global__ void __launch_bounds__(320, 1)
         // K = 256 features in 16 steps of 16 (four 64-wide boxes)
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * Cfg::SBOX + (kk & 3) * 32;
           const uint32_t kb = (kk >> 2) * Cfg::TBOX + (kk & 3) * 32;
-          mma_bf16_f32(d_t, smem_desc_sw128(sh + ka, 16, 1024), smem_desc_sw128(sa + kb, 16, 1024),
-                       idesc_t, kk != 0 ? 1u : 0u);
+          mma_bf16_f32_ta(d_t, s_tmem + 8 * kk, smem_desc_sw128(sa + kb, 16, 1024), idesc_t,
+                          kk != 0 ? 1u : 0u);
         }
         // K = 64 tokens in 4 steps of 16 rows; A's 128 features are boxes
         // 2r, 2r + 1 (one box apart), C's 256 features are all four boxes
@@ -192,6 +182,28 @@ __global__ void __launch_bounds__(320, 1)
     const int half = (warp - 2) >> 2;
     const int f = g * 32 + lane;  // output feature within the half
     const bool leader = (warp == 2 && lane == 0);
+    if (ntiles > 0) {
+      // S half into TMEM: this thread's row f (feature f0 + 128 r + f),
+      // features [128 half, 128 half + 128) as 64 columns of two bf16
+      const uint4* src = reinterpret_cast<const uint4*>(
+          args.S + static_cast<int64_t>(f0 + 128 * r + f) * 256 + 128 * half);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = __ldg(src + 8 * c + u);
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
+        }
+        tmem_st_32x32b_x32(tmem_base + 384 + 64 * half + 32 * c + (static_cast<uint32_t>(g * 32) << 16), w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sfull);
+    }
     for (int i = 0; i < ntiles; ++i) {
       const int m0 = (slot + i * args.nslots) * 64;
       const int acc = i & 1;
