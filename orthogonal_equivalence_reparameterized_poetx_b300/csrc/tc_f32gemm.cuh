@@ -1,6 +1,7 @@
 // Batched fp32-grade GEMM on the tensor cores (tcgen05), for the small dense
 // per-block products of the bf16 layer path: the Cayley backward
-// 2 M^T G M^T and the panel updates of the blocked Gauss-Jordan builder.
+// 2 M^T G M^T (b >= 256), the batched Neumann chain rule (b >= 256) and the
+// Neumann builder products of small blocks.
 //
 //   C[z] = alpha * A[z] B[z]^T + beta * C[z],   z = 0 .. batch-1
 //

@@ -32,7 +32,7 @@ def px():
     ("fp32", 128, 96, 32, 32, "cayley"),
     ("fp32", 200, 136, 64, 48, "cayley"),      # ragged blocks on both sides
     ("bf16", 384, 256, 64, 64, "cayley"),
-    ("bf16", 768, 512, 512, 256, "cayley"),    # blocked builder, ragged R block
+    ("bf16", 768, 512, 512, 256, "cayley"),    # cluster builders, ragged R block
     ("bf16", 256, 256, 128, 128, "neumann"),
 ])
 def test_merge_matches_oracle_and_preserves_the_map(px, dtype, m, n, bR, bP, mode):

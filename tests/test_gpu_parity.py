@@ -72,7 +72,7 @@ def test_fp32_neumann_b256_ragged(px):
 
 
 def test_fp32_cluster_builder_b256(px):
-    # 256-wide blocks: one cluster of eight CTAs per block
+    # 256-wide blocks: one cluster of two 1024-thread CTAs per block
     _case(px, 512, 384, 256, 128, 64, "fp32", gstd=0.02)
 
 
