@@ -770,10 +770,13 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
         ready = build_all(1000 + s)
         for e in ready:
             stream.wait_event(e)
+        # every linear has its own device buffers, so the asynchronous host
+        # step may stream later linears' inputs while earlier ones compute;
+        # the step ends with one synchronisation
         for st in layers:
-            px.poetx_linear_step_host(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
-                                      st["dY"], st["Y"], st["h"], st["u"], st["dX"], st["dgR"],
-                                      st["dgP"], ghR[id(st)], ghP[id(st)], workspace, stream)
+            px.poetx_linear_step_host_async(st["desc"], st["params"], st["W0p"], Xh, dYh, T, st["X"],
+                                            st["dY"], st["Y"], st["h"], st["u"], st["dX"], st["dgR"],
+                                            st["dgP"], ghR[id(st)], ghP[id(st)], workspace, stream)
         if wl.merge_each_step:
             for li in range(len(layers)):
                 e = torch.cuda.Event()

@@ -230,6 +230,26 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
                                     float* dGenP_dev, float* dGenR_host, float* dGenP_host,
                                     void* workspace, void* stream);
 
+/* Asynchronous form of poetx_linear_step_host: the same copies, forward,
+ * backward and gradient copies, enqueued without synchronising.  Both host
+ * to device copies run on a copy stream of the library (X first) and are NOT
+ * ordered after earlier work on `stream`, so that a sequence of calls keeps
+ * the host link busy with later layers' inputs while earlier layers compute.
+ * The caller guarantees that X_dev and dY_dev are not in use by earlier,
+ * unfinished work (give each call in flight its own device buffers, or
+ * synchronise first).  The forward waits for X and the backward for dY on
+ * `stream`; the gradient copies follow on `stream`.  The host gradients are
+ * valid, and the host input buffers may be reused, once `stream` has been
+ * synchronised.  Errors: as poetx_linear_step_host (on an error the call
+ * waits for its own copies to finish before returning). */
+poetx_status poetx_linear_step_host_async(const poetx_layer_desc* desc, const void* params,
+                                          const void* W0p, const void* X_host,
+                                          const void* dY_host, int64_t T, void* X_dev,
+                                          void* dY_dev, void* Y_dev, void* saved_h_dev,
+                                          void* saved_u_dev, void* dX_dev, float* dGenR_dev,
+                                          float* dGenP_dev, float* dGenR_host,
+                                          float* dGenP_host, void* workspace, void* stream);
+
 /* One AdamW step on a packed generator array (the step after the backward).
  * The pages train the generators with an optimizer they do not name; the
  * reading is AdamW with decoupled weight decay (Loshchilov & Hutter, ICLR

@@ -26,7 +26,8 @@ __all__ = [
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
-    "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
+    "poetx_linear_step_host", "poetx_linear_step_host_async", "poetx_device_status",
+    "poetx_selftest_bounded_wait",
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count", "KIND_NAMES", "Layer",
     "EXPORTED_SYMBOLS", "poetx_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -43,7 +44,8 @@ EXPORTED_SYMBOLS = [
     "poetx_status_string", "poetx_version", "poetx_perm_generate", "poetx_gen_length",
     "poetx_params_size", "poetx_params_build", "poetx_weight_premerge", "poetx_workspace_size",
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
-    "poetx_linear_step_host", "poetx_device_status", "poetx_selftest_bounded_wait",
+    "poetx_linear_step_host", "poetx_linear_step_host_async", "poetx_device_status",
+    "poetx_selftest_bounded_wait",
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "poetx_linear_fwd_noalloc", "poetx_set_pipeline", "poetx_pipeline_active",
@@ -109,6 +111,7 @@ def _load():
         "poetx_merge_workspace_size": (SZ, [D]),
         "poetx_merge": (I32, [D, P, P, U64, U64, P, P]),
         "poetx_linear_step_host": (I32, [D, P, P, P, P, I64, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "poetx_linear_step_host_async": (I32, [D, P, P, P, P, I64, P, P, P, P, P, P, P, P, P, P, P, P]),
         "poetx_device_status": (I32, [I32]),
         "poetx_generator_adamw": (I32, [P, P, P, P, I64, I64, ctypes.c_float, ctypes.c_float,
                                         ctypes.c_float, ctypes.c_float, ctypes.c_float, P]),
@@ -249,6 +252,16 @@ def poetx_linear_step_host(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev,
         _ptr(dY_dev), _ptr(Y_dev), _ptr(saved_h_dev), _ptr(saved_u_dev), _ptr(dX_dev), _ptr(dGenR_dev),
         _ptr(dGenP_dev), _ptr(dGenR_host), _ptr(dGenP_host), _ptr(workspace), _stream(stream)),
         "poetx_linear_step_host")
+
+
+def poetx_linear_step_host_async(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev, Y_dev,
+                                 saved_h_dev, saved_u_dev, dX_dev, dGenR_dev, dGenP_dev, dGenR_host,
+                                 dGenP_host, workspace, stream=None):
+    _check(LIB.poetx_linear_step_host_async(
+        ctypes.byref(desc), _ptr(params), _ptr(W0p), _ptr(X_host), _ptr(dY_host), T, _ptr(X_dev),
+        _ptr(dY_dev), _ptr(Y_dev), _ptr(saved_h_dev), _ptr(saved_u_dev), _ptr(dX_dev), _ptr(dGenR_dev),
+        _ptr(dGenP_dev), _ptr(dGenR_host), _ptr(dGenP_host), _ptr(workspace), _stream(stream)),
+        "poetx_linear_step_host_async")
 
 
 def poetx_generator_adamw(gen, grad, m1, m2, length, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,

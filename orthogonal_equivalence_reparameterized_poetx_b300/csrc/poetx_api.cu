@@ -2201,39 +2201,44 @@ cudaStream_t step_copy_stream() {
   return streams[dev];
 }
 
-}  // namespace
-
-extern "C" {
-
-poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params, const void* W0p,
-                                    const void* X_host, const void* dY_host, int64_t T, void* X_dev,
-                                    void* dY_dev, void* Y_dev, void* saved_h_dev, void* saved_u_dev,
-                                    void* dX_dev, float* dGenR_dev, float* dGenP_dev,
-                                    float* dGenR_host, float* dGenP_host, void* workspace,
-                                    void* stream) {
+// One forward + backward step from host buffers (see poetx_linear_step_host
+// and poetx_linear_step_host_async in poetx.h).
+poetx_status step_host_impl(const poetx_layer_desc* desc, const void* params, const void* W0p,
+                            const void* X_host, const void* dY_host, int64_t T, void* X_dev,
+                            void* dY_dev, void* Y_dev, void* saved_h_dev, void* saved_u_dev,
+                            void* dX_dev, float* dGenR_dev, float* dGenP_dev, float* dGenR_host,
+                            float* dGenP_host, void* workspace, void* stream, bool async) {
   POETX_TRY(check_desc(desc));
   if (T < 0 || !X_host || !dY_host || !X_dev || !dY_dev || !dGenR_host || !dGenP_host)
     return POETX_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t e = desc->dtype == POETX_DTYPE_BF16 ? 2 : 4;
-  POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, static_cast<size_t>(T) * desc->n * e,
-                             cudaMemcpyHostToDevice, st));
-  // dY is copied on a second stream once X has arrived, so that it crosses
-  // the host link while the forward runs (the two copies would only share
-  // the link if they overlapped each other); the backward waits for it.
-  // The wait on an event of `st` also orders the copy after all earlier
-  // work on `st`, which may still read dY_dev.
+  const size_t xb = static_cast<size_t>(T) * desc->n * e, yb = static_cast<size_t>(T) * desc->m * e;
   cudaStream_t cs = step_copy_stream();
   Ev x_done, dy_done;
-  if (cs) {
+  if (async && cs) {
+    // both copies on the copy stream, X first, not ordered after earlier
+    // work on `stream` (the caller guarantees the device buffers are free):
+    // consecutive calls keep the host link busy while earlier layers compute
+    POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, cs));
+    POETX_TRY(x_done.record(cs));
+    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, yb, cudaMemcpyHostToDevice, cs));
+    POETX_TRY(dy_done.record(cs));
+    POETX_TRY(x_done.wait_on(st));
+  } else if (cs) {
+    // dY is copied on a second stream once X has arrived, so that it crosses
+    // the host link while the forward runs (the two copies would only share
+    // the link if they overlapped each other); the backward waits for it.
+    // The wait on an event of `st` also orders the copy after all earlier
+    // work on `st`, which may still read dY_dev.
+    POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, st));
     POETX_TRY(x_done.record(st));
     POETX_TRY(x_done.wait_on(cs));
-    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
-                               cudaMemcpyHostToDevice, cs));
+    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, yb, cudaMemcpyHostToDevice, cs));
     POETX_TRY(dy_done.record(cs));
   } else {
-    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, static_cast<size_t>(T) * desc->m * e,
-                               cudaMemcpyHostToDevice, st));
+    POETX_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, st));
+    POETX_CUDA(cudaMemcpyAsync(dY_dev, dY_host, yb, cudaMemcpyHostToDevice, st));
   }
   auto run = [&]() -> poetx_status {
     POETX_TRY(poetx_linear_fwd(desc, params, W0p, X_dev, T, Y_dev, saved_h_dev, saved_u_dev,
@@ -2244,7 +2249,7 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
   };
   const poetx_status rs = run();
   if (rs != POETX_OK) {
-    // the dY copy may still be reading the caller's host buffer
+    // the copies may still be reading the caller's host buffers
     if (cs) (void)cudaStreamSynchronize(cs);
     return rs;
   }
@@ -2253,8 +2258,34 @@ poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* pa
     POETX_CUDA(cudaMemcpyAsync(dGenR_host, dGenR_dev, lr * 4, cudaMemcpyDeviceToHost, st));
   if (lp > 0)
     POETX_CUDA(cudaMemcpyAsync(dGenP_host, dGenP_dev, lp * 4, cudaMemcpyDeviceToHost, st));
-  POETX_CUDA(cudaStreamSynchronize(st));
+  if (!async) POETX_CUDA(cudaStreamSynchronize(st));
   return POETX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params, const void* W0p,
+                                    const void* X_host, const void* dY_host, int64_t T, void* X_dev,
+                                    void* dY_dev, void* Y_dev, void* saved_h_dev, void* saved_u_dev,
+                                    void* dX_dev, float* dGenR_dev, float* dGenP_dev,
+                                    float* dGenR_host, float* dGenP_host, void* workspace,
+                                    void* stream) {
+  return step_host_impl(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev, Y_dev, saved_h_dev,
+                        saved_u_dev, dX_dev, dGenR_dev, dGenP_dev, dGenR_host, dGenP_host, workspace,
+                        stream, false);
+}
+
+poetx_status poetx_linear_step_host_async(const poetx_layer_desc* desc, const void* params,
+                                          const void* W0p, const void* X_host, const void* dY_host,
+                                          int64_t T, void* X_dev, void* dY_dev, void* Y_dev,
+                                          void* saved_h_dev, void* saved_u_dev, void* dX_dev,
+                                          float* dGenR_dev, float* dGenP_dev, float* dGenR_host,
+                                          float* dGenP_host, void* workspace, void* stream) {
+  return step_host_impl(desc, params, W0p, X_host, dY_host, T, X_dev, dY_dev, Y_dev, saved_h_dev,
+                        saved_u_dev, dX_dev, dGenR_dev, dGenP_dev, dGenR_host, dGenP_host, workspace,
+                        stream, true);
 }
 
 poetx_status poetx_generator_adamw(float* gen, const float* grad, float* m1, float* m2, int64_t len,

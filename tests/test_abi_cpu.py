@@ -130,6 +130,9 @@ def test_argument_errors_return_before_launch():
                                         256, 256, gh_r, gh_p, 256, None) == px.POETX_ERR_INVALID_ARG
     assert L.poetx_linear_step_host(D, 256, 256, 256, 256, -1, 256, 256, 256, None, None, None,
                                     256, 256, 256, 256, 256, None) == px.POETX_ERR_INVALID_ARG
+    assert L.poetx_linear_step_host_async(D, 256, 256, None, 256, 4, 256, 256, 256, None, None,
+                                          None, 256, 256, 256, 256, 256,
+                                          None) == px.POETX_ERR_INVALID_ARG
     # invalid descriptor
     bad = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32")
     bad.mode = 7

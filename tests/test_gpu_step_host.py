@@ -122,3 +122,30 @@ def test_step_host_zero_tokens(px):
                               B["dgP"], gR, gP, layer.workspace)
     assert px.poetx_device_status(reset=True) == px.POETX_OK
     assert float(gR.abs().max()) == 0.0 and float(gP.abs().max()) == 0.0
+
+
+def test_async_steps_in_flight_equal_synchronous_steps(px):
+    """Two layers' asynchronous host steps enqueued back to back, each with
+    its own device buffers, then one synchronisation: the same results, bit
+    for bit, as the synchronous calls."""
+    cases = [(640, 512, 64, 400, 15), (512, 1376, 128, 300, 16)]
+    setups = []
+    for m, n, b, T, index in cases:
+        inp, desc, layer = _layer(px, m, n, b, T, "bf16", index=index)
+        setups.append((inp, layer, T, _device_bufs(layer, T, True), _device_bufs(layer, T, True)))
+    want = [_step_host(px, layer, _host(inp.X, True), _host(inp.dY, True), T, Bs)
+            for inp, layer, T, Bs, _ in setups]
+    hosts = []
+    for inp, layer, T, _, Ba in setups:
+        Xh, dYh = _host(inp.X, True), _host(inp.dY, True)
+        gR = torch.empty(layer.len_R, dtype=torch.float32, pin_memory=True)
+        gP = torch.empty(layer.len_P, dtype=torch.float32, pin_memory=True)
+        px.poetx_linear_step_host_async(layer.desc, layer.params, layer.W0p, Xh, dYh, T, Ba["X"],
+                                        Ba["dY"], Ba["Y"], Ba["h"], Ba["u"], Ba["dX"], Ba["dgR"],
+                                        Ba["dgP"], gR, gP, layer.workspace)
+        hosts.append((Xh, dYh, gR, gP))
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+    for (inp, layer, T, _, Ba), (_, _, gR, gP), w in zip(setups, hosts, want):
+        assert torch.equal(Ba["Y"].cpu(), w["Y"]) and torch.equal(Ba["dX"].cpu(), w["dX"])
+        assert torch.equal(gR, w["dgR"]) and torch.equal(gP, w["dgP"])
