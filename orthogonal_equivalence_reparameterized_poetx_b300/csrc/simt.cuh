@@ -546,10 +546,14 @@ __device__ __forceinline__ float sel4(const float (&v)[4], int q) {
 //   A_ij -= (A_iK D^-1) A_Kj     (i, j outside K)
 //   A_Kj  = D^-1 A_Kj,  A_iK = -A_iK D^-1,  A_KK = D^-1.
 // D's symmetric part stays >= I (Schur complements of I - Q), so its
-// unpivoted inverse is well conditioned.  Each round: every thread inverts
-// D in registers, 128 threads form c_i = A_iK D^-1, and each element takes a
-// rank-4 update (one 16-byte shared load, four FMAs); two barriers per four
-// pivots.  `sm` holds 2560 floats.
+// unpivoted inverse is well conditioned.  Each round: the P threads of row
+// group ty = 0 invert D in registers and publish, for their row / column
+// tx, c_tx = A_txK D^-1 and the new pivot-row entries D^-1 A_K,tx (and one
+// of them D^-1 itself); then every element takes a rank-4 update (one
+// 16-byte shared load, four FMAs).  Two barriers per four pivots.  `sm`
+// holds kGj4SmemFloats floats.
+constexpr int kGj4SmemFloats = 2560 + 512 + 32;
+
 template <int PT>
 __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], const GjShape<PT>& sh,
                                                     int tx, int ty, float* sm) {
@@ -557,6 +561,8 @@ __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], cons
   float* rowK0 = sm;          // [2][4][128]: panel rows A_Kj
   float* colK0 = sm + 1024;   // [2][128][4]: panel columns A_iK
   float* cK = sm + 2048;      // [128][4]: c_i = A_iK D^-1
+  float* nrK = sm + 2560;     // [4][128]: new pivot rows D^-1 A_K*
+  float* dK = sm + 3072;      // [4][4]: D^-1
 #pragma unroll
   for (int r = 0; r < kGjMaxRows; ++r) {
     const int i = ty + R * r;
@@ -569,25 +575,26 @@ __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], cons
   for (int k0 = 0, buf = 0; k0 < P; k0 += 4, buf ^= 1) {
     const float* rk = rowK0 + buf * 512;
     const float* ck = colK0 + buf * 512;
-    float D[4][4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) D[p][q] = rk[p * 128 + k0 + q];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {  // in-place unpivoted Gauss-Jordan on the 4 x 4 block
-      const float pv = 1.0f / D[p][p];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) D[p][q] = (q == p) ? pv : D[p][q] * pv;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i == p) continue;
-        const float f = D[i][p];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) D[i][q] = (q == p) ? -f * pv : fmaf(-f, D[p][q], D[i][q]);
-      }
-    }
+    const float rj[4] = {rk[tx], rk[128 + tx], rk[256 + tx], rk[384 + tx]};
     if (ty == 0) {
+      float D[4][4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) D[p][q] = rk[p * 128 + k0 + q];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {  // in-place unpivoted Gauss-Jordan on the 4 x 4 block
+        const float pv = 1.0f / D[p][p];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) D[p][q] = (q == p) ? pv : D[p][q] * pv;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i == p) continue;
+          const float f = D[i][p];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) D[i][q] = (q == p) ? -f * pv : fmaf(-f, D[p][q], D[i][q]);
+        }
+      }
       const float4 ai = *reinterpret_cast<const float4*>(ck + tx * 4);
       float4 c;
       c.x = ai.x * D[0][0] + ai.y * D[1][0] + ai.z * D[2][0] + ai.w * D[3][0];
@@ -595,17 +602,19 @@ __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], cons
       c.z = ai.x * D[0][2] + ai.y * D[1][2] + ai.z * D[2][2] + ai.w * D[3][2];
       c.w = ai.x * D[0][3] + ai.y * D[1][3] + ai.z * D[2][3] + ai.w * D[3][3];
       *reinterpret_cast<float4*>(cK + tx * 4) = c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        nrK[q * 128 + tx] = D[q][0] * rj[0] + D[q][1] * rj[1] + D[q][2] * rj[2] + D[q][3] * rj[3];
+      if (tx == 0) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dK[p * 4 + q] = D[p][q];
+      }
     }
-    const float rj[4] = {rk[tx], rk[128 + tx], rk[256 + tx], rk[384 + tx]};
     const int qj = tx - k0;
     const bool colK = (qj >= 0 && qj < 4);
-    float nr[4], dcol[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      nr[q] = D[q][0] * rj[0] + D[q][1] * rj[1] + D[q][2] * rj[2] + D[q][3] * rj[3];
-      dcol[q] = sel4(D[q], qj & 3);
-    }
-    __syncthreads();  // cK ready
+    __syncthreads();  // cK, nrK and dK ready
     const int k1 = k0 + 4;
     float* rkn = rowK0 + (buf ^ 1) * 512;
     float* ckn = colK0 + (buf ^ 1) * 512;
@@ -618,7 +627,7 @@ __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], cons
         const int qi = i - k0;
         float v;
         if (qi >= 0 && qi < 4) {
-          v = colK ? sel4(dcol, qi) : sel4(nr, qi);
+          v = colK ? dK[qi * 4 + qj] : nrK[qi * 128 + tx];
         } else if (colK) {
           v = -cK[i * 4 + qj];
         } else {
@@ -631,7 +640,7 @@ __device__ __forceinline__ void gj_register_invert4(float (&a)[kGjMaxRows], cons
         if (colK1) ckn[i * 4 + qj1] = v;
       }
     }
-    __syncthreads();  // next panel published; cK free
+    __syncthreads();  // next panel published; cK, nrK and dK free
   }
 }
 
@@ -667,7 +676,7 @@ __global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide fir
   __nv_bfloat16* __restrict__ Bsb = cs.Bsb;
   __nv_bfloat16* __restrict__ BsbT = cs.BsbT;
   __shared__ float rowbuf[256], colbuf[256];
-  __shared__ __align__(16) float gj4_sm[2560];
+  __shared__ __align__(16) float gj4_sm[kGj4SmemFloats];
   extern __shared__ float bsm[];  // P x (P + 1) staging of B for the transposed writes
   const GjShape<PT> sh(s.b);
   const int P = sh.P, R = sh.R, NR = sh.NR;
@@ -728,7 +737,7 @@ __global__ void __launch_bounds__(1024) cayley_block_kernel(const CayleySide fir
 // in + z*in_bs with leading dimension in_ld, written to out likewise.
 __global__ void __launch_bounds__(1024) gj_invert128_kernel(const float* in, int64_t in_bs, int in_ld,
                                                             float* out, int64_t out_bs, int out_ld) {
-  __shared__ __align__(16) float gj4_sm[2560];
+  __shared__ __align__(16) float gj4_sm[kGj4SmemFloats];
   const GjShape<128> sh(128);
   const int tx = threadIdx.x % 128, ty = threadIdx.x / 128;
   const float* src = in + blockIdx.x * in_bs;
