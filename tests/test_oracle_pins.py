@@ -239,7 +239,8 @@ def _fd_grad(spec, W0, X, dY, gR, gP, which, h=1e-6):
 
 @pytest.mark.parametrize("spec", [
     _spec(8, 8, 4, 4), _spec(7, 9, 4, 4), _spec(8, 8, 4, 4, mode="neumann"),
-    _spec(6, 10, 3, 5, mode="neumann", k=2)])
+    _spec(6, 10, 3, 5, mode="neumann", k=2), _spec(6, 6, 3, 3, mode="neumann", k=1),
+    _spec(6, 6, 3, 3, mode="neumann", k=6)])
 def test_generator_grad_matches_finite_differences(spec):
     W0, X, dY, gR, gP = _rand_layer(spec, 3, gstd=0.2)
     dX, dgR, dgP, _ = O.backward(spec, W0, X, dY, gR, gP)
