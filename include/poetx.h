@@ -221,7 +221,13 @@ poetx_status poetx_merge(const poetx_layer_desc* desc, const void* params, void*
  * poetx_linear_bwd (into dX_dev, dGenR_dev, dGenP_dev, overwriting), and
  * copies the generator gradients back into dGenR_host / dGenP_host.  Host
  * buffers should be pinned for asynchronous copies.  Synchronises `stream`
- * before returning.  saved_h_dev and saved_u_dev may be NULL (recompute). */
+ * before returning.  saved_h_dev and saved_u_dev may be NULL (recompute).
+ * dY is copied on a second stream of the library once X has arrived, so that
+ * it overlaps the forward; both copies stay ordered after earlier work on
+ * `stream`.  Errors (returned before any copy): INVALID_ARG for T < 0 or a
+ * NULL host buffer, device input buffer or host gradient; UNSUPPORTED for
+ * T > 2^31 - 256; then the errors of poetx_linear_fwd / poetx_linear_bwd,
+ * after which the call waits for its own copies before returning. */
 poetx_status poetx_linear_step_host(const poetx_layer_desc* desc, const void* params,
                                     const void* W0p, const void* X_host,
                                     const void* dY_host, int64_t T, void* X_dev,

@@ -2211,6 +2211,9 @@ poetx_status step_host_impl(const poetx_layer_desc* desc, const void* params, co
   POETX_TRY(check_desc(desc));
   if (T < 0 || !X_host || !dY_host || !X_dev || !dY_dev || !dGenR_host || !dGenP_host)
     return POETX_ERR_INVALID_ARG;
+  // the forward and backward take at most 2^31 - 256 tokens: refuse before
+  // any copy is enqueued
+  if (T > (int64_t(1) << 31) - 256) return POETX_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t e = desc->dtype == POETX_DTYPE_BF16 ? 2 : 4;
   const size_t xb = static_cast<size_t>(T) * desc->n * e, yb = static_cast<size_t>(T) * desc->m * e;

@@ -133,6 +133,9 @@ def test_argument_errors_return_before_launch():
     assert L.poetx_linear_step_host_async(D, 256, 256, None, 256, 4, 256, 256, 256, None, None,
                                           None, 256, 256, 256, 256, 256,
                                           None) == px.POETX_ERR_INVALID_ARG
+    # token counts the kernels cannot index are refused before any copy
+    assert L.poetx_linear_step_host(D, 256, 256, 256, 256, 1 << 31, 256, 256, 256, None, None, None,
+                                    256, 256, 256, 256, 256, None) == px.POETX_ERR_UNSUPPORTED
     # invalid descriptor
     bad = px.make_desc(64, 64, 8, 8, 1, 2, dtype="fp32")
     bad.mode = 7
