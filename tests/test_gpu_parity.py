@@ -216,3 +216,38 @@ def test_bounded_wait_gives_up_and_reports_timeout(px):
     assert px.poetx_device_status(reset=False) == px.POETX_OK
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum()) == 8.0
+
+
+# ------------------------------------------------------------------ degenerate cases
+
+@pytest.mark.parametrize("m,n,b,mode,dtype", [
+    (1376, 1032, 64, "cayley", "bf16"), (768, 640, 256, "neumann", "bf16"),
+    (512, 384, 512 // 4, "cayley", "fp32"),
+])
+def test_zero_generators_reduce_to_the_plain_linear(px, m, n, b, mode, dtype):
+    """With zero generators every block is the identity (Cayley and Neumann
+    alike), so under any permutations the layer is Y = X W0^T and dX = dY W0,
+    and the generator gradients are the skew part of the token reductions.
+    Checked against torch's own matmul, independently of the oracle: this
+    pins the gathers and scatters as exact inverses of each other."""
+    T = 333
+    inp = make_inputs(m, n, b, b, T, dtype, index=21)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype=dtype, mode=mode)
+    layer = px.Layer(desc, T)
+    layer.build(torch.zeros_like(inp.genR).cuda(), torch.zeros_like(inp.genP).cuda())
+    layer.premerge(inp.W0.cuda())
+    X, dY = inp.X.cuda(), inp.dY.cuda()
+    Y = torch.empty(T, m, dtype=layer.dtype, device="cuda")
+    dX = torch.empty(T, n, dtype=layer.dtype, device="cuda")
+    dgR = torch.empty(layer.len_R, device="cuda")
+    dgP = torch.empty(layer.len_P, device="cuda")
+    layer.forward(X, Y)
+    layer.backward(X, dY, dX, dgR, dgP)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status(reset=True) == px.POETX_OK
+    W0 = inp.W0.double()
+    Y_ref = inp.X.double() @ W0.T
+    dX_ref = inp.dY.double() @ W0
+    tol = TOL[dtype]
+    assert rel_fro(Y.double().cpu().numpy(), Y_ref.numpy()) <= tol
+    assert rel_fro(dX.double().cpu().numpy(), dX_ref.numpy()) <= tol
