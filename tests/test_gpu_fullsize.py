@@ -32,6 +32,10 @@ CASES = [
     ("d2048_block", 0, 256),        # q 2048 -> 2048, b = 256
     ("d4096_ffn", 0, 512),          # up 4096 -> 11008, b = 512 (ragged 256 block), recompute
     ("d4096_ffn", 1, 32),           # down 11008 -> 4096, b = 32, recompute
+    ("d2048_block", 6, 128),        # down 5632 -> 2048: 44 super-blocks on the P side
+    ("d4096_ffn", 0, 256),          # up 4096 -> 11008, b = 256: the 11008 side too wide for
+                                    # the fused 256-wide reduction (separate transform + GradRed)
+    ("d4096_ffn", 1, 128),          # down 11008 -> 4096, b = 128: 86 super-blocks fused
 ]
 
 
