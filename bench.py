@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import tempfile
 import os
 import statistics
 import subprocess
@@ -68,6 +69,8 @@ def parse():
                          "(CHUNKS 1 disables it); default: the library's setting")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small profiling cases only)")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--builds-only", action="store_true",
                     help="time only the block builds (poetx_blocks_build) of each linear, "
                          "in isolation, and print one JSON line")
@@ -204,14 +207,21 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_path=None):
+        """log_path: keep the raw samples there; default a temporary file,
+        removed once the samples are summarised."""
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.keep = log_path is not None
+        if log_path is None:
+            fd, log_path = tempfile.mkstemp(prefix="poetx_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = log_path
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if os.path.dirname(self.path):
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
@@ -244,6 +254,11 @@ class ClockSampler:
                 for nm, v in zip(names, parts[4:8]):
                     if v.lower().startswith("active"):
                         reasons.add(nm)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
@@ -541,7 +556,7 @@ def main():
     px.poetx_profile_enable(not use_graph)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
-    clocks = ClockSampler(gpu_idx)
+    clocks = ClockSampler(gpu_idx, args.clock_log)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
