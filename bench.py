@@ -413,6 +413,10 @@ def main():
         inp = synth.layer_inputs(lin, li, T, wl.dtype, lr, lp)
         st = dict(lin=lin, desc=desc, lr=lr, lp=lp)
         st["params"] = torch.empty(px.poetx_params_size(desc), dtype=torch.uint8, device=dev)
+        if wl.merge_each_step:
+            # the next step's blocks are built into a second buffer while the
+            # merge still reads the current one
+            st["params_next"] = torch.empty_like(st["params"])
         if args.weight == "int8":   # int8 codes and row scales, poetx_weight_size bytes
             st["W0p"] = torch.empty(px.poetx_weight_size(desc), dtype=torch.uint8, device=dev)
         else:
@@ -447,6 +451,7 @@ def main():
     # while the main stream runs the other layers' forward and backward.
     # Each merge has its own scratch so concurrent merges do not share it.
     side = [torch.cuda.Stream(dev, priority=lo) for _ in layers]
+    side_build = [torch.cuda.Stream(dev, priority=lo) for _ in layers]
     merge_ws = ([torch.empty(px.poetx_merge_workspace_size(st["desc"]), dtype=torch.uint8,
                              device=dev) for st in layers] if wl.merge_each_step else None)
     bwd_done = [None] * len(layers)    # event after layer l's backward in the previous step
@@ -459,8 +464,9 @@ def main():
         st["desc"].seed_R, st["desc"].seed_P = nR, nP
 
     def build_all(tag=None):
-        """Issue every layer's (merge +) build on its side stream; returns per-layer
-        events the main stream waits on before that layer's forward."""
+        """Issue every layer's merge and build on its side streams; returns
+        per-layer events the main stream waits on before that layer's
+        forward."""
         start = torch.cuda.Event()
         start.record(stream)
         ready = []
@@ -470,15 +476,32 @@ def main():
             # without merges the build only follows the step's start
             dep = bwd_done[li] if (wl.merge_each_step and bwd_done[li] is not None) else start
             ss.wait_event(dep)
-            if wl.merge_each_step and bwd_done[li] is not None:
-                merge_one(li, st, ss, tag if tag is not None else step_counter[0])
-            if wl.merge_each_step:   # new seeds after the merge: permutations and blocks
-                px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
-            else:                    # same seeds: the blocks only (device work only)
+            if not wl.merge_each_step:   # same seeds: the blocks only (device work only)
                 px.poetx_blocks_build(st["desc"], st["genR"], st["genP"], st["params"], ss)
+                e = torch.cuda.Event()
+                e.record(ss)
+                ready.append([e])
+                continue
+            evs = []
+            if bwd_done[li] is not None:
+                # the merge reads this step's blocks and rewrites W0'; it sets
+                # the new seeds on the host before the next build is issued
+                merge_one(li, st, ss, tag if tag is not None else step_counter[0])
+                e = torch.cuda.Event()
+                e.record(ss)
+                evs.append(e)
+            # new seeds: permutations and blocks into the other parameter
+            # buffer, on the layer's second side stream, beside the merge (the
+            # buffer was last read by the step before the previous one, which
+            # `dep` follows)
+            sb = side_build[li]
+            sb.wait_event(dep)
+            px.poetx_params_build(st["desc"], st["genR"], st["genP"], st["params_next"], sb)
             e = torch.cuda.Event()
-            e.record(ss)
-            ready.append(e)
+            e.record(sb)
+            evs.append(e)
+            st["params"], st["params_next"] = st["params_next"], st["params"]
+            ready.append(evs)
         return ready
 
     def drain_merges(tag):
@@ -502,7 +525,8 @@ def main():
         s = step_counter[0]
         ready = build_all(s)
         for li, st in enumerate(layers):
-            stream.wait_event(ready[li])
+            for e in ready[li]:
+                stream.wait_event(e)
             px.poetx_linear_fwd(st["desc"], st["params"], st["W0p"], st["X"], T, st["Y"], st["h"],
                                 st["u"], workspace, stream)
         for li in reversed(range(len(layers))):
@@ -783,8 +807,9 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
     def step():
         s = cnt[0]
         ready = build_all(1000 + s)
-        for e in ready:
-            stream.wait_event(e)
+        for evs in ready:
+            for e in evs:
+                stream.wait_event(e)
         # every linear has its own device buffers, so the asynchronous host
         # step may stream later linears' inputs while earlier ones compute;
         # the step ends with one synchronisation
