@@ -291,9 +291,9 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
  *
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc or grow a memory pool at the point of use (for
- * example code that runs while a CUDA graph is being captured, inference
- * runtimes that own every byte of device memory in a fixed arena, or hosts
- * whose allocator belongs to another framework).  It computes exactly what
+ * example inference runtimes that own every byte of device memory in a fixed
+ * arena, plugins whose host forbids device allocation inside its execution
+ * callbacks, or hosts whose allocator belongs to another framework).  It computes exactly what
  * poetx_linear_fwd computes, with the same arguments except `workspace`:
  * its scratch is a fixed, file-scope device array of
  * POETX_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that

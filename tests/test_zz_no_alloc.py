@@ -1,9 +1,9 @@
 """The allocation-free forward entry point (needs a B300).
 
 poetx_linear_fwd_noalloc serves callers that cannot allocate device memory
-where they call the layer: code running under CUDA graph capture, runtimes
-that hand out every byte from a fixed arena, or hosts whose allocator belongs
-to someone else.  Instead of a caller-provided workspace it uses a fixed
+where they call the layer: runtimes that hand out every byte from a fixed
+arena, plugins whose host forbids device allocation in its callbacks, or
+hosts whose allocator belongs to someone else.  Instead of a caller-provided workspace it uses a fixed
 device array inside the library.  These tests call it through the C ABI and
 compare it with the ordinary forward (caller-provided workspace) on the same
 inputs, twice in a row so that the second call runs on scratch the first one
