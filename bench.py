@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the plain-bf16-linear comparison and the per-linear breakdown")
-    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample tokens per linear")
+    ap.add_argument("--cpu-tokens", type=int, default=1536, help="oracle sample tokens per linear")
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="oracle tokens per linear per step of the reference arm")
     ap.add_argument("--pipeline", default=None,
