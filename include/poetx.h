@@ -35,9 +35,21 @@
  * poetx_params_size() bytes, 256-byte aligned.
  *
  * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
- * default stream.  Every call is asynchronous on that stream unless stated;
- * no call synchronises the host except poetx_device_status and the *_host
- * entry point.
+ * default stream.  Every call is asynchronous on that stream unless stated.
+ * The host waits only in poetx_device_status, poetx_linear_step_host, and
+ * the two calls that copy host-generated permutations (poetx_params_build,
+ * poetx_merge).  Those stage the indices in a process-wide ring of 32 pinned
+ * HOST slots: a call waits for the copy issued 32 such calls earlier if it
+ * is still pending, and the first call for a wider layer than any before
+ * replaces the ring (after its pending copies finish).
+ *
+ * Devices and threads.  A process uses the library on one device: the
+ * device current at the first call fixes the SM count that sizes grids and
+ * workspaces, and each kernel's shared-memory limit is raised once, on that
+ * device.  Calls for another device in the same process are not supported
+ * (their launches may fail with POETX_ERR_CUDA).  Entry points may be called
+ * from several host threads; calls that share a workspace, params buffer or
+ * output must be ordered by the caller (same stream, or events).
  *
  * Errors.  Argument errors return a status before any launch and leave all
  * outputs untouched.  A failed launch returns POETX_ERR_CUDA.  Kernels that

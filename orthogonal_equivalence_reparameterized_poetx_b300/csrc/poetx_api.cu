@@ -229,14 +229,16 @@ struct WorkLayout {
   size_t total;
 };
 
+// SM count of the device current at the first call (148 when no device can be
+// queried, e.g. for the size functions on a host without a GPU).
 int device_sm_count() {
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0;
+  static const int nsm = [] {
+    int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      nsm = 148;
-  }
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 148;
+    return n;
+  }();
   return nsm;
 }
 
