@@ -239,30 +239,41 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 8:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    smax.append(float(parts[1]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[4:8]):
-                    if v.lower().startswith("active"):
-                        reasons.add(nm)
+            summary = summarise_clock_samples(f)
         if not self.keep:
             try:
                 os.remove(self.path)
             except OSError:
                 pass
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return summary
+
+
+def summarise_clock_samples(lines):
+    """Median SM clock, maximum clock, sample count and the throttle reasons
+    seen active, from `nvidia-smi --query-gpu=<ClockSampler.FIELDS>
+    --format=csv,noheader,nounits` lines; None without a usable sample.
+    Lines that are not complete samples (a partial last line, [N/A] clocks)
+    are skipped."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            clk, clk_max = float(parts[0]), float(parts[1])
+        except ValueError:
+            continue
+        sm.append(clk)
+        smax.append(clk_max)
+        for nm, v in zip(names, parts[4:8]):
+            if v.lower().startswith("active"):
+                reasons.add(nm)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "samples": len(sm), "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- the fp64 oracle as baseline
