@@ -64,9 +64,6 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=1536, help="oracle sample tokens per linear")
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="oracle tokens per linear per step of the reference arm")
-    ap.add_argument("--pipeline", default=None,
-                    help="CHUNKS,FWD_GEMM_SMS,BWD_GEMM_SMS for the library's pipelined schedule "
-                         "(CHUNKS 1 disables it); default: the library's setting")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small profiling cases only)")
     ap.add_argument("--clock-log", default=None,
@@ -329,9 +326,8 @@ def run_reference(args, wl, b, rank):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(wl, b, args, pipeline=None):
+def workload_config(wl, b, args):
     return {
-        "pipeline": pipeline,
         "workload": wl.key, "description": wl.description,
         "linears": [f"{l.name}:{l.n}->{l.m}" for l in wl.linears],
         "tokens": wl.tokens, "b": b, "mode": args.mode, "weight": args.weight,
@@ -397,9 +393,6 @@ def main():
     if args.builds_only:
         run_builds_only(args, wl, b, px, torch, dev)
         return
-    if args.pipeline:
-        ch, fs, bs = (int(x) for x in args.pipeline.split(","))
-        px.poetx_set_pipeline(ch, fs, bs, 0)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -410,7 +403,6 @@ def main():
     lo, hi = torch.cuda.Stream.priority_range()
     stream = torch.cuda.Stream(dev, priority=hi)
     torch.cuda.set_stream(stream)
-    pipe_info = {"active": px.poetx_pipeline_active(), "setting": args.pipeline or "library default"}
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     T = wl.tokens
 
@@ -675,8 +667,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic: seeded N(0,1) activations, N(0,0.02^2) W0, "
                                    "N(0,0.01^2) packed generators",
-        "config": dict(workload_config(wl, b, args, pipeline=pipe_info),
-                       cuda_graph=graph is not None),
+        "config": dict(workload_config(wl, b, args), cuda_graph=graph is not None),
         "tflops": tflops, "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
         "tflops_frac_of_bf16_burst": tflops / peaks["bf16"],
         "step_tflop": flops / 1e12, "roofline": roof, "kernels": kinds,

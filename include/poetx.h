@@ -30,7 +30,10 @@
  * Memory.  Every pointer argument is DEVICE memory owned by the caller
  * unless its comment says HOST.  The library allocates no device memory on
  * any path; per-call scratch comes from the caller's `workspace`, sized by
- * the matching *_workspace_size function, 256-byte aligned.  Layer state
+ * the matching *_workspace_size function, 256-byte aligned.  The one
+ * exception is a fixed module array of POETX_NOALLOC_SCRATCH_BYTES that
+ * every device loading the library holds from module load until exit, the
+ * scratch of poetx_linear_fwd_noalloc (and of nothing else).  Layer state
  * (block matrices, permutations) lives in the caller's `params` buffer of
  * poetx_params_size() bytes, 256-byte aligned.
  *
@@ -315,10 +318,14 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
  *   - Sizes whose poetx_workspace_size(desc, T) exceeds
  *     POETX_NOALLOC_SCRATCH_BYTES are rejected with POETX_ERR_UNSUPPORTED
  *     before any launch (use poetx_linear_fwd with your own workspace).
- *   - It calls no cudaMalloc, cudaFree or other allocating routine.  The
- *     first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call outside any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine (with
+ *     the profiling counters off, as they are by default: when on, they
+ *     create timing events).  The first call on each device looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device
+ *     current) and caches it for the life of the process; make that first
+ *     call outside any stream capture, and do not reset the device
+ *     (cudaDeviceReset) after it, since the cached address would then name
+ *     released module memory.
  *   - Every call on a device shares the same scratch and leaves its contents
  *     behind; the forward writes every scratch byte it reads, so nothing
  *     needs to start at zero.  Calls whose executions overlap on the GPU
@@ -329,24 +336,6 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
 poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, const void* params,
                                       const void* W0p, const void* X, int64_t T, void* Y,
                                       void* saved_h, void* saved_u, void* stream);
-
-/* Pipelined schedule of the bf16 forward and backward.  With T >=
- * min_tokens the library splits the tokens into `chunks` (2..4) and runs the
- * GEMM of one chunk on a partition of `*_gemm_sms` SMs while the gathers,
- * block transforms and token reductions of neighbouring chunks run on the
- * remaining SMs (two CUDA green contexts with their own streams, ordered
- * with events against the caller's stream).  The results are those of the
- * sequential schedule: the same kernels on disjoint token ranges.
- * chunks <= 1 disables the pipeline (the default); 0 for an SM count or
- * min_tokens keeps its current value.  Applies to calls made after it, on
- * every device. */
-void poetx_set_pipeline(int32_t chunks, int32_t fwd_gemm_sms, int32_t bwd_gemm_sms,
-                        int64_t min_tokens);
-
-/* 1 if the pipelined schedule is enabled and the current device can be
- * partitioned (green contexts available), else 0.  May create the green
- * contexts on first use. */
-int32_t poetx_pipeline_active(void);
 
 /* Kernel classes reported by the profiling counters below. */
 enum {
@@ -360,7 +349,9 @@ enum {
   POETX_KIND_MERGE = 7,       /* merge and weight pre-merge                        */
   POETX_KIND_SIMT = 8,        /* fp32 CUDA-core path of the layer                  */
   POETX_KIND_DEQUANT = 9,     /* int8 weight dequantization (POET-XQ)              */
-  POETX_NUM_KINDS = 10
+  POETX_KIND_XCHG = 10,       /* permutation fused with the block transform (and,  */
+                              /* in the backward, the per-block token reduction)   */
+  POETX_NUM_KINDS = 11
 };
 
 /* Profiling.  While enabled, each group of launches of one kernel class is

@@ -31,7 +31,6 @@ __all__ = [
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count", "KIND_NAMES", "Layer",
     "EXPORTED_SYMBOLS", "poetx_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "poetx_set_pipeline", "poetx_pipeline_active",
 ]
 
 POETX_OK, POETX_ERR_INVALID_ARG, POETX_ERR_UNSUPPORTED = 0, 1, 2
@@ -48,7 +47,7 @@ EXPORTED_SYMBOLS = [
     "poetx_selftest_bounded_wait",
     "poetx_set_wait_timeout_ns", "poetx_profile_enable", "poetx_profile_reset",
     "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
-    "poetx_linear_fwd_noalloc", "poetx_set_pipeline", "poetx_pipeline_active",
+    "poetx_linear_fwd_noalloc",
     "poetx_weight_size", "poetx_blocks_build", "poetx_generator_adamw",
 ]
 
@@ -56,7 +55,7 @@ EXPORTED_SYMBOLS = [
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KIND_NAMES = ["gemm_fwd", "gemm_dgrad", "blockdiag", "gradred", "gather", "build", "genbwd",
-              "merge", "simt", "dequant"]
+              "merge", "simt", "dequant", "xchg"]
 
 
 class PoetxError(RuntimeError):
@@ -124,8 +123,6 @@ def _load():
         "poetx_profile_kind_name": (ctypes.c_char_p, [I32]),
         "poetx_launch_count": (I64, []),
         "poetx_linear_fwd_noalloc": (I32, [D, P, P, P, I64, P, P, P, P]),
-        "poetx_set_pipeline": (V, [I32, I32, I32, I64]),
-        "poetx_pipeline_active": (I32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -304,15 +301,6 @@ def poetx_profile_kind_name(kind: int) -> str:
 
 def poetx_launch_count() -> int:
     return LIB.poetx_launch_count()
-
-
-def poetx_set_pipeline(chunks: int, fwd_gemm_sms: int = 0, bwd_gemm_sms: int = 0,
-                       min_tokens: int = 0):
-    LIB.poetx_set_pipeline(chunks, fwd_gemm_sms, bwd_gemm_sms, min_tokens)
-
-
-def poetx_pipeline_active() -> bool:
-    return bool(LIB.poetx_pipeline_active())
 
 
 class Layer:

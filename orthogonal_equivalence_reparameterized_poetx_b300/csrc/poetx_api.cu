@@ -33,6 +33,7 @@
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
 #include "tc_neumann_bwd.cuh"
+#include "tc_xchg.cuh"
 
 using namespace poetx;
 
@@ -225,6 +226,8 @@ Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
 struct WorkLayout {
   size_t off_n1, off_n2, off_m1, off_m2, off_m3;
   size_t off_partR, off_partP, off_GR, off_GP, off_t1, off_t2, off_nsc, off_wdq;
+  size_t off_ring, off_flags;
+  int64_t flag_words;  // produced[nbands], consumed[nbands], abort word
   int splitsR, splitsP;
   size_t total;
 };
@@ -242,30 +245,59 @@ int device_sm_count() {
   return nsm;
 }
 
-// SMs that launches from this host thread may use: the whole device, or the
-// size of the green-context partition the current pipeline stage runs in.
-thread_local int t_cta_budget = 0;
-int launch_sms() { return t_cta_budget > 0 ? t_cta_budget : device_sm_count(); }
+// SMs the library's persistent launches size their grids for.
+int launch_sms() { return device_sm_count(); }
 
-struct CtaBudget {
-  int prev;
-  explicit CtaBudget(int n) : prev(t_cta_budget) { t_cta_budget = n; }
-  ~CtaBudget() { t_cta_budget = prev; }
+// Plan of one exchange pass (tc_xchg.cuh) over a side of d features with
+// 128-wide super-blocks: Q CTAs per slot own all super-blocks (at most two
+// each with the token reduction, whose accumulators take 128 TMEM columns
+// per super-block; at most six without), S slots fill the SMs, and the ring
+// holds E = S x rounds bands of 64 tokens (two to three rounds, capped so
+// that it stays well inside L2).  ok == false: the pass runs as separate
+// permutation and transform kernels.
+struct XchgPlan {
+  bool ok = false;
+  int Q = 0, S = 0, E = 0, nbands = 0, aw = 0, bpw = 0;
+  size_t ring_bytes = 0;
 };
 
-// Most token chunks a pipelined forward or backward uses.
-constexpr int kMaxChunks = 4;
+XchgPlan xchg_plan(const SideGeom& g, int sb, int nsb, int64_t T, bool red, int sms) {
+  XchgPlan p;
+  const int d = g.d;
+  if (sb != 128 || T <= 0 || d % 8 != 0 || d > XchgCfg::MAX_D) return p;
+  const int gmax = XchgCfg::max_g(red);
+  p.Q = (nsb + gmax - 1) / gmax;
+  if (p.Q < 1 || p.Q > sms) return p;
+  p.nbands = static_cast<int>((T + 63) / 64);
+  p.S = std::min(sms / p.Q, p.nbands);
+  const size_t band = static_cast<size_t>(64) * d * 2;
+  const int64_t per_slot = (p.nbands + p.S - 1) / p.S;
+  const int64_t cap = std::max<int64_t>(2, static_cast<int64_t>((40u << 20) / (band * p.S)));
+  const int rounds = static_cast<int>(std::min<int64_t>(per_slot, std::min<int64_t>(8, cap)));
+  p.E = p.S * rounds;
+  const int rows = XchgCfg::BAND_BYTES / (2 * d);  // row buffers of the band side
+  p.aw = std::min(XchgCfg::BAND_WARPS, rows);
+  p.bpw = std::max(1, std::min(XchgCfg::MAX_BPW, rows / p.aw));
+  p.ring_bytes = static_cast<size_t>(p.E) * band;
+  p.ok = true;
+  return p;
+}
 
-// Upper bound on reduction partial slots for T tokens split into at most
-// kMaxChunks chunks, whatever SM budget each chunk runs under.
+XchgPlan xchg_plan(const SideLayout& S, int64_t T, bool red) {
+  return xchg_plan(S.g, S.sb, S.nsb, T, red, launch_sms());
+}
+
+// Upper bound on the reduction partial slots written for T tokens: GradRed
+// token splits, the fused transform + reduction's token slots, or the
+// exchange pass's slots.
 int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
   const int tps = S.sb / 128;
   const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
   const int64_t smax = std::max<int64_t>(
       1, std::min<int64_t>((4 * device_sm_count() + per_split - 1) / per_split, (T + 63) / 64));
-  // the fused transform + reduction writes one slot per CTA of a super-block
   const int64_t fused = std::max<int64_t>(1, device_sm_count() / S.nsb);
-  return std::max(smax * kMaxChunks, fused);
+  const XchgPlan xp = xchg_plan(S.g, S.sb, S.nsb, T, true, device_sm_count());
+  return std::max({smax, fused, static_cast<int64_t>(xp.ok ? xp.S : 1)});
 }
 
 // Pre-merged weight buffer: m x n of the dtype, or (POET-XQ) m x n int8
@@ -291,7 +323,6 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   W.off_m3 = off; off = align_up(off + tm);
   W.splitsR = W.splitsP = 0;
   if (d.dtype == POETX_DTYPE_BF16) {
-    (void)nsm;
     W.splitsR = static_cast<int>(partial_slots_bound(P.R, T));
     W.splitsP = static_cast<int>(partial_slots_bound(P.P, T));
     W.off_partR = off;
@@ -314,6 +345,20 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * std::max(d.neumann_k + 3, 10));
   W.off_wdq = off;  // dequantized int8 weight (bf16 m x n)
   if (weight_int8(d)) off = align_up(off + static_cast<size_t>(d.m) * d.n * 2);
+  // exchange passes: the ring of the largest pass, then the per-band counters
+  W.off_ring = off;
+  if (d.dtype == POETX_DTYPE_BF16) {
+    size_t ring = 0;
+    for (const SideLayout* S : {&P.R, &P.P})
+      for (bool red : {false, true}) {
+        const XchgPlan xp = xchg_plan(S->g, S->sb, S->nsb, T, red, nsm);
+        if (xp.ok) ring = std::max(ring, xp.ring_bytes);
+      }
+    off = align_up(off + ring);
+  }
+  W.off_flags = off;
+  W.flag_words = d.dtype == POETX_DTYPE_BF16 ? 2 * ((T + 63) / 64) + 64 : 0;
+  off = align_up(off + static_cast<size_t>(W.flag_words) * 4);
   W.total = off;
   return W;
 }
@@ -720,6 +765,50 @@ poetx_status tc_bdgr256(cudaStream_t st, const SideLayout& S, const void* in, co
   POETX_LAUNCHED();
   *slots += a.nslots;
   return POETX_OK;
+}
+
+// ------------------------------------------------------------------ exchange passes
+// One launch of tc_xchg_kernel: cooperative (all CTAs resident at once, one
+// per SM), after zeroing the per-band counters and the abort word.
+template <bool GATHER, bool RED>
+poetx_status launch_xchg(cudaStream_t st, const CUtensorMap& tin, const CUtensorMap& tc,
+                         const CUtensorMap& tout, XchgArgs a, uint32_t* flags) {
+  auto kern = tc_xchg_kernel<GATHER, RED>;
+  constexpr int smem = XchgCfg::smem<RED>();
+  static cudaError_t attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  a.produced = flags;
+  a.consumed = flags + a.nbands;
+  a.abort_word = flags + 2 * a.nbands;
+  a.timeout_ns = g_timeout_ns;
+  POETX_CUDA(cudaMemsetAsync(flags, 0, (2 * static_cast<size_t>(a.nbands) + 1) * 4, st));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(a.Q * a.S));
+  cfg.blockDim = dim3(XchgCfg::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  POETX_CUDA(cudaLaunchKernelEx(&cfg, kern, tin, tc, tout, a));
+  POETX_LAUNCHED();
+  return POETX_OK;
+}
+
+XchgArgs xchg_args(const SideLayout& S, const XchgPlan& xp, int64_t T) {
+  XchgArgs a{};
+  a.T = static_cast<int>(T);
+  a.d = S.g.d;
+  a.nsb = S.nsb;
+  a.Q = xp.Q;
+  a.S = xp.S;
+  a.nbands = xp.nbands;
+  a.E = xp.E;
+  a.aw = xp.aw;
+  a.bpw = xp.bpw;
+  return a;
 }
 
 // One tensor-core merge pass (tc_merge.cuh): with A = Ahi (+ Alo), M x N
@@ -1226,6 +1315,77 @@ struct Ctx {
   mutable int slotsR = 0, slotsP = 0;
 };
 
+// An event recorded on one stream for later waits on others.
+struct Ev {
+  cudaEvent_t e = nullptr;
+  ~Ev() {
+    if (e) cudaEventDestroy(e);
+  }
+  poetx_status record(cudaStream_t st) {
+    if (!e) POETX_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    POETX_CUDA(cudaEventRecord(e, st));
+    return POETX_OK;
+  }
+  poetx_status wait_on(cudaStream_t st) const {
+    POETX_CUDA(cudaStreamWaitEvent(st, e, 0));
+    return POETX_OK;
+  }
+};
+
+// Permutation into the block basis fused with the block transform:
+//   u = in[:, pi] (rows of the ring, or of `u_out` when the caller keeps u),
+//   out = u S^T per super-block (S = Bmat), and with a reduction operand Cm
+//   the partial slots of u^T Cm (one per slot of the pass).
+poetx_status xchg_gather(const Ctx& c, const SideLayout& S, const XchgPlan& xp, const int32_t* pi,
+                         const void* in, void* u_out, const void* Bmat, void* out, const void* Cm,
+                         float* partial, int64_t T) {
+  ProfScope prof(POETX_KIND_XCHG, c.st);
+  const int d = S.g.d;
+  const bool red = Cm != nullptr;
+  void* ring = u_out ? u_out : c.ws + c.W.off_ring;
+  CUtensorMap tin, tcm, tout;
+  POETX_TRY(tmap_bf16(&tin, ring, u_out ? static_cast<uint64_t>(T) : static_cast<uint64_t>(xp.E) * 64, d, d, 64));
+  POETX_TRY(tmap_bf16(&tcm, red ? Cm : ring, red ? static_cast<uint64_t>(T) : 64, d, d, 64));
+  POETX_TRY(tmap_bf16(&tout, out, T, d, d, 64));
+  XchgArgs a = xchg_args(S, xp, T);
+  a.ring_full = u_out ? 1 : 0;
+  a.idx = pi;
+  a.band_src = reinterpret_cast<const uint16_t*>(in);
+  a.band_dst = reinterpret_cast<uint16_t*>(ring);
+  a.Bmat = reinterpret_cast<const __nv_bfloat16*>(Bmat);
+  a.partial = partial;
+  uint32_t* flags = c.w<uint32_t>(c.W.off_flags);
+  if (red) return launch_xchg<true, true>(c.st, tin, tcm, tout, a, flags);
+  return launch_xchg<true, false>(c.st, tin, tcm, tout, a, flags);
+}
+
+// Block transform fused with the permutation out of the block basis:
+//   z = in S^T per super-block (S = Bmat) into the ring, out[:, i] = z[:, pinv[i]],
+//   and with a reduction operand Cm the partial slots of in^T Cm.
+poetx_status xchg_scatter(const Ctx& c, const SideLayout& S, const XchgPlan& xp, const int32_t* pinv,
+                          const void* in, const void* Bmat, void* out, const void* Cm, float* partial,
+                          int64_t T) {
+  ProfScope prof(POETX_KIND_XCHG, c.st);
+  const int d = S.g.d;
+  const bool red = Cm != nullptr;
+  void* ring = c.ws + c.W.off_ring;
+  CUtensorMap tin, tcm, tout;
+  POETX_TRY(tmap_bf16(&tin, in, T, d, d, 64));
+  POETX_TRY(tmap_bf16(&tcm, red ? Cm : in, T, d, d, 64));
+  POETX_TRY(tmap_bf16(&tout, ring, static_cast<uint64_t>(xp.E) * 64, d, d, 64));
+  XchgArgs a = xchg_args(S, xp, T);
+  a.ring_full = 0;
+  a.idx = pinv;
+  a.band_src = reinterpret_cast<const uint16_t*>(ring);
+  a.band_dst = reinterpret_cast<uint16_t*>(out);
+  a.ring = reinterpret_cast<uint16_t*>(ring);
+  a.Bmat = reinterpret_cast<const __nv_bfloat16*>(Bmat);
+  a.partial = partial;
+  uint32_t* flags = c.w<uint32_t>(c.W.off_flags);
+  if (red) return launch_xchg<false, true>(c.st, tin, tcm, tout, a, flags);
+  return launch_xchg<false, false>(c.st, tin, tcm, tout, a, flags);
+}
+
 poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs,
                       float* us) {
   const int m = c.d.m, n = c.d.n;
@@ -1245,229 +1405,35 @@ poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T,
   return POETX_OK;
 }
 
-// ------------------------------------------------------------------ green-context pipeline
-// The bf16 forward and backward can run as a software pipeline over token
-// chunks on two disjoint SM partitions (CUDA green contexts): the GEMM stages
-// of chunk k on one partition while the memory-bound stages (gathers, block
-// transforms, token reductions) of neighbouring chunks run on the other.
-// Stages are ordered by events; the first and last memory stages use the
-// whole device on the caller's stream.  Every stage is the same kernel as in
-// the sequential schedule, on disjoint token ranges of the same buffers.
-
-typedef CUresult (*PFN_cuDeviceGet_t)(CUdevice*, int);
-typedef CUresult (*PFN_cuDeviceGetDevResource_t)(CUdevice, CUdevResource*, CUdevResourceType);
-typedef CUresult (*PFN_cuDevSmResourceSplitByCount_t)(CUdevResource*, unsigned int*,
-                                                     const CUdevResource*, CUdevResource*,
-                                                     unsigned int, unsigned int);
-typedef CUresult (*PFN_cuDevResourceGenerateDesc_t)(CUdevResourceDesc*, CUdevResource*, unsigned int);
-typedef CUresult (*PFN_cuGreenCtxCreate_t)(CUgreenCtx*, CUdevResourceDesc, CUdevice, unsigned int);
-typedef CUresult (*PFN_cuGreenCtxStreamCreate_t)(CUstream*, CUgreenCtx, unsigned int, int);
-
-// Off by default: measured on B300 at d = 2048 and d = 4096 the partitioned
-// schedule is slower than the sequential one (the gathers and block
-// transforms are bound by per-SM throughput, so they slow down in proportion
-// to the SMs they lose, as do the GEMMs).
-struct PipeCfg {
-  int chunks = 1;          // token chunks (1 disables the pipeline)
-  int fwd_gemm_sms = 112;  // SMs of the GEMM partition in the forward
-  int bwd_gemm_sms = 72;   // and in the backward
-  int64_t min_tokens = 8192;
-};
-PipeCfg g_pipe;
-std::mutex g_pipe_mu;
-
-struct GreenPart {
-  bool ok = false;
-  int ng = 0, nm = 0;
-  cudaStream_t sg = nullptr, sm = nullptr;
-};
-
-template <typename F>
-bool driver_fn(const char* name, F* out) {
-  void* p = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion(name, &p, CUDART_VERSION, cudaEnableDefault, &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || !p)
-    return false;
-  *out = reinterpret_cast<F>(p);
-  return true;
-}
-
-// Two green contexts on the current device: `ng` SMs for GEMMs and the rest
-// for memory-bound stages, each with a non-blocking stream.  Cached per
-// (device, ng); ok == false if the driver cannot partition.
-GreenPart green_partition(int ng) {
-  static std::mutex mu;
-  static std::vector<std::pair<std::pair<int, int>, GreenPart>> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GreenPart{};
-  std::lock_guard<std::mutex> lock(mu);
-  for (auto& e : cache)
-    if (e.first.first == dev && e.first.second == ng) return e.second;
-  GreenPart gp;
-  PFN_cuDeviceGet_t dget;
-  PFN_cuDeviceGetDevResource_t getres;
-  PFN_cuDevSmResourceSplitByCount_t split;
-  PFN_cuDevResourceGenerateDesc_t gendesc;
-  PFN_cuGreenCtxCreate_t gcreate;
-  PFN_cuGreenCtxStreamCreate_t gstream;
-  if (driver_fn("cuDeviceGet", &dget) && driver_fn("cuDeviceGetDevResource", &getres) &&
-      driver_fn("cuDevSmResourceSplitByCount", &split) &&
-      driver_fn("cuDevResourceGenerateDesc", &gendesc) && driver_fn("cuGreenCtxCreate", &gcreate) &&
-      driver_fn("cuGreenCtxStreamCreate", &gstream)) {
-    CUdevice cd;
-    CUdevResource all, grp, rest;
-    unsigned int n = 1;
-    CUdevResourceDesc dg, dm;
-    CUgreenCtx cg, cm;
-    CUstream sg, sm;
-    if (dget(&cd, dev) == CUDA_SUCCESS && getres(cd, &all, CU_DEV_RESOURCE_TYPE_SM) == CUDA_SUCCESS &&
-        split(&grp, &n, &all, &rest, 0, static_cast<unsigned>(ng)) == CUDA_SUCCESS && n == 1 &&
-        rest.sm.smCount > 0 && gendesc(&dg, &grp, 1) == CUDA_SUCCESS &&
-        gendesc(&dm, &rest, 1) == CUDA_SUCCESS &&
-        gcreate(&cg, dg, cd, CU_GREEN_CTX_DEFAULT_STREAM) == CUDA_SUCCESS &&
-        gcreate(&cm, dm, cd, CU_GREEN_CTX_DEFAULT_STREAM) == CUDA_SUCCESS &&
-        gstream(&sg, cg, CU_STREAM_NON_BLOCKING, 0) == CUDA_SUCCESS &&
-        gstream(&sm, cm, CU_STREAM_NON_BLOCKING, 0) == CUDA_SUCCESS) {
-      gp.ok = true;
-      gp.ng = static_cast<int>(grp.sm.smCount);
-      gp.nm = static_cast<int>(rest.sm.smCount);
-      gp.sg = reinterpret_cast<cudaStream_t>(sg);
-      gp.sm = reinterpret_cast<cudaStream_t>(sm);
-    }
-  }
-  (void)cudaGetLastError();
-  cache.push_back({{dev, ng}, gp});
-  return gp;
-}
-
-// An event recorded on one stream for later waits on others.
-struct Ev {
-  cudaEvent_t e = nullptr;
-  ~Ev() {
-    if (e) cudaEventDestroy(e);
-  }
-  poetx_status record(cudaStream_t st) {
-    if (!e) POETX_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
-    POETX_CUDA(cudaEventRecord(e, st));
-    return POETX_OK;
-  }
-  poetx_status wait_on(cudaStream_t st) const {
-    POETX_CUDA(cudaStreamWaitEvent(st, e, 0));
-    return POETX_OK;
-  }
-};
-
-// Token chunks: `count` ranges, multiples of 128 tokens except the last.
-struct Chunks {
-  int count = 1;
-  int64_t t0[kMaxChunks] = {0};
-  int64_t len[kMaxChunks] = {0};
-};
-
-// Schedule of one bf16 pass: the pipeline when green partitions exist and T
-// is large enough, else one chunk on the caller's stream.
-struct Plan {
-  Chunks ch;
-  GreenPart gp;
-  bool piped = false;
-};
-
-Plan make_plan(int64_t T, bool backward) {
-  Plan pl;
-  PipeCfg cfg;
-  {
-    std::lock_guard<std::mutex> lock(g_pipe_mu);
-    cfg = g_pipe;
-  }
-  const int C = std::min(std::max(cfg.chunks, 1), kMaxChunks);
-  if (C > 1 && T >= cfg.min_tokens && T >= C * 128) {
-    pl.gp = green_partition(backward ? cfg.bwd_gemm_sms : cfg.fwd_gemm_sms);
-    if (pl.gp.ok) {
-      pl.piped = true;
-      const int64_t per = ((T + C - 1) / C + 127) / 128 * 128;
-      int k = 0;
-      for (int64_t t = 0; t < T && k < kMaxChunks; t += per, ++k) {
-        pl.ch.t0[k] = t;
-        pl.ch.len[k] = std::min(per, T - t);
-      }
-      pl.ch.count = k;
-    }
-  }
-  if (!pl.piped) {
-    pl.ch.count = 1;
-    pl.ch.t0[0] = 0;
-    pl.ch.len[0] = T;
-  }
-  return pl;
-}
-
-// Forward, bf16:  A(k): X -> u (gather) -> v (P blocks);  G(k): h = v W0'^T;
-// Z(k): h -> z (R blocks) -> Y (scatter), on token chunk k.
-// Pipelined order (GEMM partition g, memory partition m, caller stream c):
-//   c: A(0) | g: G(0) G(1) ... G(C-1) | m: A(1), Z(0), A(2), Z(1), ... Z(C-2) | c: Z(C-1)
+// Forward, bf16 ("POET-X ...", Methodologie §1: Y = R(W0(P x)) evaluated on
+// the input):  X -> u = X[:, pi_P] -> v = u B_P^T (blocks) -> h = v W0'^T ->
+// z = h B_R^T (blocks) -> Y[:, pi_R] = z.  With 128-wide super-blocks each
+// permutation runs fused with its block transform (tc_xchg.cuh): u and z
+// only pass through an L2-resident ring, except that a kept u is written
+// to saved_u.  Other block sizes run separate permutation and transform
+// kernels through the workspace.
 poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X, int64_t T,
                       __nv_bfloat16* Y, __nv_bfloat16* hs, __nv_bfloat16* us) {
   const int m = c.d.m, n = c.d.n;
-  auto* u = us ? us : c.w<__nv_bfloat16>(c.W.off_n1);
   auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
   auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
-  auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
   const SideLayout &R = c.L.R, &P = c.L.P;
   const auto* BsbP = c.p<__nv_bfloat16>(P.off_Bsb);
   const auto* BsbR = c.p<__nv_bfloat16>(R.off_Bsb);
-  const Plan pl = make_plan(T, false);
-  const Chunks& ch = pl.ch;
-  auto A = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, u + t0 * n, c.piP(), len, n));
-    return tc_blockdiag(st, u + t0 * n, BsbP, v + t0 * n, len, n, P.sb, P.nsb);
-  };
-  auto G = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    return tc_dense_nt(st, v + t0 * n, W0p, h + t0 * m, len, m, n);
-  };
-  auto Z = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    POETX_TRY(tc_blockdiag(st, h + t0 * m, BsbR, z + t0 * m, len, m, R.sb, R.nsb));
-    return gather_cols<__nv_bfloat16>(st, z + t0 * m, Y + t0 * m, c.piRinv(), len, m);
-  };
-  if (!pl.piped) {
-    POETX_TRY(A(0, c.st, 0));
-    POETX_TRY(G(0, c.st, 0));
-    return Z(0, c.st, 0);
+  const XchgPlan xP = xchg_plan(P, T, false);
+  if (xP.ok) {
+    POETX_TRY(xchg_gather(c, P, xP, c.piP(), X, us, BsbP, v, nullptr, nullptr, T));
+  } else {
+    auto* u = us ? us : c.w<__nv_bfloat16>(c.W.off_n1);
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
+    POETX_TRY(tc_blockdiag(c.st, u, BsbP, v, T, n, P.sb, P.nsb));
   }
-  const int C = ch.count;
-  const cudaStream_t sc = c.st, sg = pl.gp.sg, sm = pl.gp.sm;
-  const int ng = pl.gp.ng, nm = pl.gp.nm;
-  Ev start, evA[kMaxChunks], evG[kMaxChunks], done_m;
-  POETX_TRY(start.record(sc));
-  POETX_TRY(start.wait_on(sm));
-  POETX_TRY(A(0, sc, 0));
-  POETX_TRY(evA[0].record(sc));
-  POETX_TRY(evA[0].wait_on(sg));
-  POETX_TRY(A(1, sm, nm));
-  POETX_TRY(evA[1].record(sm));
-  POETX_TRY(G(0, sg, ng));
-  POETX_TRY(evG[0].record(sg));
-  for (int k = 1; k < C; ++k) {
-    POETX_TRY(evA[k].wait_on(sg));
-    POETX_TRY(G(k, sg, ng));
-    POETX_TRY(evG[k].record(sg));
-    POETX_TRY(evG[k - 1].wait_on(sm));
-    POETX_TRY(Z(k - 1, sm, nm));
-    if (k + 1 < C) {
-      POETX_TRY(A(k + 1, sm, nm));
-      POETX_TRY(evA[k + 1].record(sm));
-    }
-  }
-  POETX_TRY(done_m.record(sm));
-  POETX_TRY(evG[C - 1].wait_on(sc));
-  POETX_TRY(Z(C - 1, sc, 0));
-  return done_m.wait_on(sc);
+  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
+  const XchgPlan xR = xchg_plan(R, T, false);
+  if (xR.ok) return xchg_scatter(c, R, xR, c.piRinv(), h, BsbR, Y, nullptr, nullptr, T);
+  auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
+  POETX_TRY(tc_blockdiag(c.st, h, BsbR, z, T, m, R.sb, R.nsb));
+  return gather_cols<__nv_bfloat16>(c.st, z, Y, c.piRinv(), T, m);
 }
 
 bool fused_cayley_bwd_ok(const poetx_layer_desc& d, int b) {
@@ -1652,14 +1618,16 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
   return POETX_OK;
 }
 
-// Backward, bf16, on token chunk k:
-//   RA(k) recompute only: X -> u (gather) -> v (P blocks);  RG(k): h = v W0'^T
-//   U(k)  stored h: X -> u (gather)
-//   R1(k) dY -> dz (gather) -> dh (R^T blocks);  GR(k): partials of dz^T h
-//   D(k)  dv = dh W0';  GP(k): partials of dv^T u;  E(k): dv -> du (P^T blocks) -> dX
-// Pipelined order: the GEMMs (RG, D) on the GEMM partition, the rest on the
-// memory partition; chunk 0's first stages and the last chunk's final
-// stages on the caller's stream with the whole device.
+// Backward, bf16 (the chain rule of the forward's steps):
+//   u    = X[:, pi_P] when not kept; in recompute mode also v = u B_P^T and
+//          h = v W0'^T (gradient checkpointing, Methodologie §5)
+//   dz   = dY[:, pi_R];  dh = dz B_R;  partials of G_R = dz^T h
+//   dv   = dh W0'
+//   du   = dv B_P;  partials of G_P = dv^T u;  dX[:, pi_P] = du
+// With 128-wide super-blocks the permutation of dY, the R-side transform and
+// its reduction run as one exchange pass, and so do the P-side transform,
+// its reduction and the permutation into dX; the per-block reductions of the
+// partials follow in bwd_common_tail.
 poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X,
                       const __nv_bfloat16* dY, const __nv_bfloat16* hs, const __nv_bfloat16* us,
                       int64_t T, __nv_bfloat16* dX) {
@@ -1678,52 +1646,34 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   const auto* BsbPT = c.p<__nv_bfloat16>(P.off_BsbT);
   const bool recompute = (hs == nullptr);
   const __nv_bfloat16* h = recompute ? hbuf : hs;
-  auto* dv = v;     // v of a chunk is dead once its h is formed
-  auto* du = ubuf;  // u of a chunk is dead once its dv^T u partials are formed (a saved u is not written)
+  auto* dv = v;     // v is dead once h is formed
+  auto* du = ubuf;  // u is dead once the dv^T u partials are formed (a saved u is not written)
   const int64_t strideR = static_cast<int64_t>(R.nsb) * R.sb * R.sb;
   const int64_t strideP = static_cast<int64_t>(P.nsb) * P.sb * P.sb;
   c.slotsR = c.slotsP = 0;
-  const Plan pl = make_plan(T, true);
-  const Chunks& ch = pl.ch;
-  auto RA = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    if (!us) POETX_TRY(gather_cols<__nv_bfloat16>(st, X + t0 * n, ubuf + t0 * n, c.piP(), len, n));
-    if (!recompute) return POETX_OK;
-    return tc_blockdiag(st, u + t0 * n, BsbP, v + t0 * n, len, n, P.sb, P.nsb);
-  };
-  auto RG = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    return tc_dense_nt(st, v + t0 * n, W0p, hbuf + t0 * m, len, m, n);
-  };
-  auto R1 = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    POETX_TRY(gather_cols<__nv_bfloat16>(st, dY + t0 * m, dz + t0 * m, c.piR(), len, m));
-    return tc_blockdiag(st, dz + t0 * m, BsbRT, dh + t0 * m, len, m, R.sb, R.nsb);
-  };
-  auto GR = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    return tc_gradred(st, R, dz + t0 * m, h + t0 * m, partR + c.slotsR * strideR, len, &c.slotsR);
-  };
-  auto D = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    return tc_dense_nn(st, dh + t0 * m, W0p, dv + t0 * n, len, n, m);
-  };
-  auto GPE = [&](int k, cudaStream_t st, int budget) -> poetx_status {
-    CtaBudget bg(budget);
-    const int64_t t0 = ch.t0[k], len = ch.len[k];
-    POETX_TRY(tc_gradred(st, P, dv + t0 * n, u + t0 * n, partP + c.slotsP * strideP, len, &c.slotsP));
-    if (!dX) return POETX_OK;
-    POETX_TRY(tc_blockdiag(st, dv + t0 * n, BsbPT, du + t0 * n, len, n, P.sb, P.nsb));
-    return gather_cols<__nv_bfloat16>(st, du + t0 * n, dX + t0 * n, c.piPinv(), len, n);
-  };
-  if (!pl.piped) {
-    POETX_TRY(RA(0, c.st, 0));
-    if (recompute) POETX_TRY(RG(0, c.st, 0));
+
+  // u (when not kept), and in recompute mode v and h
+  if (!us && recompute) {
+    const XchgPlan xP = xchg_plan(P, T, false);
+    if (xP.ok) {
+      POETX_TRY(xchg_gather(c, P, xP, c.piP(), X, ubuf, BsbP, v, nullptr, nullptr, T));
+    } else {
+      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
+      POETX_TRY(tc_blockdiag(c.st, ubuf, BsbP, v, T, n, P.sb, P.nsb));
+    }
+  } else if (!us) {
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
+  } else if (recompute) {
+    POETX_TRY(tc_blockdiag(c.st, us, BsbP, v, T, n, P.sb, P.nsb));
+  }
+  if (recompute) POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
+
+  // R side: dz, dh and the dz^T h partials
+  const XchgPlan xR = xchg_plan(R, T, true);
+  if (xR.ok) {
+    POETX_TRY(xchg_gather(c, R, xR, c.piR(), dY, nullptr, BsbRT, dh, h, partR, T));
+    c.slotsR = xR.S;
+  } else {
     POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
     if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
       POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
@@ -1731,54 +1681,31 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
       POETX_TRY(tc_bdgr256(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
     } else {
       POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
-      POETX_TRY(GR(0, c.st, 0));
+      POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, &c.slotsR));
     }
-    POETX_TRY(D(0, c.st, 0));
-    if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
-      POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
-      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
-    } else if (dX && bdgr256_ok(P)) {
-      POETX_TRY(tc_bdgr256(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
-      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
-    } else {
-      POETX_TRY(GPE(0, c.st, 0));
-    }
-  } else {
-    const int C = ch.count;
-    const cudaStream_t sc = c.st, sg = pl.gp.sg, sm = pl.gp.sm;
-    const int ng = pl.gp.ng, nm = pl.gp.nm;
-    Ev start, evRA[kMaxChunks], evRG[kMaxChunks], evR1[kMaxChunks], evD[kMaxChunks], done_m;
-    POETX_TRY(start.record(sc));
-    POETX_TRY(start.wait_on(sm));
-    POETX_TRY(start.wait_on(sg));
-    for (int k = 0; k < C; ++k) {
-      const cudaStream_t mst = (k == 0) ? sc : sm;   // chunk 0's first stages: whole device
-      const int mb = (k == 0) ? 0 : nm;
-      POETX_TRY(RA(k, mst, mb));
-      if (recompute) {
-        POETX_TRY(evRA[k].record(mst));
-        POETX_TRY(evRA[k].wait_on(sg));
-        POETX_TRY(RG(k, sg, ng));
-        POETX_TRY(evRG[k].record(sg));
-      }
-      POETX_TRY(R1(k, mst, mb));
-      POETX_TRY(evR1[k].record(mst));
-      POETX_TRY(evR1[k].wait_on(sg));
-      if (k == 0) POETX_TRY(evR1[0].wait_on(sm));   // later chunks' stages follow chunk 0's
-      POETX_TRY(D(k, sg, ng));
-      POETX_TRY(evD[k].record(sg));
-      if (recompute) POETX_TRY(evRG[k].wait_on(sm));
-      POETX_TRY(GR(k, sm, nm));
-      if (k >= 1) {
-        POETX_TRY(evD[k - 1].wait_on(sm));
-        POETX_TRY(GPE(k - 1, sm, nm));
-      }
-    }
-    POETX_TRY(done_m.record(sm));
-    POETX_TRY(evD[C - 1].wait_on(sc));
-    POETX_TRY(done_m.wait_on(sc));
-    POETX_TRY(GPE(C - 1, sc, 0));
   }
+
+  POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
+
+  // P side: du, the dv^T u partials and dX
+  const XchgPlan xP = xchg_plan(P, T, true);
+  if (dX && xP.ok) {
+    POETX_TRY(xchg_scatter(c, P, xP, c.piPinv(), dv, BsbPT, dX, u, partP, T));
+    c.slotsP = xP.S;
+  } else if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
+    POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+  } else if (dX && bdgr256_ok(P)) {
+    POETX_TRY(tc_bdgr256(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+  } else {
+    POETX_TRY(tc_gradred(c.st, P, dv, u, partP, T, &c.slotsP));
+    if (dX) {
+      POETX_TRY(tc_blockdiag(c.st, dv, BsbPT, du, T, n, P.sb, P.nsb));
+      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+    }
+  }
+
   ProfScope prof(POETX_KIND_GENBWD, c.st);
   // exact Cayley blocks of b <= 128: the generator backward runs fused per block
   // in bwd_common_tail; otherwise reduce the partials into G here.
@@ -2400,7 +2327,7 @@ poetx_status poetx_profile_read(int32_t kind, int64_t* groups, double* total_ms)
 const char* poetx_profile_kind_name(int32_t kind) {
   static const char* names[POETX_NUM_KINDS] = {"gemm_fwd", "gemm_dgrad", "blockdiag", "gradred",
                                                "gather", "build", "genbwd", "merge", "simt",
-                                               "dequant"};
+                                               "dequant", "xchg"};
   return (kind >= 0 && kind < POETX_NUM_KINDS) ? names[kind] : "unknown";
 }
 
@@ -2443,26 +2370,3 @@ extern "C" poetx_status poetx_linear_fwd_noalloc(const poetx_layer_desc* desc, c
   }
   return poetx_linear_fwd(desc, params, W0p, X, T, Y, saved_h, saved_u, scratch, stream);
 }
-
-extern "C" {
-
-void poetx_set_pipeline(int32_t chunks, int32_t fwd_gemm_sms, int32_t bwd_gemm_sms,
-                        int64_t min_tokens) {
-  std::lock_guard<std::mutex> lock(g_pipe_mu);
-  g_pipe.chunks = std::min<int32_t>(std::max<int32_t>(chunks, 1), kMaxChunks);
-  if (fwd_gemm_sms > 0) g_pipe.fwd_gemm_sms = fwd_gemm_sms;
-  if (bwd_gemm_sms > 0) g_pipe.bwd_gemm_sms = bwd_gemm_sms;
-  if (min_tokens > 0) g_pipe.min_tokens = min_tokens;
-}
-
-int32_t poetx_pipeline_active(void) {
-  PipeCfg cfg;
-  {
-    std::lock_guard<std::mutex> lock(g_pipe_mu);
-    cfg = g_pipe;
-  }
-  if (cfg.chunks <= 1) return 0;
-  return (green_partition(cfg.fwd_gemm_sms).ok && green_partition(cfg.bwd_gemm_sms).ok) ? 1 : 0;
-}
-
-}  // extern "C"

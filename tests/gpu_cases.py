@@ -16,6 +16,52 @@ def rel_fro(a, b) -> float:
     return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
 
 
+def worst_row_rel(a, b) -> float:
+    """Largest relative error of a single row, max_t ||a_t - b_t|| / ||b_t||:
+    a wrong tile of tokens or a wrong short row cannot hide in the aggregate."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.size == 0:
+        return 0.0
+    nb = np.linalg.norm(b, axis=1)
+    return float((np.linalg.norm(a - b, axis=1) / np.where(nb > 0, nb, 1.0)).max())
+
+
+def packed_block_slices(d: int, b: int):
+    """Slices of the packed generator vector that belong to each block
+    (blocks of b, then a ragged d mod b; 1 x 1 blocks have no entries)."""
+    out, off = [], 0
+    for s in O.block_sizes(d, b):
+        n = s * (s - 1) // 2
+        if n:
+            out.append(slice(off, off + n))
+        off += n
+    return out
+
+
+def worst_block_rel(a, b, d: int, bs: int) -> float:
+    """Largest relative Frobenius error of one block's packed gradient."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return max((rel_fro(a[sl], b[sl]) for sl in packed_block_slices(d, bs)), default=0.0)
+
+
+def parity_errors(g, o, m, n, bR, bP) -> dict:
+    """Aggregate relative Frobenius errors of Y, dX, dgR, dgP, plus the worst
+    row of Y and dX and the worst block of dgR and dgP."""
+    errs = {k: rel_fro(g[k], o[k]) for k in ("Y", "dX", "dgR", "dgP")
+            if g.get(k) is not None and o[k].size}
+    if g.get("Y") is not None and o["Y"].size:
+        errs["Y_worst_row"] = worst_row_rel(g["Y"], o["Y"])
+    if g.get("dX") is not None and o["dX"].size:
+        errs["dX_worst_row"] = worst_row_rel(g["dX"], o["dX"])
+    if o["dgR"].size:
+        errs["dgR_worst_block"] = worst_block_rel(g["dgR"], o["dgR"], m, bR)
+    if o["dgP"].size:
+        errs["dgP_worst_block"] = worst_block_rel(g["dgP"], o["dgP"], n, bP)
+    return errs
+
+
 def make_inputs(m, n, bR, bP, T, dtype, index=0, t0=0, t1=None, gstd=synth.STD_GEN):
     lin = synth.Linear("case", n, m)
     lr, lp = O.packed_length(m, bR), O.packed_length(n, bP)

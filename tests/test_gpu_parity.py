@@ -3,7 +3,10 @@
 Every case runs forward + backward through the C ABI and through the oracle
 on identical seeded inputs (the oracle consumes the already-rounded values)
 and compares Y, dX and both packed generator gradients by relative Frobenius
-error: <= 1e-5 for fp32, <= 2e-2 for bf16 with fp32 accumulation.  The
+error: <= 1e-5 for fp32, <= 2e-2 for bf16 with fp32 accumulation.  The same
+bound holds for the worst single row of Y and dX and for the worst single
+block of each generator gradient, so a local error cannot hide in the
+aggregate.  The
 pre-merged weight W0' is a pure permutation copy and must match bit for bit,
 which also checks the device permutations against the oracle's.
 
@@ -16,7 +19,7 @@ import pytest
 import torch
 
 import oracle as O
-from tests.gpu_cases import make_inputs, rel_fro, run_gpu, run_oracle
+from tests.gpu_cases import make_inputs, parity_errors, rel_fro, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +48,7 @@ def _case(px, m, n, bR, bP, T, dtype, mode="cayley", k=3, recompute=False, index
         u_o = inp.X.double().numpy()[:, O.permutation(inp.seed_P, n)]
         assert np.array_equal(g["u"], u_o), "saved u must be the permuted input, bit for bit"
     tol = TOL[dtype]
-    errs = {k_: rel_fro(g[k_], o[k_]) for k_ in ("Y", "dX", "dgR", "dgP") if o[k_].size}
+    errs = parity_errors(g, o, m, n, bR, bP)
     for k_, e in errs.items():
         assert e <= tol, f"{k_}: rel Frobenius {e:.3e} > {tol:.0e} ({errs})"
     return errs
@@ -165,6 +168,32 @@ def test_bf16_neumann_b512_ragged(px):
 
 def test_bf16_single_token_and_single_block(px):
     _case(px, 128, 128, 128, 128, 1, "bf16")
+
+
+@pytest.mark.parametrize("recompute", [False, True])
+def test_bf16_exchange_ring_reuse_long_tokens(px, recompute):
+    # 151 bands of 64 tokens (ragged tail of 17): every slot of every exchange
+    # pass cycles through its ring entries several times, in both directions
+    _case(px, 2048, 1024, 128, 128, 64 * 150 + 17, "bf16", recompute=recompute, index=7)
+
+
+@pytest.mark.parametrize("recompute,save_u", [(False, True), (True, False)])
+def test_fused_exchange_passes_replace_the_gathers(px, recompute, save_u):
+    """With 128-wide super-blocks every permutation runs inside an exchange
+    pass with its block transform: no separate gather launches, four
+    exchange passes (five when the backward re-forms u and v)."""
+    m, n, b, T = 1024, 768, 128, 1000
+    inp = make_inputs(m, n, b, b, T, "bf16", index=9)
+    desc = px.make_desc(m, n, b, b, inp.seed_R, inp.seed_P, dtype="bf16")
+    px.poetx_profile_reset()
+    px.poetx_profile_enable(True)
+    try:
+        run_gpu(px, desc, inp, recompute, save_u=save_u)
+    finally:
+        px.poetx_profile_enable(False)
+    kinds = {name: px.poetx_profile_read(k)[0] for k, name in enumerate(px.KIND_NAMES)}
+    assert kinds["gather"] == 0, kinds
+    assert kinds["xchg"] == (5 if recompute else 4), kinds
 
 
 # ------------------------------------------------------------------ other ABI behaviour
