@@ -349,9 +349,7 @@ enum {
   POETX_KIND_MERGE = 7,       /* merge and weight pre-merge                        */
   POETX_KIND_SIMT = 8,        /* fp32 CUDA-core path of the layer                  */
   POETX_KIND_DEQUANT = 9,     /* int8 weight dequantization (POET-XQ)              */
-  POETX_KIND_XCHG = 10,       /* permutation fused with the block transform (and,  */
-                              /* in the backward, the per-block token reduction)   */
-  POETX_NUM_KINDS = 11
+  POETX_NUM_KINDS = 10
 };
 
 /* Profiling.  While enabled, each group of launches of one kernel class is

@@ -55,7 +55,7 @@ EXPORTED_SYMBOLS = [
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KIND_NAMES = ["gemm_fwd", "gemm_dgrad", "blockdiag", "gradred", "gather", "build", "genbwd",
-              "merge", "simt", "dequant", "xchg"]
+              "merge", "simt", "dequant"]
 
 
 class PoetxError(RuntimeError):

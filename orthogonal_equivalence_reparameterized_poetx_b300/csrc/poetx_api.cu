@@ -33,7 +33,6 @@
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
 #include "tc_neumann_bwd.cuh"
-#include "tc_xchg.cuh"
 
 using namespace poetx;
 
@@ -226,8 +225,6 @@ Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
 struct WorkLayout {
   size_t off_n1, off_n2, off_m1, off_m2, off_m3;
   size_t off_partR, off_partP, off_GR, off_GP, off_t1, off_t2, off_nsc, off_wdq;
-  size_t off_ring, off_flags;
-  int64_t flag_words;  // produced[nbands], consumed[nbands], abort word
   int splitsR, splitsP;
   size_t total;
 };
@@ -248,56 +245,15 @@ int device_sm_count() {
 // SMs the library's persistent launches size their grids for.
 int launch_sms() { return device_sm_count(); }
 
-// Plan of one exchange pass (tc_xchg.cuh) over a side of d features with
-// 128-wide super-blocks: Q CTAs per slot own all super-blocks (at most two
-// each with the token reduction, whose accumulators take 128 TMEM columns
-// per super-block; at most six without), S slots fill the SMs, and the ring
-// holds E = S x rounds bands of 64 tokens (two to three rounds, capped so
-// that it stays well inside L2).  ok == false: the pass runs as separate
-// permutation and transform kernels.
-struct XchgPlan {
-  bool ok = false;
-  int Q = 0, S = 0, E = 0, nbands = 0, aw = 0, bpw = 0;
-  size_t ring_bytes = 0;
-};
-
-XchgPlan xchg_plan(const SideGeom& g, int sb, int nsb, int64_t T, bool red, int sms) {
-  XchgPlan p;
-  const int d = g.d;
-  if (sb != 128 || T <= 0 || d % 8 != 0 || d > XchgCfg::MAX_D) return p;
-  const int gmax = XchgCfg::max_g(red);
-  p.Q = (nsb + gmax - 1) / gmax;
-  if (p.Q < 1 || p.Q > sms) return p;
-  p.nbands = static_cast<int>((T + 63) / 64);
-  p.S = std::min(sms / p.Q, p.nbands);
-  const size_t band = static_cast<size_t>(64) * d * 2;
-  const int64_t per_slot = (p.nbands + p.S - 1) / p.S;
-  const int64_t cap = std::max<int64_t>(2, static_cast<int64_t>((40u << 20) / (band * p.S)));
-  const int rounds = static_cast<int>(std::min<int64_t>(per_slot, std::min<int64_t>(8, cap)));
-  p.E = p.S * rounds;
-  const int rows = XchgCfg::BAND_BYTES / (2 * d);  // row buffers of the band side
-  p.aw = std::min(XchgCfg::BAND_WARPS, rows);
-  p.bpw = std::max(1, std::min(XchgCfg::MAX_BPW, rows / p.aw));
-  p.ring_bytes = static_cast<size_t>(p.E) * band;
-  p.ok = true;
-  return p;
-}
-
-XchgPlan xchg_plan(const SideLayout& S, int64_t T, bool red) {
-  return xchg_plan(S.g, S.sb, S.nsb, T, red, launch_sms());
-}
-
 // Upper bound on the reduction partial slots written for T tokens: GradRed
-// token splits, the fused transform + reduction's token slots, or the
-// exchange pass's slots.
+// token splits or the fused transform + reduction's token slots.
 int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
   const int tps = S.sb / 128;
   const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
   const int64_t smax = std::max<int64_t>(
       1, std::min<int64_t>((4 * device_sm_count() + per_split - 1) / per_split, (T + 63) / 64));
   const int64_t fused = std::max<int64_t>(1, device_sm_count() / S.nsb);
-  const XchgPlan xp = xchg_plan(S.g, S.sb, S.nsb, T, true, device_sm_count());
-  return std::max({smax, fused, static_cast<int64_t>(xp.ok ? xp.S : 1)});
+  return std::max(smax, fused);
 }
 
 // Pre-merged weight buffer: m x n of the dtype, or (POET-XQ) m x n int8
@@ -345,20 +301,6 @@ WorkLayout work_layout(const poetx_layer_desc& d, const ParamsLayout& P, int64_t
   if (d.mode == POETX_MODE_NEUMANN) off = align_up(off + gmax * std::max(d.neumann_k + 3, 10));
   W.off_wdq = off;  // dequantized int8 weight (bf16 m x n)
   if (weight_int8(d)) off = align_up(off + static_cast<size_t>(d.m) * d.n * 2);
-  // exchange passes: the ring of the largest pass, then the per-band counters
-  W.off_ring = off;
-  if (d.dtype == POETX_DTYPE_BF16) {
-    size_t ring = 0;
-    for (const SideLayout* S : {&P.R, &P.P})
-      for (bool red : {false, true}) {
-        const XchgPlan xp = xchg_plan(S->g, S->sb, S->nsb, T, red, nsm);
-        if (xp.ok) ring = std::max(ring, xp.ring_bytes);
-      }
-    off = align_up(off + ring);
-  }
-  W.off_flags = off;
-  W.flag_words = d.dtype == POETX_DTYPE_BF16 ? 2 * ((T + 63) / 64) + 64 : 0;
-  off = align_up(off + static_cast<size_t>(W.flag_words) * 4);
   W.total = off;
   return W;
 }
@@ -765,50 +707,6 @@ poetx_status tc_bdgr256(cudaStream_t st, const SideLayout& S, const void* in, co
   POETX_LAUNCHED();
   *slots += a.nslots;
   return POETX_OK;
-}
-
-// ------------------------------------------------------------------ exchange passes
-// One launch of tc_xchg_kernel: cooperative (all CTAs resident at once, one
-// per SM), after zeroing the per-band counters and the abort word.
-template <bool GATHER, bool RED>
-poetx_status launch_xchg(cudaStream_t st, const CUtensorMap& tin, const CUtensorMap& tc,
-                         const CUtensorMap& tout, XchgArgs a, uint32_t* flags) {
-  auto kern = tc_xchg_kernel<GATHER, RED>;
-  constexpr int smem = XchgCfg::smem<RED>();
-  static cudaError_t attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
-  a.produced = flags;
-  a.consumed = flags + a.nbands;
-  a.abort_word = flags + 2 * a.nbands;
-  a.timeout_ns = g_timeout_ns;
-  POETX_CUDA(cudaMemsetAsync(flags, 0, (2 * static_cast<size_t>(a.nbands) + 1) * 4, st));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.Q * a.S));
-  cfg.blockDim = dim3(XchgCfg::THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  POETX_CUDA(cudaLaunchKernelEx(&cfg, kern, tin, tc, tout, a));
-  POETX_LAUNCHED();
-  return POETX_OK;
-}
-
-XchgArgs xchg_args(const SideLayout& S, const XchgPlan& xp, int64_t T) {
-  XchgArgs a{};
-  a.T = static_cast<int>(T);
-  a.d = S.g.d;
-  a.nsb = S.nsb;
-  a.Q = xp.Q;
-  a.S = xp.S;
-  a.nbands = xp.nbands;
-  a.E = xp.E;
-  a.aw = xp.aw;
-  a.bpw = xp.bpw;
-  return a;
 }
 
 // One tensor-core merge pass (tc_merge.cuh): with A = Ahi (+ Alo), M x N
@@ -1332,60 +1230,6 @@ struct Ev {
   }
 };
 
-// Permutation into the block basis fused with the block transform:
-//   u = in[:, pi] (rows of the ring, or of `u_out` when the caller keeps u),
-//   out = u S^T per super-block (S = Bmat), and with a reduction operand Cm
-//   the partial slots of u^T Cm (one per slot of the pass).
-poetx_status xchg_gather(const Ctx& c, const SideLayout& S, const XchgPlan& xp, const int32_t* pi,
-                         const void* in, void* u_out, const void* Bmat, void* out, const void* Cm,
-                         float* partial, int64_t T) {
-  ProfScope prof(POETX_KIND_XCHG, c.st);
-  const int d = S.g.d;
-  const bool red = Cm != nullptr;
-  void* ring = u_out ? u_out : c.ws + c.W.off_ring;
-  CUtensorMap tin, tcm, tout;
-  POETX_TRY(tmap_bf16(&tin, ring, u_out ? static_cast<uint64_t>(T) : static_cast<uint64_t>(xp.E) * 64, d, d, 64));
-  POETX_TRY(tmap_bf16(&tcm, red ? Cm : ring, red ? static_cast<uint64_t>(T) : 64, d, d, 64));
-  POETX_TRY(tmap_bf16(&tout, out, T, d, d, 64));
-  XchgArgs a = xchg_args(S, xp, T);
-  a.ring_full = u_out ? 1 : 0;
-  a.idx = pi;
-  a.band_src = reinterpret_cast<const uint16_t*>(in);
-  a.band_dst = reinterpret_cast<uint16_t*>(ring);
-  a.Bmat = reinterpret_cast<const __nv_bfloat16*>(Bmat);
-  a.partial = partial;
-  uint32_t* flags = c.w<uint32_t>(c.W.off_flags);
-  if (red) return launch_xchg<true, true>(c.st, tin, tcm, tout, a, flags);
-  return launch_xchg<true, false>(c.st, tin, tcm, tout, a, flags);
-}
-
-// Block transform fused with the permutation out of the block basis:
-//   z = in S^T per super-block (S = Bmat) into the ring, out[:, i] = z[:, pinv[i]],
-//   and with a reduction operand Cm the partial slots of in^T Cm.
-poetx_status xchg_scatter(const Ctx& c, const SideLayout& S, const XchgPlan& xp, const int32_t* pinv,
-                          const void* in, const void* Bmat, void* out, const void* Cm, float* partial,
-                          int64_t T) {
-  ProfScope prof(POETX_KIND_XCHG, c.st);
-  const int d = S.g.d;
-  const bool red = Cm != nullptr;
-  void* ring = c.ws + c.W.off_ring;
-  CUtensorMap tin, tcm, tout;
-  POETX_TRY(tmap_bf16(&tin, in, T, d, d, 64));
-  POETX_TRY(tmap_bf16(&tcm, red ? Cm : in, T, d, d, 64));
-  POETX_TRY(tmap_bf16(&tout, ring, static_cast<uint64_t>(xp.E) * 64, d, d, 64));
-  XchgArgs a = xchg_args(S, xp, T);
-  a.ring_full = 0;
-  a.idx = pinv;
-  a.band_src = reinterpret_cast<const uint16_t*>(ring);
-  a.band_dst = reinterpret_cast<uint16_t*>(out);
-  a.ring = reinterpret_cast<uint16_t*>(ring);
-  a.Bmat = reinterpret_cast<const __nv_bfloat16*>(Bmat);
-  a.partial = partial;
-  uint32_t* flags = c.w<uint32_t>(c.W.off_flags);
-  if (red) return launch_xchg<false, true>(c.st, tin, tcm, tout, a, flags);
-  return launch_xchg<false, false>(c.st, tin, tcm, tout, a, flags);
-}
-
 poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T, float* Y, float* hs,
                       float* us) {
   const int m = c.d.m, n = c.d.n;
@@ -1406,33 +1250,20 @@ poetx_status fwd_fp32(const Ctx& c, const float* W0p, const float* X, int64_t T,
 }
 
 // Forward, bf16 ("POET-X ...", Methodologie §1: Y = R(W0(P x)) evaluated on
-// the input):  X -> u = X[:, pi_P] -> v = u B_P^T (blocks) -> h = v W0'^T ->
-// z = h B_R^T (blocks) -> Y[:, pi_R] = z.  With 128-wide super-blocks each
-// permutation runs fused with its block transform (tc_xchg.cuh): u and z
-// only pass through an L2-resident ring, except that a kept u is written
-// to saved_u.  Other block sizes run separate permutation and transform
-// kernels through the workspace.
+// the input):  X -> u = X[:, pi_P] (gather) -> v = u B_P^T (blocks) ->
+// h = v W0'^T -> z = h B_R^T (blocks) -> Y[:, pi_R] = z (scatter).
 poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X, int64_t T,
                       __nv_bfloat16* Y, __nv_bfloat16* hs, __nv_bfloat16* us) {
   const int m = c.d.m, n = c.d.n;
+  auto* u = us ? us : c.w<__nv_bfloat16>(c.W.off_n1);
   auto* v = c.w<__nv_bfloat16>(c.W.off_n2);
   auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
-  const SideLayout &R = c.L.R, &P = c.L.P;
-  const auto* BsbP = c.p<__nv_bfloat16>(P.off_Bsb);
-  const auto* BsbR = c.p<__nv_bfloat16>(R.off_Bsb);
-  const XchgPlan xP = xchg_plan(P, T, false);
-  if (xP.ok) {
-    POETX_TRY(xchg_gather(c, P, xP, c.piP(), X, us, BsbP, v, nullptr, nullptr, T));
-  } else {
-    auto* u = us ? us : c.w<__nv_bfloat16>(c.W.off_n1);
-    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
-    POETX_TRY(tc_blockdiag(c.st, u, BsbP, v, T, n, P.sb, P.nsb));
-  }
-  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
-  const XchgPlan xR = xchg_plan(R, T, false);
-  if (xR.ok) return xchg_scatter(c, R, xR, c.piRinv(), h, BsbR, Y, nullptr, nullptr, T);
   auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
-  POETX_TRY(tc_blockdiag(c.st, h, BsbR, z, T, m, R.sb, R.nsb));
+  const SideLayout &R = c.L.R, &P = c.L.P;
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
+  POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
+  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
+  POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
   return gather_cols<__nv_bfloat16>(c.st, z, Y, c.piRinv(), T, m);
 }
 
@@ -1624,10 +1455,7 @@ poetx_status bwd_fp32(const Ctx& c, const float* W0p, const float* X, const floa
 //   dz   = dY[:, pi_R];  dh = dz B_R;  partials of G_R = dz^T h
 //   dv   = dh W0'
 //   du   = dv B_P;  partials of G_P = dv^T u;  dX[:, pi_P] = du
-// With 128-wide super-blocks the permutation of dY, the R-side transform and
-// its reduction run as one exchange pass, and so do the P-side transform,
-// its reduction and the permutation into dX; the per-block reductions of the
-// partials follow in bwd_common_tail.
+// The per-block reductions of the partials follow in bwd_common_tail.
 poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat16* X,
                       const __nv_bfloat16* dY, const __nv_bfloat16* hs, const __nv_bfloat16* us,
                       int64_t T, __nv_bfloat16* dX) {
@@ -1653,46 +1481,27 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   c.slotsR = c.slotsP = 0;
 
   // u (when not kept), and in recompute mode v and h
-  if (!us && recompute) {
-    const XchgPlan xP = xchg_plan(P, T, false);
-    if (xP.ok) {
-      POETX_TRY(xchg_gather(c, P, xP, c.piP(), X, ubuf, BsbP, v, nullptr, nullptr, T));
-    } else {
-      POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
-      POETX_TRY(tc_blockdiag(c.st, ubuf, BsbP, v, T, n, P.sb, P.nsb));
-    }
-  } else if (!us) {
-    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
-  } else if (recompute) {
-    POETX_TRY(tc_blockdiag(c.st, us, BsbP, v, T, n, P.sb, P.nsb));
+  if (!us) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
+  if (recompute) {
+    POETX_TRY(tc_blockdiag(c.st, u, BsbP, v, T, n, P.sb, P.nsb));
+    POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
   }
-  if (recompute) POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
 
   // R side: dz, dh and the dz^T h partials
-  const XchgPlan xR = xchg_plan(R, T, true);
-  if (xR.ok) {
-    POETX_TRY(xchg_gather(c, R, xR, c.piR(), dY, nullptr, BsbRT, dh, h, partR, T));
-    c.slotsR = xR.S;
+  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
+  if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
+    POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
+  } else if (bdgr256_ok(R)) {
+    POETX_TRY(tc_bdgr256(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
   } else {
-    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
-    if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
-      POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
-    } else if (bdgr256_ok(R)) {
-      POETX_TRY(tc_bdgr256(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
-    } else {
-      POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
-      POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, &c.slotsR));
-    }
+    POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
+    POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, &c.slotsR));
   }
 
   POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
 
   // P side: du, the dv^T u partials and dX
-  const XchgPlan xP = xchg_plan(P, T, true);
-  if (dX && xP.ok) {
-    POETX_TRY(xchg_scatter(c, P, xP, c.piPinv(), dv, BsbPT, dX, u, partP, T));
-    c.slotsP = xP.S;
-  } else if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
+  if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
     POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
     POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
   } else if (dX && bdgr256_ok(P)) {
@@ -2327,7 +2136,7 @@ poetx_status poetx_profile_read(int32_t kind, int64_t* groups, double* total_ms)
 const char* poetx_profile_kind_name(int32_t kind) {
   static const char* names[POETX_NUM_KINDS] = {"gemm_fwd", "gemm_dgrad", "blockdiag", "gradred",
                                                "gather", "build", "genbwd", "merge", "simt",
-                                               "dequant", "xchg"};
+                                               "dequant"};
   return (kind >= 0 && kind < POETX_NUM_KINDS) ? names[kind] : "unknown";
 }
 

@@ -53,8 +53,9 @@ __global__ void __launch_bounds__(320, 1)
   using Cfg = Bdgr256Cfg;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array, so that the
+  // compiler keeps shared-memory instructions for the accesses through it
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   uint8_t* out_stage = stages + STAGES * Cfg::STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT);
@@ -208,7 +209,9 @@ __global__ void __launch_bounds__(320, 1)
       const int m0 = (slot + i * args.nslots) * 64;
       const int acc = i & 1;
       const uint32_t acc_phase = (i >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, tmo, abort_flag)) break;
+      const bool waited = mbar_wait(&tfull[acc], acc_phase, tmo, abort_flag);
+      // leave together: the named barriers below have no deadline
+      if (named_barrier_any(1, 256, !waited)) break;
       tc_fence_after();
       uint32_t v[32];
       tmem_ld_32x32b_x32(tmem_base + 256 + acc * 64 + half * 32 + (static_cast<uint32_t>(g * 32) << 16), v);

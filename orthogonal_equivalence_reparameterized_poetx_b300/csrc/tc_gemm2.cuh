@@ -49,8 +49,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   using Cfg = TcPairCfg;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array, so that the
+  // compiler keeps shared-memory instructions for the accesses through it
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* out_stage = smem + STAGES * Cfg::STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT_BYTES);
   uint64_t* empty = full + STAGES;
@@ -181,7 +182,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       const int n0 = (tile % ntn) * 256;
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, tmo, abort_flag)) break;
+      const bool waited = mbar_wait(&tfull[acc], acc_phase, tmo, abort_flag);
+      // leave together: the named barriers below have no deadline
+      if (named_barrier_any(1, 256, !waited)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(g * 32) << 16);
 #pragma unroll 1

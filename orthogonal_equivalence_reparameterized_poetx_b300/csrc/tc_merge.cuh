@@ -59,8 +59,9 @@ __global__ void __launch_bounds__(320, 1)
   using Cfg = MergeCfg<A_SPLIT>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array, so that the
+  // compiler keeps shared-memory instructions for the accesses through it
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;

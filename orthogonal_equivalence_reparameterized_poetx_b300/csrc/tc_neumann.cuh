@@ -63,8 +63,9 @@ __global__ void __cluster_dims__(NeuCfg<BS>::C, 1, 1) __launch_bounds__(288, 1)
   using Cfg = NeuCfg<BS>;
   constexpr int NT = Cfg::NT, RS = Cfg::RS, C = Cfg::C, NK = Cfg::NK;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned by pointer arithmetic on the shared array, so that the
+  // compiler keeps shared-memory instructions for the accesses through it
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* cvt_full = reinterpret_cast<uint64_t*>(smem + 2 * Cfg::BUF);  // [2]
   uint64_t* mma_done = cvt_full + 2;                                       // [2]
   uint64_t* acc_full = mma_done + 2;
