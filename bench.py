@@ -61,9 +61,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the plain-bf16-linear comparison and the per-linear breakdown")
-    ap.add_argument("--cpu-tokens", type=int, default=1536, help="oracle sample tokens per linear")
-    ap.add_argument("--ref-tokens", type=int, default=128,
-                    help="oracle tokens per linear per step of the reference arm")
+    ap.add_argument("--cpu-tokens", type=int, default=1536,
+                    help="oracle sample tokens per linear (the cpu_baseline leg and each step of "
+                         "the reference arm)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (measured in child processes after the main line)")
+    ap.add_argument("--extra-steps", type=int, default=10,
+                    help="timed steps of each other workload (3 warm-up steps each)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (small profiling cases only)")
     ap.add_argument("--clock-log", default=None,
@@ -302,16 +306,16 @@ def run_reference(args, wl, b, rank):
     if rank != 0:
         return
     for _ in range(args.warmup):
-        oracle_sample(wl, b, args.ref_tokens, args.mode)
+        oracle_sample(wl, b, args.cpu_tokens, args.mode)
     times = []
     threads = None
     for _ in range(args.steps):
-        t, threads = oracle_sample(wl, b, args.ref_tokens, args.mode)
+        t, threads = oracle_sample(wl, b, args.cpu_tokens, args.mode)
         times.append(t)
     tot = sum(times)
-    tps = args.ref_tokens * args.steps / tot
-    sample = (f"{len(wl.linears)} linears x {args.ref_tokens} tokens per step (of {wl.tokens}), "
-              f"fwd+bwd with block build, fp64 numpy; merge not timed")
+    tps = args.cpu_tokens * args.steps / tot
+    sample = (f"{len(wl.linears)} linears x {args.cpu_tokens} tokens per step (of {wl.tokens}), "
+              f"fwd+bwd with block build, fp64 numpy; merge not timed (the cpu_baseline sample)")
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -326,6 +330,15 @@ def run_reference(args, wl, b, rank):
     print(json.dumps(line), flush=True)
 
 
+def graph_replay(wl, args) -> bool:
+    """Whether the timed steps replay a captured CUDA graph: on request, or
+    (auto) for workloads without a per-step merge, whose new permutations
+    come from the host, and without an optimizer step, whose step count
+    comes from the host."""
+    return args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step
+                                  and args.optimizer == "none")
+
+
 def workload_config(wl, b, args):
     return {
         "workload": wl.key, "description": wl.description,
@@ -336,6 +349,7 @@ def workload_config(wl, b, args):
         "merge_each_step": wl.merge_each_step,
         "l2": "inputs larger than L2 (activations of all linears, several GB per step)",
         "parallelism": f"dp{args.gpus}",
+        "cuda_graph": graph_replay(wl, args),
     }
 
 
@@ -560,8 +574,7 @@ def main():
         raise SystemExit("device status reported a timeout during warm-up")
 
     # (an optimizer step takes its step count from the host, so it stays eager)
-    use_graph = args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step
-                                       and args.optimizer == "none")
+    use_graph = graph_replay(wl, args)
     if use_graph and wl.merge_each_step:
         raise SystemExit("--graph on needs a workload without a per-step merge")
     graph = None
@@ -643,9 +656,9 @@ def main():
         launches_top = kinds[top]["groups"]
         achieved = per_step * args.steps / (kinds[top]["ms"] / 1e3) / 1e12
         roof = {"kernel": top, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_sustained"],
-                "peak_source": f"{peaks['source']} bf16 sustained",
+                "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"],
+                "peak_source": f"{peaks['source']} bf16 burst",
                 "launches": launches_top,
                 "avg_launch_ms": kinds[top]["ms"] / launches_top,
                 "flops_per_launch": per_step * args.steps / launches_top,
@@ -667,9 +680,11 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic: seeded N(0,1) activations, N(0,0.02^2) W0, "
                                    "N(0,0.01^2) packed generators",
-        "config": dict(workload_config(wl, b, args), cuda_graph=graph is not None),
-        "tflops": tflops, "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
+        "config": workload_config(wl, b, args),
+        "tflops": tflops, "tflops_frac_of_bf16_peak": tflops / peaks["bf16"],
+        "tflops_frac_of_bf16_peak_basis": f"{peaks['source']} bf16 burst ({peaks['bf16']} TFLOP/s)",
         "tflops_frac_of_bf16_burst": tflops / peaks["bf16"],
+        "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
         "step_tflop": flops / 1e12, "roofline": roof, "kernels": kinds,
         "kernels_timing": ("library CUDA events on the launching streams over as many eager "
                            "steps run right after the timed region"),
@@ -695,10 +710,61 @@ def main():
             "kind": "oracle",
             "sample": (f"{len(wl.linears)} linears x {args.cpu_tokens} tokens (of {T}), fwd+bwd "
                        f"with block build, fp64 numpy, {secs:.1f} s; merge not timed")}
+    # ---- the other workloads, each in a child process (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_extra:
+        line["workloads"] = run_extra_workloads(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+# The benchmark's other configurations, measured after the main line: the
+# single fp32 linear, the LLaMA-60M and d = 1024 blocks, the d = 2048 block
+# with 256-wide blocks, and the d = 4096 FFN pair at b = 128 and b = 512.
+EXTRA_WORKLOADS = [("fp32_256", 32), ("llama60m_block", 32), ("d1024_block", 64),
+                   ("d2048_block", 256), ("d4096_ffn", 128), ("d4096_ffn", 512)]
+
+
+def summarise_extra(d: dict) -> dict:
+    """The fields of a child benchmark line that the main line reports."""
+    roof = d.get("roofline") or {}
+    clk = d.get("clocks") or {}
+    return {
+        "workload": d["config"]["workload"], "b": d["config"]["b"], "dtype": d["dtype"],
+        "tokens_per_s": d["value"], "ms_per_step": d["ms_per_step"], "steps": d["steps"],
+        "step_tflop": d.get("step_tflop"), "tflops": d.get("tflops"),
+        "frac_of_bf16_burst": d.get("tflops_frac_of_bf16_burst"),
+        "frac_of_bf16_sustained": d.get("tflops_frac_of_bf16_sustained"),
+        "cuda_graph": d["config"].get("cuda_graph"), "recompute": d["config"].get("recompute"),
+        "merge_each_step": d["config"].get("merge_each_step"),
+        "roofline": {k: roof.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit", "frac")}
+        if roof else None,
+        "gpu_launches": d.get("gpu_launches"),
+        "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")} if clk else None,
+        "device_status": d.get("device_status"),
+    }
+
+
+def run_extra_workloads(args):
+    out = []
+    for key, b in EXTRA_WORKLOADS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", key, "--b", str(b),
+               "--steps", str(args.extra_steps), "--warmup", "3", "--mode", args.mode,
+               "--no-e2e", "--no-cpu-baseline", "--no-overhead", "--no-extra"]
+        t0 = time.time()
+        try:
+            res = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+            lines = [l for l in res.stdout.strip().splitlines() if l.startswith("{")]
+            if res.returncode != 0 or not lines:
+                out.append({"workload": key, "b": b, "error": (res.stderr or res.stdout)[-400:]})
+                continue
+            rec = summarise_extra(json.loads(lines[-1]))
+            rec["wall_s"] = round(time.time() - t0, 1)
+            out.append(rec)
+        except Exception as exc:  # a failed child is reported, not fatal to the main line
+            out.append({"workload": key, "b": b, "error": repr(exc)[-400:]})
+    return out
 
 
 def flush_l2(torch, buf):
@@ -841,7 +907,12 @@ def run_e2e(args, wl, b, layers, workspace, stream, dev, px, torch, world, dist,
         el = float(t.item())
     return {"value": world * T * args.steps / el, "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": 1e3 * el / args.steps}
+            "ms_per_step": 1e3 * el / args.steps,
+            "scope": ("per step and linear through poetx_linear_step_host_async: X and dY copied "
+                      "host -> device from pinned buffers, forward and backward (with the step's "
+                      "block builds and, where the workload merges, the merges), packed generator "
+                      "gradients copied device -> host; Y and dX stay on the device"),
+            "timing": "host wall clock around the steps, one device synchronisation per step"}
 
 
 if __name__ == "__main__":

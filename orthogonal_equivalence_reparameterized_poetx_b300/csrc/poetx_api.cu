@@ -1990,8 +1990,11 @@ poetx_status step_host_impl(const poetx_layer_desc* desc, const void* params, co
   };
   const poetx_status rs = run();
   if (rs != POETX_OK) {
-    // the copies may still be reading the caller's host buffers
+    // the copies may still be reading the caller's host buffers: wait for the
+    // copy stream, and for the caller's stream when the copies ran on it or
+    // the call is synchronous (results ignored: the first error is returned)
     if (cs) (void)cudaStreamSynchronize(cs);
+    if (!cs || !async) (void)cudaStreamSynchronize(st);
     return rs;
   }
   const int64_t lr = poetx_gen_length(desc->m, desc->b_R), lp = poetx_gen_length(desc->n, desc->b_P);
