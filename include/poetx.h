@@ -302,6 +302,16 @@ poetx_status poetx_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
  * launches; 0 restores the default (2 s). */
 void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
 
+/* Programmatic dependent launch of the forward, backward and optimizer
+ * kernels (on by default; on != 0 turns it on).  When on, each of those
+ * kernels may start on the GPU while the kernel before it on the same stream
+ * finishes: it sets up its shared memory, barriers and tensor memory, then
+ * waits for that kernel to complete before reading or writing global
+ * memory, so results are identical either way; only the gaps between
+ * launches change.  Applies to launches issued after the call (a captured
+ * CUDA graph keeps the setting it was captured with). */
+void poetx_set_dependent_launch(int32_t on);
+
 /* Forward for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers

@@ -23,6 +23,26 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the grids this
+// launch depends on have completed and their memory operations are visible
+// (it returns at once when the launch has no such dependency); a kernel
+// launched as a programmatic dependent must call it before its first access
+// to global memory that another kernel writes.  griddep_launch_dependents
+// lets the next launch of the stream start to be scheduled once every CTA of
+// this grid has called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Both, in that order: every thread of a kernel that the library may launch
+// as a programmatic dependent calls this once, on every path, after its
+// set-up of shared memory, barriers and tensor memory and before its first
+// global-memory access (also before any early return).
+__device__ __forceinline__ void griddep_enter() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const T* __restrict__ 
                                                           T* __restrict__ out,
                                                           const int32_t* __restrict__ idx,
                                                           int64_t rows, int d, int rows_per_iter) {
+  griddep_enter();
   extern __shared__ __align__(16) uint8_t gsm[];
   T* buf = reinterpret_cast<T*>(gsm);
   uint4* buf4 = reinterpret_cast<uint4*>(gsm);
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(256) gather_rows_pipelined_kernel(const uint16
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_enter();
   auto issue = [&](int64_t k, int s) {
     const int64_t b = blockIdx.x + k * gridDim.x;
     if (b >= nblocks) return;
@@ -364,6 +366,7 @@ __global__ void __launch_bounds__(256) gather_cols_bf16x2_kernel(const uint4* __
                                                                  const int32_t* __restrict__ idx,
                                                                  int64_t rows, int d,
                                                                  int pairs_per_iter) {
+  griddep_enter();
   extern __shared__ __align__(16) uint8_t gsm[];
   uint32_t* w = reinterpret_cast<uint32_t*>(gsm);
   const int vpr = d / 8;  // 16-byte vectors per row
@@ -426,6 +429,7 @@ __global__ void __launch_bounds__(256) gather_cols_scalar_kernel(const T* __rest
                                                                  T* __restrict__ out,
                                                                  const int32_t* __restrict__ idx,
                                                                  int64_t rows, int d) {
+  griddep_enter();
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
     for (int c = threadIdx.x; c < d; c += blockDim.x) out[r * d + c] = in[r * d + __ldg(idx + c)];
 }
@@ -905,6 +909,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ gen, con
                                                     float* __restrict__ m1, float* __restrict__ m2, int64_t len,
                                                     float beta1, float beta2, float eps, float decay_factor,
                                                     float step_size, float inv_sqrt_bc2) {
+  griddep_enter();
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < len;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float g = grad[e];
@@ -924,6 +929,7 @@ __global__ void __launch_bounds__(256) gradred_reduce_kernel(const float* __rest
                                                              int64_t split_stride, int splits,
                                                              SideGeom s, int sb,
                                                              float* __restrict__ G) {
+  griddep_enter();
   const int64_t bb = static_cast<int64_t>(s.b) * s.b;
   const int64_t total = static_cast<int64_t>(s.nblk) * bb;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
@@ -945,6 +951,7 @@ __global__ void __launch_bounds__(256) gradred_reduce_kernel(const float* __rest
 // time), consecutive lanes on consecutive packed entries.
 __global__ void __launch_bounds__(256) pack_grad_kernel(const float* __restrict__ GQ, SideGeom s,
                                                         float* __restrict__ out, int accumulate) {
+  griddep_enter();
   const int k = blockIdx.x;
   const int i = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -979,6 +986,7 @@ template <int P>
 __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
     const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s, int sb,
     const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
+  griddep_enter();
   constexpr int LD = P + 4;
   constexpr int NT = cbwd_threads<P>();
   constexpr int CT = (P / 4) * (P / 4);  // threads of the matrix products
@@ -1003,17 +1011,33 @@ __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
     g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     mv[u] = *reinterpret_cast<const float4*>(Mk + i * P + j4);
   }
-  for (int p = 0; p < splits; ++p) {
-    float4 w[PER];
+  // SU splits' loads are issued before any of them is added (SU * PER
+  // float4 in flight per thread); the sum keeps ascending split order
+  constexpr int SU = PER >= 8 ? 1 : 8 / PER;
+  auto split_ld = [&](int p, int u) {
+    const int e = threadIdx.x + NT * u;
+    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
+    return *reinterpret_cast<const float4*>(Pk + p * split_stride + static_cast<int64_t>(i) * sb + j4);
+  };
+  int p = 0;
+  for (; p + SU <= splits; p += SU) {
+    float4 w[SU][PER];
+#pragma unroll
+    for (int q = 0; q < SU; ++q)
+#pragma unroll
+      for (int u = 0; u < PER; ++u) w[q][u] = split_ld(p + q, u);
+#pragma unroll
+    for (int q = 0; q < SU; ++q)
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        g[u].x += w[q][u].x; g[u].y += w[q][u].y; g[u].z += w[q][u].z; g[u].w += w[q][u].w;
+      }
+  }
+  for (; p < splits; ++p) {
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-      const int e = threadIdx.x + NT * u;
-      const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
-      w[u] = *reinterpret_cast<const float4*>(Pk + p * split_stride + static_cast<int64_t>(i) * sb + j4);
-    }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      g[u].x += w[u].x; g[u].y += w[u].y; g[u].z += w[u].z; g[u].w += w[u].w;
+      const float4 w = split_ld(p, u);
+      g[u].x += w.x; g[u].y += w.y; g[u].z += w.z; g[u].w += w.w;
     }
   }
 #pragma unroll
@@ -1123,6 +1147,7 @@ struct CbwdSide {
 // layer in one launch).
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(256) cayley_bwd_cluster_kernel(
     const CbwdSide a, const CbwdSide b, int accumulate) {
+  griddep_enter();
   constexpr int P = 128, LD = kCbwdLD, TLD = kCbwdTLD;
   const int kg = blockIdx.x / 4;
   const bool on_a = kg < a.s.nblk;
@@ -1157,17 +1182,31 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(256) cayley_bwd_clus
       g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       m[u] = *reinterpret_cast<const float4*>(Mk + i * P + j4);
     }
-    for (int p = 0; p < splits; ++p) {
-      float4 w[PER];
+    // two splits' loads in flight before they are added (ascending split order)
+    auto split_ld = [&](int p, int u) {
+      const int e = tid + 256 * u;
+      const int i = r0 + e / (P / 4), j4 = 4 * (e % (P / 4));
+      return *reinterpret_cast<const float4*>(Pk + p * split_stride + i * P + j4);
+    };
+    int p = 0;
+    for (; p + 2 <= splits; p += 2) {
+      float4 w[2][PER];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) w[q][u] = split_ld(p + q, u);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          g[u].x += w[q][u].x; g[u].y += w[q][u].y; g[u].z += w[q][u].z; g[u].w += w[q][u].w;
+        }
+    }
+    if (p < splits) {
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
-        const int e = tid + 256 * u;
-        const int i = r0 + e / (P / 4), j4 = 4 * (e % (P / 4));
-        w[u] = *reinterpret_cast<const float4*>(Pk + p * split_stride + i * P + j4);
-      }
-#pragma unroll
-      for (int u = 0; u < PER; ++u) {
-        g[u].x += w[u].x; g[u].y += w[u].y; g[u].z += w[u].z; g[u].w += w[u].w;
+        const float4 w = split_ld(p, u);
+        g[u].x += w.x; g[u].y += w.y; g[u].z += w.z; g[u].w += w.w;
       }
     }
 #pragma unroll

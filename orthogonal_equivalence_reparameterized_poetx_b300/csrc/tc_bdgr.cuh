@@ -29,6 +29,7 @@ struct BdgrArgs {
   int N;          // features d
   int nsb;        // super-blocks
   int nslots;     // CTAs per super-block
+  int b;          // block size (32, 64 or 128): only the b x b diagonal blocks of a partial are written
   float* partial; // [nslots][nsb][128][128]
   uint64_t timeout_ns;
 };
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_enter();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -221,6 +223,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       const int col = half * 64 + c * 32;
+      // the reduction is read only on the diagonal b x b blocks (one block
+      // per warp's 32 rows, b >= 32): other column chunks are skipped
+      if (col / args.b != row / args.b) continue;
       uint32_t r[32];
       if (ntiles > 0) {
         tmem_ld_32x32b_x32(tmem_base + 256 + col + (static_cast<uint32_t>(g * 32) << 16), r);

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_enter();
 
   if (warp == 0) {
     if (lane == 0) {

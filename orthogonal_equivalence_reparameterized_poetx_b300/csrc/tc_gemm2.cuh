@@ -93,6 +93,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_enter();
 
   if (warp == 0) {
     if (lane == 0) {

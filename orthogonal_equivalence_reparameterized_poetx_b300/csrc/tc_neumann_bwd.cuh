@@ -136,6 +136,7 @@ __global__ void __cluster_dims__(NeuCfg<BS>::C, 1, 1) __launch_bounds__(288, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_enter();
 
   // epilogue thread mapping: row i of the tile, columns hh * NT/2 + [0, NT/2)
   const int gq = warp & 3, hh = warp >> 2;
