@@ -334,9 +334,10 @@ def graph_replay(wl, args) -> bool:
     """Whether the timed steps replay a captured CUDA graph: on request, or
     (auto) for workloads without a per-step merge, whose new permutations
     come from the host, and without an optimizer step, whose step count
-    comes from the host."""
+    comes from the host, on one GPU (with several ranks the per-layer
+    gradient sums run eagerly on their own stream)."""
     return args.graph == "on" or (args.graph == "auto" and not wl.merge_each_step
-                                  and args.optimizer == "none")
+                                  and args.optimizer == "none" and args.gpus == 1)
 
 
 def workload_config(wl, b, args):
@@ -472,6 +473,11 @@ def main():
     merge_ws = ([torch.empty(px.poetx_merge_workspace_size(st["desc"]), dtype=torch.uint8,
                              device=dev) for st in layers] if wl.merge_each_step else None)
     bwd_done = [None] * len(layers)    # event after layer l's backward in the previous step
+    # data parallel: each layer's packed gradients are summed over ranks on
+    # their own stream, right after that layer's backward, while the main
+    # stream runs the next layer's backward; the main stream waits for a
+    # layer's sum only before its optimizer update and at the end of the step
+    comm = torch.cuda.Stream(dev, priority=hi) if dist is not None else None
     merged = [0]                       # merges issued so far (for fresh seeds)
 
     def merge_one(li, st, ss, tag):
@@ -540,6 +546,7 @@ def main():
 
     def step():
         s = step_counter[0]
+        reduced = []
         ready = build_all(s)
         for li, st in enumerate(layers):
             for e in ready[li]:
@@ -551,8 +558,17 @@ def main():
             px.poetx_linear_bwd(st["desc"], st["params"], st["W0p"], st["X"], st["dY"], st["h"],
                                 st["u"], T, st["dX"], st["dgR"], st["dgP"], 0, workspace, stream)
             if dist is not None:
-                dist.all_reduce(st["dgR"])
-                dist.all_reduce(st["dgP"])
+                e = torch.cuda.Event()
+                e.record(stream)
+                comm.wait_event(e)
+                with torch.cuda.stream(comm):
+                    dist.all_reduce(st["dgR"])
+                    dist.all_reduce(st["dgP"])
+                red = torch.cuda.Event()
+                red.record(comm)
+                reduced.append(red)
+                if args.optimizer == "adamw":
+                    stream.wait_event(red)
             if args.optimizer == "adamw":
                 mR, vR, mP, vP = st["mom"]
                 px.poetx_generator_adamw(st["genR"], st["dgR"], mR, vR, st["lr"], s + 1, 1e-3,
@@ -562,6 +578,8 @@ def main():
             e = torch.cuda.Event()
             e.record(stream)
             bwd_done[li] = e
+        for red in reduced:   # the step's gradients are summed before it ends
+            stream.wait_event(red)
         # the merges of this step are issued at the start of the next step (they
         # overlap its builds and forwards); the timed region ends with drain_merges
         step_counter[0] += 1
@@ -616,13 +634,23 @@ def main():
     launches = (launches_per_step * args.steps if graph is not None
                 else px.poetx_launch_count() - launches0)
     clk = clocks.stop()
-    # per-class device times (roofline) from as many steps, run eagerly with
-    # the library's timing events right after the timed region
+    # per-class device times (roofline) from as many steps with the library's
+    # timing events, right after the timed region: replayed from a graph when
+    # the timed steps are (the events become graph nodes, so the times hold
+    # no host launch gaps), else eager
     px.poetx_profile_reset()
     px.poetx_profile_enable(True)
-    for _ in range(args.steps):
-        step()
-    drain_merges(step_counter[0])
+    if graph is not None:
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph, stream=stream):
+            for _ in range(args.steps):
+                step()
+        px.poetx_profile_enable(False)
+        pgraph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
+        drain_merges(step_counter[0])
     torch.cuda.synchronize(dev)
     px.poetx_profile_enable(False)
     elapsed_ms = ev0.elapsed_time(ev1)
@@ -686,8 +714,10 @@ def main():
         "tflops_frac_of_bf16_burst": tflops / peaks["bf16"],
         "tflops_frac_of_bf16_sustained": tflops / peaks["bf16_sustained"],
         "step_tflop": flops / 1e12, "roofline": roof, "kernels": kinds,
-        "kernels_timing": ("library CUDA events on the launching streams over as many eager "
-                           "steps run right after the timed region"),
+        "kernels_timing": ("library CUDA events on the launching streams over as many steps "
+                           "run right after the timed region, "
+                           + ("replayed from a captured graph (events as graph nodes)"
+                              if graph is not None else "eager")),
         "gpu_launches": launches, "clocks": clk,
         "device_status": px.poetx_status_string(status),
     }

@@ -364,7 +364,10 @@ enum {
 
 /* Profiling.  While enabled, each group of launches of one kernel class is
  * bracketed by CUDA events recorded on the launching stream (for the tensor-
- * core classes a group is a single launch).  poetx_profile_read synchronises
+ * core classes a group is a single launch).  Inside a stream capture the
+ * events become event-record nodes of the graph, so a replay of the graph
+ * times the captured launches (read after the replay; a later replay
+ * overwrites the times).  poetx_profile_read synchronises
  * on those events and returns, for `kind`, the number of groups and their
  * summed device time in milliseconds.  poetx_profile_reset forgets all
  * records.  poetx_launch_count returns the number of kernel launches the

@@ -70,6 +70,17 @@ struct Profiler {
 };
 Profiler g_prof;
 
+// Records a timing event on `st`.  Inside a stream capture the record becomes
+// an event-record node of the graph (an external record), so each replay of
+// the graph times the captured launches.
+void prof_record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 // Brackets the launches made during its lifetime with events on `st`.
 struct ProfScope {
   int kind;
@@ -79,13 +90,13 @@ struct ProfScope {
     if (!g_prof.on) return;
     std::lock_guard<std::mutex> lock(g_prof.mu);
     start = g_prof.get();
-    cudaEventRecord(start, st);
+    prof_record(start, st);
   }
   ~ProfScope() {
     if (!start) return;
     std::lock_guard<std::mutex> lock(g_prof.mu);
     cudaEvent_t stop = g_prof.get();
-    cudaEventRecord(stop, st);
+    prof_record(stop, st);
     g_prof.recs.push_back(ProfRecord{kind, start, stop});
   }
 };
@@ -1316,18 +1327,32 @@ poetx_status launch_cayley_bwd_clusters(cudaStream_t st, const CbwdSide& a, cons
   return launch_dep(cayley_bwd_cluster_kernel, blocks * 4, 256, kCbwdSmem, st, 0, a, b, accumulate);
 }
 
+// 32- or 64-wide blocks of one or two sides (side b may be empty), one CTA
+// per block (see cayley_bwd_kernel).
+poetx_status launch_cayley_bwd_small(cudaStream_t st, int P, const CbwdSide& a, const CbwdSide& b,
+                                     int accumulate) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(cayley_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(cbwd_smem<64>()));
+  });
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  const int blocks = a.s.nblk + b.s.nblk;
+  if (blocks == 0) return POETX_OK;
+  if (P == 64)
+    return launch_dep(cayley_bwd_kernel<64>, blocks, kCbwdThreads, cbwd_smem<64>(), st, 0, a, b, accumulate);
+  if (P == 32)
+    return launch_dep(cayley_bwd_kernel<32>, blocks, kCbwdThreads, cbwd_smem<32>(), st, 0, a, b, accumulate);
+  return POETX_ERR_UNSUPPORTED;
+}
+
 // Fused reduction + Cayley backward + packing for one side (see cayley_bwd_kernel).
 poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_t* params,
                               const float* partial, int splits, float* t1, float* t2, float* dGen,
                               int accumulate) {
   ProfScope prof(POETX_KIND_GENBWD, st);
   const int b = S.g.b;
-  const size_t smem = 3 * static_cast<size_t>(b) * (b + 4) * 4;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(cayley_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         3 * 64 * 68 * 4);
-  });
   const float* M = reinterpret_cast<const float*>(params + S.off_M);
   const int64_t stride = static_cast<int64_t>(S.nsb) * S.sb * S.sb;
   if (b >= 256) {
@@ -1346,15 +1371,10 @@ poetx_status fused_cayley_bwd(cudaStream_t st, const SideLayout& S, const uint8_
     POETX_TRY(tc_f32_gemm(st, b, b, b, nb, t, m, t2, b, bb, 2.f, 0.f));
     return launch_dep(pack_grad_kernel, dim3(nb, (b + 7) / 8), 256, 0, st, 0, t2, S.g, dGen, accumulate);
   }
-  if (b == 128) {  // four CTAs (one cluster) per block
-    CbwdSide a{partial, stride, splits, S.g, M, dGen}, none{};
-    none.s.nblk = 0;
-    return launch_cayley_bwd_clusters(st, a, none, accumulate);
-  }
-  auto kern = b == 64 ? cayley_bwd_kernel<64> : cayley_bwd_kernel<32>;
-  const int threads = b == 64 ? cbwd_threads<64>() : cbwd_threads<32>();
-  return launch_dep(kern, S.g.nblk, threads, smem, st, 0, partial, stride, splits, S.g, S.sb, M, dGen,
-                    accumulate);
+  CbwdSide a{partial, stride, splits, S.g, M, dGen}, none{};
+  none.s.nblk = 0;
+  if (b == 128) return launch_cayley_bwd_clusters(st, a, none, accumulate);  // four CTAs per block
+  return launch_cayley_bwd_small(st, b, a, none, accumulate);
 }
 
 // bf16 Neumann layers with 128-wide blocks: the chain rule of the
@@ -1396,14 +1416,15 @@ poetx_status bwd_common_tail(const Ctx& c, float* dGenR, float* dGenP, int accum
   float* nsc = c.w<float>(c.W.off_nsc);
   const bool doR = dGenR && poetx_gen_length(c.d.m, c.d.b_R) > 0;
   const bool doP = dGenP && poetx_gen_length(c.d.n, c.d.b_P) > 0;
-  if (doR && doP && c.d.b_R == 128 && c.d.b_P == 128 && fused_cayley_bwd_ok(c.d, 128)) {
-    // both sides' 128-wide blocks in one launch
+  if (doR && doP && c.d.b_R == c.d.b_P && c.d.b_R <= 128 && fused_cayley_bwd_ok(c.d, c.d.b_R)) {
+    // both sides' blocks in one launch
     ProfScope prof(POETX_KIND_GENBWD, c.st);
     const CbwdSide r{c.w<float>(c.W.off_partR), static_cast<int64_t>(c.L.R.nsb) * c.L.R.sb * c.L.R.sb,
                      c.slotsR, c.L.R.g, c.p<float>(c.L.R.off_M), dGenR};
     const CbwdSide p{c.w<float>(c.W.off_partP), static_cast<int64_t>(c.L.P.nsb) * c.L.P.sb * c.L.P.sb,
                      c.slotsP, c.L.P.g, c.p<float>(c.L.P.off_M), dGenP};
-    return launch_cayley_bwd_clusters(c.st, r, p, accumulate);
+    if (c.d.b_R == 128) return launch_cayley_bwd_clusters(c.st, r, p, accumulate);
+    return launch_cayley_bwd_small(c.st, c.d.b_R, r, p, accumulate);
   }
   if (fused_neumann_bwd_ok(c.d, c.d.b_R) || fused_neumann_bwd_ok(c.d, c.d.b_P)) {
     // five scratch matrices per side: side R at nsc, side P after them

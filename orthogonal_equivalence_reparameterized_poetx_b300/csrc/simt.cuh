@@ -966,94 +966,110 @@ __global__ void __launch_bounds__(256) pack_grad_kernel(const float* __restrict_
   }
 }
 
-// Cayley backward of one block per CTA (b = P in {32, 64, 128}, bf16 path), fused:
+// One side's operands of the Cayley backward: split partials
+// ([split][super-block][128][128] for 128-wide super-blocks), M per block,
+// packed output.
+struct CbwdSide {
+  const float* partial;
+  int64_t split_stride;
+  int splits;
+  SideGeom s;
+  const float* M;
+  float* out;
+};
+
+// Cayley backward of one P x P block per CTA (P in {32, 64}, bf16 path) for
+// the blocks of one or two sides (blocks [0, a.s.nblk) of side a, the rest
+// of side b), fused:
 //   G   = sum over token splits of the reduction partials (fixed order);
 //   GQ  = 2 M^T G M^T with M = (I - Q)^-1;
 //   g_ij (+)= GQ[i][j] - GQ[j][i] packed row by row (i < j < size).
-// (P/4)^2 threads, each owning a 4 x 4 tile of the products; matrices live in
+// Split reduction: every thread owns one float4 of the block and sums a
+// contiguous run of the splits (1024 / (P * P / 4) runs per block), eight
+// splits' loads in flight; the runs are then added in ascending order.
+// Products: (P/4)^2 threads own a 4 x 4 tile each; the matrices live in
 // shared memory with rows padded to P + 4 floats so 16-byte loads stay
-// aligned.  The second product reads T^T and M^T so both operands are
-// contiguous along the loop.
-// Threads of cayley_bwd_kernel<P>: the (P/4)^2 that hold a 4 x 4 tile of the
-// matrix products, and at least 256 so the split reduction has enough loads
-// in flight.
+// aligned, and the second product reads T^T and M^T so both operands are
+// contiguous along the loop.  A block lies on the diagonal of its 128-wide
+// super-block.
+constexpr int kCbwdThreads = 1024;
+
 template <int P>
-__host__ __device__ constexpr int cbwd_threads() {
-  return (P / 4) * (P / 4) > 256 ? (P / 4) * (P / 4) : 256;
+__host__ __device__ constexpr int cbwd_runs() { return kCbwdThreads / (P * P / 4); }
+
+template <int P>
+__host__ __device__ constexpr size_t cbwd_smem() {
+  return static_cast<size_t>(3 * P * (P + 4) + (cbwd_runs<P>() - 1) * P * P) * 4;
 }
 
 template <int P>
-__global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
-    const float* __restrict__ partial, int64_t split_stride, int splits, SideGeom s, int sb,
-    const float* __restrict__ Mall, float* __restrict__ out, int accumulate) {
+__global__ void __launch_bounds__(kCbwdThreads) cayley_bwd_kernel(const CbwdSide a, const CbwdSide b,
+                                                                  int accumulate) {
   griddep_enter();
   constexpr int LD = P + 4;
-  constexpr int NT = cbwd_threads<P>();
+  constexpr int NT = kCbwdThreads;
+  constexpr int E = P * P / 4;           // float4 per block
+  constexpr int RUNS = cbwd_runs<P>();
   constexpr int CT = (P / 4) * (P / 4);  // threads of the matrix products
+  constexpr int SB = 128;                // super-block width of the partials
+  static_assert(RUNS * E == NT && P <= SB, "threads must tile the block");
   extern __shared__ __align__(16) float cbs[];
   float* Gs = cbs;             // G, then T^T
   float* Ms = cbs + P * LD;    // M, then GQ
   float* Mt = Ms + P * LD;     // M^T
-  const int k = blockIdx.x;
-  const float* Mk = Mall + static_cast<int64_t>(k) * P * P;
-  // block k (P <= sb) lies inside super-block (k * P) / sb at offset o0 on the diagonal
-  const int sbi = (k * P) / sb, o0 = k * P - sbi * sb;
-  const float* Pk = partial + static_cast<int64_t>(sbi) * sb * sb + static_cast<int64_t>(o0) * sb + o0;
-  // G (summed over splits in a fixed order) and M: PER float4 of each per
-  // thread, the loads of one split all in flight together
-  constexpr int PER = P * P / 4 / NT;
-  static_assert(PER * NT == P * P / 4, "threads must tile the block");
-  float4 g[PER], mv[PER];
-#pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int e = threadIdx.x + NT * u;
-    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
-    g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    mv[u] = *reinterpret_cast<const float4*>(Mk + i * P + j4);
-  }
-  // SU splits' loads are issued before any of them is added (SU * PER
-  // float4 in flight per thread); the sum keeps ascending split order
-  constexpr int SU = PER >= 8 ? 1 : 8 / PER;
-  auto split_ld = [&](int p, int u) {
-    const int e = threadIdx.x + NT * u;
-    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
-    return *reinterpret_cast<const float4*>(Pk + p * split_stride + static_cast<int64_t>(i) * sb + j4);
-  };
-  int p = 0;
-  for (; p + SU <= splits; p += SU) {
-    float4 w[SU][PER];
+  float4* run_sums = reinterpret_cast<float4*>(Mt + P * LD);  // runs 1.. [RUNS - 1][E]
+  const int kg = blockIdx.x;
+  const bool on_a = kg < a.s.nblk;
+  const CbwdSide& side = on_a ? a : b;
+  const int k = on_a ? kg : kg - a.s.nblk;
+  const SideGeom s = side.s;
+  const int tid = threadIdx.x;
+  const int e = tid % E, run = tid / E;
+  const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
+  const float* Mk = side.M + static_cast<int64_t>(k) * P * P;
+  float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (run == 0) mv = *reinterpret_cast<const float4*>(Mk + i * P + j4);
+  // block k lies in super-block (k * P) / SB at diagonal offset o0
+  const int sbi = (k * P) / SB, o0 = k * P - sbi * SB;
+  const float* src = side.partial + static_cast<int64_t>(sbi) * SB * SB +
+                     static_cast<int64_t>(o0 + i) * SB + o0 + j4;
+  const int per = (side.splits + RUNS - 1) / RUNS;
+  const int p0 = min(side.splits, run * per), p1 = min(side.splits, p0 + per);
+  float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int SU = 8;
+  int p = p0;
+  for (; p + SU <= p1; p += SU) {
+    float4 w[SU];
 #pragma unroll
     for (int q = 0; q < SU; ++q)
+      w[q] = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(p + q) * side.split_stride);
 #pragma unroll
-      for (int u = 0; u < PER; ++u) w[q][u] = split_ld(p + q, u);
-#pragma unroll
-    for (int q = 0; q < SU; ++q)
-#pragma unroll
-      for (int u = 0; u < PER; ++u) {
-        g[u].x += w[q][u].x; g[u].y += w[q][u].y; g[u].z += w[q][u].z; g[u].w += w[q][u].w;
-      }
-  }
-  for (; p < splits; ++p) {
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const float4 w = split_ld(p, u);
-      g[u].x += w.x; g[u].y += w.y; g[u].z += w.z; g[u].w += w.w;
+    for (int q = 0; q < SU; ++q) {
+      g.x += w[q].x; g.y += w[q].y; g.z += w[q].z; g.w += w[q].w;
     }
   }
+  for (; p < p1; ++p) {
+    const float4 w = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(p) * side.split_stride);
+    g.x += w.x; g.y += w.y; g.z += w.z; g.w += w.w;
+  }
+  if (RUNS > 1 && run > 0) run_sums[(run - 1) * E + e] = g;
+  __syncthreads();
+  if (run == 0) {
 #pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int e = threadIdx.x + NT * u;
-    const int i = e / (P / 4), j4 = 4 * (e % (P / 4));
-    *reinterpret_cast<float4*>(Gs + i * LD + j4) = g[u];
-    *reinterpret_cast<float4*>(Ms + i * LD + j4) = mv[u];
-    Mt[(j4 + 0) * LD + i] = mv[u].x;
-    Mt[(j4 + 1) * LD + i] = mv[u].y;
-    Mt[(j4 + 2) * LD + i] = mv[u].z;
-    Mt[(j4 + 3) * LD + i] = mv[u].w;
+    for (int r = 1; r < RUNS; ++r) {
+      const float4 w = run_sums[(r - 1) * E + e];
+      g.x += w.x; g.y += w.y; g.z += w.z; g.w += w.w;
+    }
+    *reinterpret_cast<float4*>(Gs + i * LD + j4) = g;
+    *reinterpret_cast<float4*>(Ms + i * LD + j4) = mv;
+    Mt[(j4 + 0) * LD + i] = mv.x;
+    Mt[(j4 + 1) * LD + i] = mv.y;
+    Mt[(j4 + 2) * LD + i] = mv.z;
+    Mt[(j4 + 3) * LD + i] = mv.w;
   }
   __syncthreads();
-  const bool mm = threadIdx.x < CT;  // holds a tile of the products
-  const int tr = (threadIdx.x % CT) / (P / 4), tc = threadIdx.x % (P / 4);
+  const bool mm = tid < CT;  // holds a tile of the products
+  const int tr = tid / (P / 4), tc = tid % (P / 4);
   float acc[4][4];
   // T = M^T G: T[i][j] = sum_q M[q][i] G[q][j]
 #pragma unroll
@@ -1063,9 +1079,9 @@ __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
   if (mm) {
 #pragma unroll 4
     for (int q = 0; q < P; ++q) {
-      const float4 a = *reinterpret_cast<const float4*>(Ms + q * LD + 4 * tr);
-      const float4 g = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
-      const float av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
+      const float4 av4 = *reinterpret_cast<const float4*>(Ms + q * LD + 4 * tr);
+      const float4 gv4 = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tc);
+      const float av[4] = {av4.x, av4.y, av4.z, av4.w}, gv[4] = {gv4.x, gv4.y, gv4.z, gv4.w};
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
@@ -1088,13 +1104,13 @@ __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
       for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
 #pragma unroll 4
     for (int q = 0; q < P; ++q) {
-      const float4 t = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tr);
-      const float4 m = *reinterpret_cast<const float4*>(Mt + q * LD + 4 * tc);
-      const float tv[4] = {t.x, t.y, t.z, t.w}, mv[4] = {m.x, m.y, m.z, m.w};
+      const float4 t4 = *reinterpret_cast<const float4*>(Gs + q * LD + 4 * tr);
+      const float4 m4 = *reinterpret_cast<const float4*>(Mt + q * LD + 4 * tc);
+      const float tv[4] = {t4.x, t4.y, t4.z, t4.w}, mw[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mv[y], acc[x][y]);
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(tv[x], mw[y], acc[x][y]);
     }
 #pragma unroll
     for (int x = 0; x < 4; ++x)
@@ -1104,12 +1120,12 @@ __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
   __syncthreads();
   // pack: one warp per row
   const int sz = block_size(s, k);
-  float* o = out + static_cast<int64_t>(k) * P * (P - 1) / 2;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = NT / 32;
-  for (int i = warp; i < sz - 1; i += nwarps) {
-    float* oi = o + (i * sz - i * (i + 1) / 2 - i - 1);
-    for (int j = i + 1 + lane; j < sz; j += 32) {
-      const float v = Ms[i * LD + j] - Ms[j * LD + i];
+  float* o = side.out + static_cast<int64_t>(k) * P * (P - 1) / 2;
+  const int warp = tid / 32, lane = tid % 32, nwarps = NT / 32;
+  for (int r = warp; r < sz - 1; r += nwarps) {
+    float* oi = o + (r * sz - r * (r + 1) / 2 - r - 1);
+    for (int j = r + 1 + lane; j < sz; j += 32) {
+      const float v = Ms[r * LD + j] - Ms[j * LD + r];
       if (accumulate) oi[j] += v;
       else oi[j] = v;
     }
@@ -1131,17 +1147,6 @@ __global__ void __launch_bounds__(cbwd_threads<P>()) cayley_bwd_kernel(
 constexpr int kCbwdLD = 132;        // padded row of a 128-wide fp32 matrix
 constexpr int kCbwdTLD = 36;        // padded row of T^T (32 wide)
 constexpr int kCbwdSmem = (2 * 128 * kCbwdLD + 128 * kCbwdTLD + 32 * kCbwdLD) * 4;
-
-// One side's operands: split partials ([split][block][128][128]), M per
-// block, packed output.
-struct CbwdSide {
-  const float* partial;
-  int64_t split_stride;
-  int splits;
-  SideGeom s;
-  const float* M;
-  float* out;
-};
 
 // Clusters [0, a.s.nblk) work on side a, the rest on side b (both sides of a
 // layer in one launch).
