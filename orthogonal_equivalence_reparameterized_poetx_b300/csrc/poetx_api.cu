@@ -17,6 +17,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -30,6 +31,7 @@
 #include "tc_merge.cuh"
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
+#include "tc_gemm_r.cuh"
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
 #include "tc_neumann_bwd.cuh"
@@ -601,6 +603,49 @@ poetx_status tc_dense_nt(cudaStream_t st, const void* A, const void* W, void* C,
   a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
   if (wide) return launch_tc<256, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
   return launch_tc<128, false, false, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
+}
+
+// h = v W0'^T and z[:, s] = h[:, s] S_s^T in one launch (tc_gemm_r.cuh),
+// for R sides with 128-wide super-blocks; h is written only when H is given.
+poetx_status tc_dense_nt_r(cudaStream_t st, const void* V, const void* W, const void* Ssb, void* H,
+                           void* Z, int64_t T, int N, int K, int nsb) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GEMM_FWD, st);
+  CUtensorMap ta, tb, ts, th, tz;
+  POETX_TRY(tmap_bf16(&ta, V, T, K, K, 128));
+  POETX_TRY(tmap_bf16(&tb, W, N, K, K, 128));
+  POETX_TRY(tmap_bf16(&ts, Ssb, static_cast<uint64_t>(nsb) * 128, 128, 128, 128));
+  POETX_TRY(tmap_bf16(&th, H ? H : Z, T, N, N, 128));
+  POETX_TRY(tmap_bf16(&tz, Z, T, N, N, 128));
+  TcGemmRArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + 127) / 128);
+  a.store_h = H != nullptr;
+  a.timeout_ns = g_timeout_ns;
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      tc_gemm_r_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGemmRCfg::SMEM);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  return launch_dep(tc_gemm_r_kernel, std::min(a.num_tiles, launch_sms()), 320, TcGemmRCfg::SMEM, st,
+                    T * N * 2, ta, tb, ts, th, tz, a);
+}
+
+// Whether the forward runs the R transform in the GEMM epilogue
+// (tc_gemm_r.cuh) instead of as a separate pass over h: where the plain
+// forward GEMM is the single-CTA 128 x 128 engine as well (outputs narrower
+// than 1024), and for outputs of at most kREpilogueMaxBytes.  Measured on
+// B300 (20-step means, two runs each), LLaMA-60M-shaped block: 0.587 ms per
+// step with no fused epilogue, 0.573 with it on the 512-wide outputs only,
+// 0.560 with it also on the 1376-wide ones (22.5 MB).  With the fused kernel
+// on every output width: d1024 block 4.24 -> 4.33 ms, d2048 block 17.14 ->
+// 18.89 ms and d4096 FFN pair 35.47 -> 39.66 ms, because wide outputs
+// otherwise run on CTA pairs with 256 x 256 tiles, which this kernel does not
+// have (1.9 ms slower forward GEMMs per d2048 step against 0.95 ms saved in
+// the R pass).
+constexpr int64_t kREpilogueMaxBytes = int64_t(32) << 20;
+bool r_epilogue(const SideLayout& R, int64_t T, int N) {
+  return R.sb == 128 && (!use_pair(T, N) || T * N * 2 <= kREpilogueMaxBytes);
 }
 
 // dv (T x N) = A (T x K) * W, W row-major K x N (B operand MN-major).
@@ -1306,8 +1351,12 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   const SideLayout &R = c.L.R, &P = c.L.P;
   POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
   POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
-  POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
-  POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
+  if (r_epilogue(R, T, m)) {
+    POETX_TRY(tc_dense_nt_r(c.st, v, W0p, c.p<__nv_bfloat16>(R.off_Bsb), hs, z, T, m, n, R.nsb));
+  } else {
+    POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
+    POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
+  }
   return gather_cols<__nv_bfloat16>(c.st, z, Y, c.piRinv(), T, m);
 }
 

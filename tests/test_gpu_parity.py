@@ -112,11 +112,14 @@ def test_bf16_b64(px):
     _case(px, 256, 640, 64, 64, 300, "bf16")
 
 
-def test_bf16_cta_pair_gemms_with_ragged_tiles(px):
+@pytest.mark.parametrize("T", [777, 12289])
+def test_bf16_cta_pair_gemms_with_ragged_tiles(px, T):
     # m = 1376 and n = 1032 are wide enough for the CTA-pair GEMMs (256 x 256
-    # tiles split over two CTAs) in the forward and the dgrad; neither they nor
-    # T = 777 are multiples of 256, and b = 64 leaves a ragged last block
-    _case(px, 1376, 1032, 64, 64, 777, "bf16")
+    # tiles split over two CTAs) in the dgrad, and at T = 12289 (outputs above
+    # 32 MB) in the forward too, where T = 777 takes the fused R epilogue;
+    # neither m, n nor T are multiples of 256, and b = 64 leaves a ragged
+    # last block
+    _case(px, 1376, 1032, 64, 64, T, "bf16")
 
 
 def test_bf16_b128(px):
@@ -164,6 +167,16 @@ def test_bf16_neumann_fused_builder_orders(px, k):
 def test_bf16_neumann_b512_ragged(px):
     # eight-CTA clusters per 512-wide block; 768 = 512 + 256 ragged
     _case(px, 768, 512, 512, 512, 130, "bf16", mode="neumann", gstd=0.01)
+
+
+@pytest.mark.parametrize("m,b,recompute", [(200, 64, False), (200, 64, True), (1000, 32, False),
+                                         (896, 128, True)])
+def test_bf16_r_transform_in_the_gemm_epilogue(px, m, b, recompute):
+    # outputs narrower than 1024 take the forward GEMM whose epilogue applies
+    # the R blocks (h written only when kept); 200 = 128 + 72 and 1000 =
+    # 7 x 128 + 104 end in a partial super-block, and 777 tokens in a partial
+    # token tile
+    _case(px, m, 320, b, b, 777, "bf16", recompute=recompute, index=3)
 
 
 def test_bf16_single_token_and_single_block(px):
