@@ -32,6 +32,7 @@
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
 #include "tc_gemm_r.cuh"
+#include "tc_gemm_p.cuh"
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
 #include "tc_neumann_bwd.cuh"
@@ -675,6 +676,48 @@ poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C,
   a.num_tiles = static_cast<int>((T + 127) / 128) * ((N + BN - 1) / BN);
   if (wide) return launch_tc<256, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
   return launch_tc<128, false, true, TileMode::Dense, __nv_bfloat16>(st, ta, tb, tc, a);
+}
+
+// dv = dh W0' with du = dv B_P and the dv^T u partials in the epilogue
+// (tc_gemm_p.cuh), for P sides with 128-wide super-blocks; dv is not written.
+// Adds the partial slots it writes to *slots.
+poetx_status tc_dense_nn_p(cudaStream_t st, const SideLayout& P, const void* dh, const void* W,
+                           const void* SsbT, const void* u, void* du, float* partial, int64_t T, int N,
+                           int K, int* slots) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GEMM_DGRAD, st);
+  CUtensorMap ta, tb, ts, tu, tdu;
+  POETX_TRY(tmap_bf16(&ta, dh, T, K, K, 128));
+  POETX_TRY(tmap_bf16(&tb, W, K, N, N, 64));
+  POETX_TRY(tmap_bf16(&ts, SsbT, static_cast<uint64_t>(P.nsb) * 128, 128, 128, 128));
+  POETX_TRY(tmap_bf16(&tu, u, T, N, N, 128));
+  POETX_TRY(tmap_bf16(&tdu, du, T, N, N, 128));
+  TcGemmPArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.nsb = P.nsb;
+  a.nslots = std::max(1, launch_sms() / P.nsb);
+  a.b = P.g.b;
+  a.partial = partial;
+  a.timeout_ns = g_timeout_ns;
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      tc_gemm_p_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGemmPCfg::SMEM);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  POETX_TRY(launch_dep(tc_gemm_p_kernel, a.nslots * P.nsb, 320, TcGemmPCfg::SMEM, st, T * N * 2, ta, tb, ts,
+                       tu, tdu, a));
+  *slots += a.nslots;
+  return POETX_OK;
+}
+
+// Whether the backward runs the P side's transform and token reduction in
+// the dgrad GEMM epilogue (tc_gemm_p.cuh): under the same rule as the
+// forward's R epilogue.  Measured on B300 (20-step means): LLaMA-60M-shaped
+// block 0.560 -> 0.532 ms per step; with the fused dgrad on every output
+// width, d1024 block 4.21 -> 4.39 ms, d2048 block 16.97 -> 18.60 ms and d4096
+// FFN pair 34.94 -> 41.17 ms (wide dgrads otherwise run on CTA pairs).
+bool p_epilogue(const SideLayout& P, int64_t T, int N) {
+  return P.sb == 128 && P.nsb <= launch_sms() && (!use_pair(T, N) || T * N * 2 <= kREpilogueMaxBytes);
 }
 
 // out[:, s] = in[:, s] * S_s^T over super-blocks: in/out T x d, Ssb (nsb*sb) x sb.
@@ -1594,16 +1637,20 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
     POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, &c.slotsR));
   }
 
-  POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
-
-  // P side: du, the dv^T u partials and dX
-  if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
+  // P side: dv, du, the dv^T u partials and dX
+  if (dX && p_epilogue(P, T, n)) {  // du and the partials in the dgrad epilogue
+    POETX_TRY(tc_dense_nn_p(c.st, P, dh, W0p, BsbPT, u, du, partP, T, n, m, &c.slotsP));
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
+  } else if (dX && bdgr_ok(P)) {  // du = dv B_P (over u) and the dv^T u partials from one read of dv
+    POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
     POETX_TRY(tc_bdgr(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
     POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
   } else if (dX && bdgr256_ok(P)) {
+    POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
     POETX_TRY(tc_bdgr256(c.st, P, dv, BsbPT, du, u, partP, T, &c.slotsP));
     POETX_TRY(gather_cols<__nv_bfloat16>(c.st, du, dX, c.piPinv(), T, n));
   } else {
+    POETX_TRY(tc_dense_nn(c.st, dh, W0p, dv, T, n, m));
     POETX_TRY(tc_gradred(c.st, P, dv, u, partP, T, &c.slotsP));
     if (dX) {
       POETX_TRY(tc_blockdiag(c.st, dv, BsbPT, du, T, n, P.sb, P.nsb));
