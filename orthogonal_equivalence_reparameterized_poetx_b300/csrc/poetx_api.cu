@@ -33,6 +33,7 @@
 #include "tc_gemm2.cuh"
 #include "tc_gemm_r.cuh"
 #include "tc_gemm_p.cuh"
+#include "tc_gemm2r.cuh"
 #include "cayley_cluster.cuh"
 #include "tc_neumann.cuh"
 #include "tc_neumann_bwd.cuh"
@@ -632,6 +633,32 @@ poetx_status tc_dense_nt_r(cudaStream_t st, const void* V, const void* W, const 
                     T * N * 2, ta, tb, ts, th, tz, a);
 }
 
+// The same on CTA pairs with 256 x 256 tiles (tc_gemm2r.cuh), for wide outputs.
+poetx_status tc_dense_nt_pair_r(cudaStream_t st, const void* V, const void* W, const void* Ssb, void* H,
+                                void* Z, int64_t T, int N, int K, int nsb) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_GEMM_FWD, st);
+  CUtensorMap ta, tb, ts, th, tz;
+  POETX_TRY(tmap_bf16(&ta, V, T, K, K, 128));
+  POETX_TRY(tmap_bf16(&tb, W, N, K, K, 128));
+  POETX_TRY(tmap_bf16(&ts, Ssb, static_cast<uint64_t>(nsb) * 128, 128, 128, 64));
+  POETX_TRY(tmap_bf16(&th, H ? H : Z, T, N, N, 128));
+  POETX_TRY(tmap_bf16(&tz, Z, T, N, N, 128));
+  TcPairRArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = N;
+  a.K = K;
+  a.num_tiles = static_cast<int>((T + 255) / 256) * ((N + 255) / 256);
+  a.store_h = H != nullptr;
+  a.timeout_ns = g_timeout_ns;
+  static cudaError_t attr_err = cudaFuncSetAttribute(
+      tc_gemm_pair_r_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcPairRCfg::SMEM_BYTES);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  const int pairs = std::max(1, std::min(a.num_tiles, launch_sms() / 2));
+  return launch_dep(tc_gemm_pair_r_kernel, 2 * pairs, 320, TcPairRCfg::SMEM_BYTES, st, T * N * 2, ta, tb,
+                    ts, th, tz, a);
+}
+
 // Whether the forward runs the R transform in the GEMM epilogue
 // (tc_gemm_r.cuh) instead of as a separate pass over h: where the plain
 // forward GEMM is the single-CTA 128 x 128 engine as well (outputs narrower
@@ -648,6 +675,15 @@ constexpr int64_t kREpilogueMaxBytes = int64_t(32) << 20;
 bool r_epilogue(const SideLayout& R, int64_t T, int N) {
   return R.sb == 128 && (!use_pair(T, N) || T * N * 2 <= kREpilogueMaxBytes);
 }
+
+// Wide outputs: the R transform in the epilogue of the CTA-pair GEMM.
+// Measured on B300 against the pair GEMM plus the separate R pass (20-step
+// means, two runs each): d1024 block 4.23 -> 4.08 ms per step, d2048 block
+// 17.00 -> 16.84 ms, d4096 FFN pair 34.70 -> 34.39 ms.  The forward GEMM
+// class itself gets slower (4.06 -> 5.05 ms per d2048 step: four pipeline
+// stages instead of six, the transform MMAs, and the extra shared-memory
+// traffic of staging h and z) but the R pass (0.95 ms) disappears.
+bool pair_r_epilogue(const SideLayout& R, int64_t T, int N) { return R.sb == 128 && use_pair(T, N); }
 
 // dv (T x N) = A (T x K) * W, W row-major K x N (B operand MN-major).
 poetx_status tc_dense_nn(cudaStream_t st, const void* A, const void* W, void* C, int64_t T, int N,
@@ -1396,6 +1432,8 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
   if (r_epilogue(R, T, m)) {
     POETX_TRY(tc_dense_nt_r(c.st, v, W0p, c.p<__nv_bfloat16>(R.off_Bsb), hs, z, T, m, n, R.nsb));
+  } else if (pair_r_epilogue(R, T, m)) {
+    POETX_TRY(tc_dense_nt_pair_r(c.st, v, W0p, c.p<__nv_bfloat16>(R.off_Bsb), hs, z, T, m, n, R.nsb));
   } else {
     POETX_TRY(tc_dense_nt(c.st, v, W0p, h, T, m, n));
     POETX_TRY(tc_blockdiag(c.st, h, c.p<__nv_bfloat16>(R.off_Bsb), z, T, m, R.sb, R.nsb));
