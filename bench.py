@@ -103,29 +103,56 @@ def step_flops(wl, b: int) -> float:
     return f
 
 
-def gemm_flops_per_step(wl, kind: str) -> float:
+# The library's placement of the block transforms of a bf16 layer (as its
+# forward and backward decide): for b <= 128 the forward R transform runs in
+# the forward GEMM's epilogue, and the backward P-side transform and token
+# reduction run in the dgrad's epilogue where that GEMM is the single-CTA
+# engine (outputs narrower than 1024, or fewer than 256 tokens) or its output
+# is at most 32 MB.
+def r_in_gemm(b: int) -> bool:
+    return b <= 128
+
+
+def p_in_dgrad(T: int, n: int, b: int) -> bool:
+    pair = n >= 1024 and T >= 256
+    return b <= 128 and (not pair or T * n * 2 <= (32 << 20))
+
+
+def gemm_flops_per_step(wl, kind: str, b: int = 0) -> float:
+    """Flops of a GEMM class: the GEMMs, plus the block-transform (and
+    reduction) flops that run in their epilogues when b is given."""
     T = wl.tokens
     f = 0.0
     for lin in wl.linears:
+        sR = block_square_sum(lin.m, b) if b else 0
+        sP = block_square_sum(lin.n, b) if b else 0
         if kind == "gemm_fwd":
             f += 2.0 * T * lin.m * lin.n * (2 if wl.recompute else 1)
+            if b and wl.dtype == "bf16" and r_in_gemm(b):
+                f += 2.0 * T * sR
         elif kind == "gemm_dgrad":
             f += 2.0 * T * lin.m * lin.n
+            if b and wl.dtype == "bf16" and p_in_dgrad(T, lin.n, b):
+                f += 4.0 * T * sP
     return f
 
 
 def kind_flops_per_step(wl, b: int, kind: str) -> float:
     T = wl.tokens
+    if kind in ("gemm_fwd", "gemm_dgrad"):
+        return gemm_flops_per_step(wl, kind, b)
     f = 0.0
     for lin in wl.linears:
         sR, sP = block_square_sum(lin.m, b), block_square_sum(lin.n, b)
-        if kind in ("gemm_fwd", "gemm_dgrad"):
-            return gemm_flops_per_step(wl, kind)
+        pd = wl.dtype == "bf16" and p_in_dgrad(T, lin.n, b)
+        rg = wl.dtype == "bf16" and r_in_gemm(b)
         if kind == "blockdiag":
-            # fwd P and R, bwd R^T and P^T, recompute P
-            f += 2.0 * T * (2 * sP + 2 * sR + (sP if wl.recompute else 0))
+            # fwd P (and R unless in the GEMM), bwd R^T (and P^T unless in the
+            # dgrad), recompute P
+            f += 2.0 * T * (sP + (0 if rg else sR) + sR + (0 if pd else sP)
+                            + (sP if wl.recompute else 0))
         elif kind == "gradred":
-            f += 2.0 * T * (sR + sP)
+            f += 2.0 * T * (sR + (0 if pd else sP))
     return f
 
 
@@ -135,11 +162,13 @@ def kind_bytes_per_step(wl, b: int, kind: str) -> float:
 
     gather: X -> u and z -> Y in the forward, dY -> dz and du -> dX in the
     backward, plus X -> u again when u is recomputed.  blockdiag: forward
-    u -> v and h -> z; backward dz -> dh and dv -> du, which for b <= 128 also
-    read h and u (the fused transform + reduction); plus u -> v when
-    recomputing.  gradred (sides whose reduction is not fused): dz^T h and
-    dv^T u read two operands.  The fused kernels are used for b <= 128 and,
-    when their grid fills the GPU, for b = 256 (as the library decides).
+    u -> v, and h -> z unless the R transform runs in the forward GEMM
+    (b <= 128); backward dz -> dh and dv -> du, which for b <= 128 also read h
+    and u (the fused transform + reduction), the latter unless it runs in the
+    dgrad's epilogue; plus u -> v when recomputing.  gradred (sides whose
+    reduction is not fused): dz^T h and dv^T u read two operands.  The fused
+    kernels are used for b <= 128 and, when their grid fills the GPU, for
+    b = 256 (as the library decides).
     """
     T = wl.tokens
     e = 2 if wl.dtype == "bf16" else 4
@@ -158,13 +187,15 @@ def kind_bytes_per_step(wl, b: int, kind: str) -> float:
     for lin in wl.linears:
         n, m = lin.n, lin.m
         fm, fn = fused(m), fused(n)
+        pd = wl.dtype == "bf16" and p_in_dgrad(T, n, b)
+        rg = wl.dtype == "bf16" and r_in_gemm(b)
         if kind == "gather":
             by += 2 * T * ((2 + r) * n + 2 * m) * e
         elif kind == "blockdiag":
-            bwd = (3 if fm else 2) * m + (3 if fn else 2) * n
-            by += T * (2 * n + 2 * m + bwd + 2 * n * r) * e
+            bwd = (3 if fm else 2) * m + (0 if pd else (3 if fn else 2) * n)
+            by += T * (2 * n + (0 if rg else 2 * m) + bwd + 2 * n * r) * e
         elif kind == "gradred":
-            by += T * ((0 if fm else 2) * m + (0 if fn else 2) * n) * e
+            by += T * ((0 if fm else 2) * m + (0 if (fn or pd) else 2) * n) * e
     return float(by)
 
 

@@ -63,13 +63,41 @@ def test_gemm_flop_classes_partition_the_gemm_flops():
 def test_d2048_memory_pass_bytes():
     wl = synth.WORKLOADS["d2048_block"]
     widths = 4 * (2048 + 2048) + 3 * (2048 + 5632)       # sum of n + m over the linears
+    sum_n = 4 * 2048 + 2 * 2048 + 5632
+    sum_m = 4 * 2048 + 2 * 5632 + 2048
+    assert sum_n + sum_m == widths
     # four permutation passes of 2 bytes in and 2 bytes out per element
     assert bench.kind_bytes_per_step(wl, 128, "gather") == 8 * T * widths
-    # forward transforms read + write (4 B), fused backward reads two and writes one (6 B)
-    assert bench.kind_bytes_per_step(wl, 128, "blockdiag") == 10 * T * widths
+    # forward P transform reads + writes (4 B per element of n; the R transform
+    # runs in the forward GEMM's epilogue), the fused backward transforms read
+    # two operands and write one (6 B per element of m and of n)
+    assert bench.kind_bytes_per_step(wl, 128, "blockdiag") == 2 * T * (5 * sum_n + 3 * sum_m)
     assert bench.kind_bytes_per_step(wl, 128, "gradred") == 0
     assert bench.kind_bytes_per_step(wl, 128, "gather") == 20669530112
-    assert bench.kind_bytes_per_step(wl, 128, "blockdiag") == 25836912640
+    assert bench.kind_bytes_per_step(wl, 128, "blockdiag") == 20199768064
+
+
+def test_epilogue_placement_follows_the_library():
+    # the R transform is in the forward GEMM for b <= 128 only
+    assert bench.r_in_gemm(32) and bench.r_in_gemm(128) and not bench.r_in_gemm(256)
+    # the P side is in the dgrad where that GEMM is single-CTA or its output <= 32 MB
+    assert bench.p_in_dgrad(8192, 512, 32)          # narrow output
+    assert bench.p_in_dgrad(8192, 1376, 32)         # 22.5 MB
+    assert not bench.p_in_dgrad(32768, 1024, 64)    # 64 MB on CTA pairs
+    assert bench.p_in_dgrad(128, 4096, 128)         # fewer than 256 tokens: single CTA
+    assert not bench.p_in_dgrad(8192, 512, 256)
+    # LLaMA-60M: every P side is in the dgrad, so the blockdiag class moves the
+    # forward P transform (4 B) and the fused R backward (6 B) only
+    wl = synth.WORKLOADS["llama60m_block"]
+    t = wl.tokens
+    sum_n = 6 * 512 + 1376
+    sum_m = 4 * 512 + 2 * 1376 + 512
+    assert bench.kind_bytes_per_step(wl, 32, "blockdiag") == 2 * t * (2 * sum_n + 3 * sum_m)
+    # and the dgrad class carries the transform and reduction flops, 4 T sum b_P^2
+    sq = lambda d: bench.block_square_sum(d, 32)
+    extra = 4 * t * (6 * sq(512) + sq(1376))
+    assert bench.kind_flops_per_step(wl, 32, "gemm_dgrad") == pytest.approx(
+        bench.gemm_flops_per_step(wl, "gemm_dgrad") + extra, rel=1e-12)
 
 
 def test_unfused_256_sides_are_counted_as_transform_plus_reduction():
@@ -81,6 +109,7 @@ def test_unfused_256_sides_are_counted_as_transform_plus_reduction():
     gr = bench.kind_bytes_per_step(wl, 256, "gradred")
     assert gr == 2 * T * (2 * m + 2 * m)      # up: R side 11008; down: P side 11008
     bd = bench.kind_bytes_per_step(wl, 256, "blockdiag")
+    # b = 256: the R transform stays a separate pass (2 * mm)
     per = lambda nn, mm, fm, fn: T * (2 * nn + 2 * mm + (3 if fm else 2) * mm + (3 if fn else 2) * nn
                                       + 2 * nn) * 2
     assert bd == per(n, m, False, True) + per(m, n, True, False)
