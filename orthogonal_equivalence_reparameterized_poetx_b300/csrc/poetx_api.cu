@@ -216,8 +216,10 @@ struct Splits {
   int splits, chunk;
 };
 
-Splits gradred_splits(const SideLayout& S, int64_t T, int nsm) {
-  const int tps = S.sb / 128;
+// Token splits of the separate reduction: `units` CTAs (or CTA pairs) each
+// taking tile x tile output tiles of the sb x sb products.
+Splits gradred_splits(const SideLayout& S, int64_t T, int nsm, int tile = 128) {
+  const int tps = S.sb / tile;
   const int per_split = S.nsb * tps * tps;
   const int64_t Tc = std::max<int64_t>(T, 1);
   const int64_t smax = std::max<int64_t>(1, std::min<int64_t>((4 * nsm + per_split - 1) / per_split,
@@ -263,10 +265,14 @@ int launch_sms() { return device_sm_count(); }
 // Upper bound on the reduction partial slots written for T tokens: GradRed
 // token splits or the fused transform + reduction's token slots.
 int64_t partial_slots_bound(const SideLayout& S, int64_t T) {
-  const int tps = S.sb / 128;
-  const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
-  const int64_t smax = std::max<int64_t>(
-      1, std::min<int64_t>((4 * device_sm_count() + per_split - 1) / per_split, (T + 63) / 64));
+  auto bound = [&](int tile, int units) {
+    const int tps = S.sb / tile;
+    const int64_t per_split = static_cast<int64_t>(S.nsb) * tps * tps;
+    return std::max<int64_t>(
+        1, std::min<int64_t>((4 * static_cast<int64_t>(units) + per_split - 1) / per_split, (T + 63) / 64));
+  };
+  int64_t smax = bound(128, device_sm_count());
+  if (S.sb >= 256) smax = std::max(smax, bound(256, std::max(1, device_sm_count() / 2)));
   const int64_t fused = std::max<int64_t>(1, device_sm_count() / S.nsb);
   return std::max(smax, fused);
 }
@@ -557,7 +563,21 @@ poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap
   return launch_dep(kern, grid, 320, smem, st, pass_bytes, ta, tb, tc, args);
 }
 
-// Dense GEMM on CTA pairs (tc_gemm2.cuh) with 256 x 256 tiles.
+// CTA-pair kernel (tc_gemm2.cuh) with 256 x 256 tiles, in any tile mode.
+template <bool B_MN, PairMode MODE>
+poetx_status launch_pair_mode(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& tc, TcPairArgs a, int64_t pass_bytes) {
+  if (a.num_tiles <= 0) return POETX_OK;
+  a.timeout_ns = g_timeout_ns;
+  auto kern = tc_gemm_pair_kernel<B_MN, MODE>;
+  static cudaError_t attr_err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcPairCfg::SMEM_BYTES);
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  const int pairs = std::max(1, std::min(a.num_tiles, launch_sms() / 2));
+  return launch_dep(kern, 2 * pairs, 320, TcPairCfg::SMEM_BYTES, st, pass_bytes, ta, tb, tc, a);
+}
+
+// Dense GEMM on CTA pairs.
 template <bool B_MN>
 poetx_status launch_pair(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tc, int64_t T, int N, int K) {
@@ -566,13 +586,7 @@ poetx_status launch_pair(cudaStream_t st, const CUtensorMap& ta, const CUtensorM
   a.N = N;
   a.K = K;
   a.num_tiles = static_cast<int>((T + 255) / 256) * ((N + 255) / 256);
-  a.timeout_ns = g_timeout_ns;
-  auto kern = tc_gemm_pair_kernel<B_MN>;
-  static cudaError_t attr_err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcPairCfg::SMEM_BYTES);
-  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
-  const int pairs = std::max(1, std::min(a.num_tiles, launch_sms() / 2));
-  return launch_dep(kern, 2 * pairs, 320, TcPairCfg::SMEM_BYTES, st, T * N * 2, ta, tb, tc, a);
+  return launch_pair_mode<B_MN, PairMode::Dense>(st, ta, tb, tc, a, T * N * 2);
 }
 
 // Wide outputs (N >= 1024) run on CTA pairs, narrower ones on single CTAs.
@@ -761,6 +775,9 @@ poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void
                           int d, int sb, int nsb) {
   if (T <= 0) return POETX_OK;
   ProfScope prof(POETX_KIND_BLOCKDIAG, st);
+  // (256 x 256 tiles on CTA pairs with K = sb were measured slower for sb >=
+  // 256 than these single-CTA 128 x 256 tiles: d4096 b = 256 block
+  // transforms 5.0 vs 3.9 ms per step)
   const int BN = sb >= 256 ? 256 : 128;
   CUtensorMap ta, tb, tc;
   POETX_TRY(tmap_bf16(&ta, in, T, d, d, 128));
@@ -782,10 +799,27 @@ poetx_status tc_blockdiag(cudaStream_t st, const void* in, const void* Ssb, void
 // *slots (the caller appends the next call's slots after them).
 poetx_status tc_gradred(cudaStream_t st, const SideLayout& S, const void* A, const void* B,
                         float* partial, int64_t T, int* slots) {
+  const int d = S.g.d, sb = S.sb, nsb = S.nsb;
+  if (sb >= 256 && use_pair(T, d)) {  // 256 x 256 tiles of each product on CTA pairs
+    const Splits sp = gradred_splits(S, T, std::max(1, launch_sms() / 2), 256);
+    *slots += sp.splits;
+    ProfScope prof(POETX_KIND_GRADRED, st);
+    CUtensorMap ta, tb;
+    POETX_TRY(tmap_bf16(&ta, A, T, d, d, 64));
+    POETX_TRY(tmap_bf16(&tb, B, T, d, d, 64));
+    TcPairArgs a{};
+    a.sb = sb;
+    a.nsb = nsb;
+    a.tokens = static_cast<int>(T);
+    a.chunk = sp.chunk;
+    a.C = partial;
+    a.split_stride = static_cast<int64_t>(nsb) * sb * sb;
+    a.num_tiles = sp.splits * nsb * (sb / 256) * (sb / 256);
+    return launch_pair_mode<true, PairMode::GradRed>(st, ta, tb, ta, a, T * static_cast<int64_t>(nsb) * sb * 2);
+  }
   const Splits sp = gradred_splits(S, T, launch_sms());
   *slots += sp.splits;
   ProfScope prof(POETX_KIND_GRADRED, st);
-  const int d = S.g.d, sb = S.sb, nsb = S.nsb;
   CUtensorMap ta, tb;
   POETX_TRY(tmap_bf16(&ta, A, T, d, d, 64));
   POETX_TRY(tmap_bf16(&tb, B, T, d, d, 64));

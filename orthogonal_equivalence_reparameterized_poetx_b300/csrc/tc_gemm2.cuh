@@ -1,8 +1,13 @@
-// Dense bf16 GEMM on CTA pairs (tcgen05 .cta_group::2).
+// bf16 GEMMs on CTA pairs (tcgen05 .cta_group::2).
 //
-// C (M x N, bf16, row-major) = A (M x K, K-major) * B^T, with B stored
+// Dense: C (M x N, bf16, row-major) = A (M x K, K-major) * B^T, with B stored
 // N x K (K-major: the forward h = v W0'^T) or K x N (MN-major: the dgrad
-// dv = dh W0').  A cluster of two CTAs owns 256 x 256 output tiles
+// dv = dh W0').
+// GradRed: partial[p][s] = sum over the tokens of split p of A[t, s]^T B[t, s]
+// for super-blocks of sb >= 256 (both operands MN-major, K = tokens), as
+// 256 x 256 fp32 tiles of each sb x sb product, stored directly.
+// ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+// Transformation", Methodologie §3: the blocks as independent matrices.)  A cluster of two CTAs owns 256 x 256 output tiles
 // (persistent over tiles): CTA r stages rows [128 r, 128 r + 128) of the A
 // tile and columns [128 r, 128 r + 128) of the B tile, the even CTA issues
 // M = 256, N = 256 MMAs that read both CTAs' shared memory, and each CTA's
@@ -26,11 +31,57 @@
 
 namespace poetx {
 
+enum class PairMode : int { Dense = 0, GradRed = 1 };
+
 struct TcPairArgs {
-  int M, N, K;
-  int num_tiles;  // ceil(M / 256) * ceil(N / 256)
+  int M, N, K;            // Dense: C is M x N, contraction K
+  int num_tiles;          // Dense: ceil(M / 256) * ceil(N / 256);
+                          // GradRed: splits * nsb * (sb / 256)^2
+  int sb;                 // GradRed: super-block size (multiple of 256)
+  int nsb;                // GradRed: super-blocks
+  int tokens, chunk;      // GradRed: tokens, tokens per split (multiple of 64)
+  float* C;               // GradRed: partials [split][nsb][sb][sb]
+  int64_t split_stride;   // GradRed: floats between split partials
   uint64_t timeout_ns;
 };
+
+// One output tile as CTA `rank` of the pair sees it.
+struct PairTile {
+  int m0;    // this CTA's A origin: rows (Dense) or features (GradRed)
+  int nb;    // this CTA's B origin (features)
+  int n0;    // Dense: the tile's first output column
+  int ky0;   // GradRed: first token of the split
+  int nk;    // k-iterations of 64
+  int p, s, i, j, row0;  // GradRed: split, super-block, tile indices, local row origin
+};
+
+template <PairMode MODE>
+__device__ __forceinline__ PairTile decode_pair(int tile, const TcPairArgs& a, uint32_t rank) {
+  PairTile t{};
+  if constexpr (MODE == PairMode::GradRed) {
+    const int tps = a.sb / 256;
+    const int per_split = a.nsb * tps * tps;
+    t.p = tile / per_split;
+    int r = tile % per_split;
+    t.s = r / (tps * tps);
+    r %= tps * tps;
+    t.i = r / tps;
+    t.j = r % tps;
+    t.row0 = t.i * 256 + 128 * static_cast<int>(rank);
+    t.m0 = t.s * a.sb + t.row0;
+    t.nb = t.s * a.sb + t.j * 256 + 128 * static_cast<int>(rank);
+    t.ky0 = t.p * a.chunk;
+    const int len = min(a.chunk, a.tokens - t.ky0);
+    t.nk = len > 0 ? (len + 63) / 64 : 0;
+  } else {
+    const int ntn = (a.N + 255) / 256;
+    t.m0 = (tile / ntn) * 256 + 128 * static_cast<int>(rank);
+    t.n0 = (tile % ntn) * 256;
+    t.nb = t.n0 + 128 * static_cast<int>(rank);
+    t.nk = (a.K + 63) / 64;
+  }
+  return t;
+}
 
 struct TcPairCfg {
   static constexpr int A_BYTES = 128 * 64 * 2;  // this CTA's 128 rows x 64 k
@@ -42,7 +93,7 @@ struct TcPairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <bool B_MN>
+template <bool B_MN, PairMode MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcPairArgs args) {
@@ -65,7 +116,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   const int lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
   const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
-  const int ntn = (args.N + 255) / 256;
   const uint64_t tmo = args.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -82,7 +132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmC);
+    if constexpr (MODE != PairMode::GradRed) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -105,21 +155,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
       for (int tile = pair; tile < args.num_tiles && ok; tile += npairs) {
-        const int m0 = (tile / ntn) * 256 + 128 * static_cast<int>(rank);
-        const int nb = (tile % ntn) * 256 + 128 * static_cast<int>(rank);
-        const int nk = (args.K + 63) / 64;
-        for (int kb = 0; kb < nk; ++kb) {
+        const PairTile t = decode_pair<MODE>(tile, args, rank);
+        for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
           uint8_t* sb = sa + Cfg::A_BYTES;
           const uint32_t fbar = dsmem_addr(&full[stage], 0);  // the even CTA's barrier
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, fbar, kb * 64, m0);
-          if constexpr (B_MN) {
-            tma_load_2d_pair(sb, &tmB, fbar, nb, kb * 64);
-            tma_load_2d_pair(sb + 64 * 128, &tmB, fbar, nb + 64, kb * 64);
+          if constexpr (MODE == PairMode::GradRed) {
+            // both operands MN-major: 64-feature x 64-token boxes
+            const int ky = t.ky0 + kb * 64;
+            tma_load_2d_pair(sa, &tmA, fbar, t.m0, ky);
+            tma_load_2d_pair(sa + 64 * 128, &tmA, fbar, t.m0 + 64, ky);
+            tma_load_2d_pair(sb, &tmB, fbar, t.nb, ky);
+            tma_load_2d_pair(sb + 64 * 128, &tmB, fbar, t.nb + 64, ky);
           } else {
-            tma_load_2d_pair(sb, &tmB, fbar, kb * 64, nb);
+            tma_load_2d_pair(sa, &tmA, fbar, kb * 64, t.m0);
+            if constexpr (B_MN) {
+              tma_load_2d_pair(sb, &tmB, fbar, t.nb, kb * 64);
+              tma_load_2d_pair(sb + 64 * 128, &tmB, fbar, t.nb + 64, kb * 64);
+            } else {
+              tma_load_2d_pair(sb, &tmB, fbar, kb * 64, t.nb);
+            }
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
@@ -138,7 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, false, B_MN);
+      constexpr bool A_MN = MODE == PairMode::GradRed;
+      constexpr bool BM = B_MN || MODE == PairMode::GradRed;
+      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, A_MN, BM);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -149,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, tmo, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * 256;
-        const int nk = (args.K + 63) / 64;
+        const int nk = decode_pair<MODE>(tile, args, rank).nk;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, tmo, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -157,9 +216,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            uint64_t bd;
-            if constexpr (B_MN) bd = smem_desc_sw128(sb + kk * 2048, 64 * 128, 1024);
+            uint64_t ad, bd;
+            if constexpr (A_MN) ad = smem_desc_sw128(sa + kk * 2048, 64 * 128, 1024);
+            else ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            if constexpr (BM) bd = smem_desc_sw128(sb + kk * 2048, 64 * 128, 1024);
             else bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
             mma_bf16_f32_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
@@ -179,8 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     const bool leader = (warp == 2 && lane == 0);
     int it = 0;
     for (int tile = pair; tile < args.num_tiles; tile += npairs, ++it) {
-      const int m0 = (tile / ntn) * 256 + 128 * static_cast<int>(rank);
-      const int n0 = (tile % ntn) * 256;
+      const PairTile t = decode_pair<MODE>(tile, args, rank);
+      const int m0 = t.m0, n0 = t.n0;
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       const bool waited = mbar_wait(&tfull[acc], acc_phase, tmo, abort_flag);
@@ -198,6 +258,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         if (sl == 1) {  // accumulator fully read: release it to the MMA thread
           tc_fence_before();
           mbar_arrive_remote(dsmem_addr(&tempty[acc], 0));
+        }
+        if constexpr (MODE == PairMode::GradRed) {
+          // fp32 partial rows straight to global memory: local feature row
+          // t.row0 + row of super-block t.s, columns t.j * 256 + c0 ..
+          if (t.nk == 0) {  // no MMA wrote this accumulator (an empty split)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) r[0][q] = r[1][q] = 0u;
+          }
+          float* out = args.C + t.p * args.split_stride + static_cast<int64_t>(t.s) * args.sb * args.sb +
+                       static_cast<int64_t>(t.row0 + row) * args.sb + t.j * 256 + c0;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<uint4*>(out + 32 * hh)[q] =
+                  make_uint4(r[hh][4 * q], r[hh][4 * q + 1], r[hh][4 * q + 2], r[hh][4 * q + 3]);
+          continue;
         }
         if (leader) bulk_wait_read_all();
         named_barrier(1, 256);
@@ -222,7 +299,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         }
       }
     }
-    if (leader) bulk_wait_all();
+    if constexpr (MODE != PairMode::GradRed) {
+      if (leader) bulk_wait_all();
+    }
   }
 
   // every MMA of the pair must be complete before TMEM is freed

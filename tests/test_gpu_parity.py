@@ -148,6 +148,15 @@ def test_bf16_b512_ragged_block_and_b256(px):
     _case(px, 768, 512, 512, 256, 260, "bf16", recompute=True)
 
 
+@pytest.mark.parametrize("m,n,b,T", [(1280, 1024, 512, 700), (1024, 1536, 256, 333)])
+def test_bf16_wide_superblocks_on_cta_pairs(px, m, n, b, T):
+    # outputs of at least 1024 with 256- and 512-wide super-blocks: the block
+    # transforms (K = sb) and, at b = 512, the token reductions run on CTA
+    # pairs with 256 x 256 tiles; 1280 = 2 x 512 + 256 ends in a partial
+    # super-block
+    _case(px, m, n, b, b, T, "bf16", gstd=0.02, index=5)
+
+
 def test_bf16_ragged_superblock(px):
     # 1376 = 10 x 128 + 96: the last 128-wide super-block is partial
     _case(px, 1376, 512, 32, 32, 128, "bf16")
