@@ -433,14 +433,12 @@ poetx_status simt_gemm(cudaStream_t st, int M, int N, int K, int batch, const TA
   SimtGemmArgs g{M, N, K, batch, A, sAm, sAk, bsA, B, sBk, sBn, bsB, C, sCm, sCn, bsC, alpha, beta};
   if (M >= 128 && N >= 128) {
     dim3 grid((N + 127) / 128, (M + 127) / 128, batch);
-    simt_gemm128_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
-    POETX_LAUNCHED();
-    return POETX_OK;
+    return launch_dep(simt_gemm128_kernel<TA, TB, TC>, grid, 256, 0, st,
+                      int64_t(M) * N * batch * int64_t(sizeof(TC)), g);
   }
   dim3 grid((N + 63) / 64, (M + 63) / 64, batch);
-  simt_gemm_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
-  POETX_LAUNCHED();
-  return POETX_OK;
+  return launch_dep(simt_gemm_kernel<TA, TB, TC>, grid, 256, 0, st, int64_t(M) * N * batch * int64_t(sizeof(TC)),
+                    g);
 }
 
 template <typename T>
@@ -1268,21 +1266,19 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
     float* R = nsc;                          // R_0 .. R_k
     float* cur = nsc + (k + 1) * tstride;    // Horner accumulator
     float* nxt = t1;
-    copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(G, bb, b, R, bb, b, b, b, 1.f, 0.f);
-    POETX_LAUNCHED();
+    POETX_TRY(launch_dep(copy2d_kernel, dim3(grid_for(bb), nb), 256, 0, st, 0, G, bb, b, R, bb, b, b, b,
+                         1.f, 0.f));
     for (int c = 1; c <= k; ++c)  // R_c = R_{c-1} Qt
       POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, R + (c - 1) * tstride, b, 1, bb, Q,
                                                1, b, bb, R + c * tstride, b, 1, bb, 1.f, 0.f));
     auto coef = [&](int p) { return (p == 0 || p == k + 1) ? 1.f : 2.f; };
     for (int a = k; a >= 0; --a) {
       float* dst = (a == k) ? cur : nxt;  // T_a
-      copy2d_kernel<<<dim3(grid_for(bb), nb), 256, 0, st>>>(R, bb, b, dst, bb, b, b, b,
-                                                            coef(a + 1), 0.f);
-      POETX_LAUNCHED();
-      for (int c = 1; c <= k - a; ++c) {
-        axpy_kernel<<<grid_for(tstride), 256, 0, st>>>(dst, R + c * tstride, coef(a + c + 1), tstride);
-        POETX_LAUNCHED();
-      }
+      POETX_TRY(launch_dep(copy2d_kernel, dim3(grid_for(bb), nb), 256, 0, st, 0, R, bb, b, dst, bb, b, b, b,
+                           coef(a + 1), 0.f));
+      for (int c = 1; c <= k - a; ++c)
+        POETX_TRY(launch_dep(axpy_kernel, grid_for(tstride), 256, 0, st, 0, dst, R + c * tstride,
+                             coef(a + c + 1), tstride));
       if (a != k) {  // nxt = T_a + Qt cur
         POETX_TRY(dense_f32_gemm(tcg, st, b, b, b, nb, Q, 1, b, bb, cur, b, 1, bb, nxt, b,
                                                  1, bb, 1.f, 1.f));
@@ -1291,9 +1287,7 @@ poetx_status generator_backward(cudaStream_t st, const poetx_layer_desc& d, cons
     }
     GQ = cur;
   }
-  pack_grad_kernel<<<dim3(nb, (b + 7) / 8), 256, 0, st>>>(GQ, S.g, dGen, accumulate);
-  POETX_LAUNCHED();
-  return POETX_OK;
+  return launch_dep(pack_grad_kernel, dim3(nb, (b + 7) / 8), 256, 0, st, 0, GQ, S.g, dGen, accumulate);
 }
 
 }  // namespace
@@ -1734,14 +1728,12 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   // exact Cayley blocks of b <= 128: the generator backward runs fused per block
   // in bwd_common_tail; otherwise reduce the partials into G here.
   if (!fused_cayley_bwd_ok(c.d, R.g.b)) {
-    gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0, c.st>>>(
-        partR, strideR, c.slotsR, R.g, R.sb, c.w<float>(c.W.off_GR));
-    POETX_LAUNCHED();
+    POETX_TRY(launch_dep(gradred_reduce_kernel, grid_for(static_cast<int64_t>(R.g.nblk) * R.bb()), 256, 0,
+                         c.st, 0, partR, strideR, c.slotsR, R.g, R.sb, c.w<float>(c.W.off_GR)));
   }
   if (!fused_cayley_bwd_ok(c.d, P.g.b)) {
-    gradred_reduce_kernel<<<grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0, c.st>>>(
-        partP, strideP, c.slotsP, P.g, P.sb, c.w<float>(c.W.off_GP));
-    POETX_LAUNCHED();
+    POETX_TRY(launch_dep(gradred_reduce_kernel, grid_for(static_cast<int64_t>(P.g.nblk) * P.bb()), 256, 0,
+                         c.st, 0, partP, strideP, c.slotsP, P.g, P.sb, c.w<float>(c.W.off_GP)));
   }
   return POETX_OK;
 }

@@ -34,6 +34,7 @@ struct SimtGemmArgs {
 
 template <typename TA, typename TB, typename TC>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemmArgs g) {
+  griddep_enter();
   __shared__ __align__(16) float As[16][68];
   __shared__ __align__(16) float Bs[16][68];
   const int z = blockIdx.z;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemmArgs g) {
 // 64 FMAs cost four 16-byte shared loads.
 template <typename TA, typename TB, typename TC>
 __global__ void __launch_bounds__(256) simt_gemm128_kernel(const SimtGemmArgs g) {
+  griddep_enter();
   __shared__ __align__(16) float As[2][8][128];
   __shared__ __align__(16) float Bs[2][8][128];
   const int z = blockIdx.z;
@@ -758,6 +760,7 @@ __global__ void __launch_bounds__(1024) gj_invert128_kernel(const float* in, int
 __global__ void __launch_bounds__(256) copy2d_kernel(const float* src, int64_t s_bs, int s_ld,
                                                      float* dst, int64_t d_bs, int d_ld, int rows,
                                                      int cols, float alpha, float beta_eye) {
+  griddep_enter();
   const int z = blockIdx.y;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < rows * cols; e += gridDim.x * blockDim.x) {
     const int i = e / cols, j = e % cols;
@@ -770,6 +773,7 @@ __global__ void __launch_bounds__(256) copy2d_kernel(const float* src, int64_t s
 // dst[e] += alpha * src[e] for e < n.
 __global__ void __launch_bounds__(256) axpy_kernel(float* __restrict__ dst, const float* __restrict__ src,
                                                    float alpha, int64_t n) {
+  griddep_enter();
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < n;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x)
     dst[e] = fmaf(alpha, src[e], dst[e]);
