@@ -461,14 +461,19 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
     const int rb = static_cast<int>(std::max<size_t>(1, std::min<size_t>(32, (32 * 1024) / row_bytes)));
     const size_t psmem = 2 * rb * row_bytes + 64;
     if (row_bytes >= 4096 && psmem <= 200 * 1024) {
-      static cudaError_t attr_err = cudaFuncSetAttribute(
-          gather_rows_pipelined_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+      // the chunk indices of rows of up to 1024 (6 * 256 for wider rows)
+      // 16-byte chunks stay in registers
+      const bool wide = d / 8 > 4 * 256;
+      auto kern = wide ? gather_rows_pipelined_kernel<6> : gather_rows_pipelined_kernel<4>;
+      static cudaError_t attr4 = cudaFuncSetAttribute(
+          gather_rows_pipelined_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      static cudaError_t attr6 = cudaFuncSetAttribute(
+          gather_rows_pipelined_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (attr4 != cudaSuccess || attr6 != cudaSuccess) return POETX_ERR_CUDA;
       const int64_t nblocks = (rows + rb - 1) / rb;
       const int grid = static_cast<int>(std::min<int64_t>(nblocks, launch_sms() * 3));
-      return launch_dep(gather_rows_pipelined_kernel, grid, 256, psmem, st, rows * d * 2,
-                        reinterpret_cast<const uint16_t*>(in), reinterpret_cast<uint4*>(out), idx,
-                        rows, d, rb, g_timeout_ns);
+      return launch_dep(kern, grid, 256, psmem, st, rows * d * 2, reinterpret_cast<const uint16_t*>(in),
+                        reinterpret_cast<uint4*>(out), idx, rows, d, rb, g_timeout_ns);
     }
     // interleaved row pairs, about 32 KB staged per iteration (at least one pair)
     const int ppi = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (16 * 1024) / row_bytes)));

@@ -255,9 +255,10 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const T* __restrict__ 
 // gather block k from one shared buffer (random 2-byte reads, 16-byte
 // coalesced stores), block k + 1 is landing in the other.  Thread t always
 // produces the 16-byte output chunks t, t + 256, ... of a row, so it keeps
-// their indices in registers when a row has at most 4 * 256 chunks.
+// their indices in registers when a row has at most KREG * 256 chunks.
 // Waits are bounded; on a timeout the CTA records it and returns.
-__global__ void __launch_bounds__(256) gather_rows_pipelined_kernel(const uint16_t* __restrict__ in,
+template <int KREG>
+__global__ void __launch_bounds__(256, 3) gather_rows_pipelined_kernel(const uint16_t* __restrict__ in,
                                                                     uint4* __restrict__ out,
                                                                     const int32_t* __restrict__ idx,
                                                                     int64_t rows, int d, int rb,
@@ -293,7 +294,6 @@ __global__ void __launch_bounds__(256) gather_rows_pipelined_kernel(const uint16
     issue(1, 1);
   }
   // this thread's chunk indices
-  constexpr int KREG = 4;
   const bool in_regs = vpr <= KREG * 256;
   int4 ia[KREG], ib[KREG];
 #pragma unroll
