@@ -441,6 +441,13 @@ poetx_status simt_gemm(cudaStream_t st, int M, int N, int K, int batch, const TA
                     g);
 }
 
+// Narrowest bf16 rows (bytes) for which the pipelined gather takes several
+// rows per pass instead of the pair-interleaved kernel.  Measured on B300:
+// 2 KB rows (d1024 block) 1.33 -> 1.23 ms of gathers per step; at 1 KB rows
+// (LLaMA-60M, 8192 tokens) the pair-interleaved kernel stays faster (0.280
+// vs 0.299 ms per step).
+constexpr size_t kNarrowGatherMinBytes = 2048;
+
 template <typename T>
 poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* idx, int64_t rows,
                          int d) {
@@ -460,16 +467,21 @@ poetx_status gather_cols(cudaStream_t st, const T* in, T* out, const int32_t* id
     // of 48 KB by 2% at d = 2048 and 5% at d = 4096).
     const int rb = static_cast<int>(std::max<size_t>(1, std::min<size_t>(32, (32 * 1024) / row_bytes)));
     const size_t psmem = 2 * rb * row_bytes + 64;
-    if (row_bytes >= 4096 && psmem <= 200 * 1024) {
+    const int vpr = d / 8;
+    const bool narrow = row_bytes >= kNarrowGatherMinBytes && vpr < 256 && 256 % vpr == 0;
+    if ((row_bytes >= 4096 || narrow) && psmem <= 200 * 1024) {
       // the chunk indices of rows of up to 1024 (6 * 256 for wider rows)
       // 16-byte chunks stay in registers
-      const bool wide = d / 8 > 4 * 256;
-      auto kern = wide ? gather_rows_pipelined_kernel<6> : gather_rows_pipelined_kernel<4>;
+      const bool wide = vpr > 4 * 256;
+      auto kern = narrow ? gather_rows_pipelined_kernel<1, true>
+                         : (wide ? gather_rows_pipelined_kernel<6, false> : gather_rows_pipelined_kernel<4, false>);
+      static cudaError_t attr1 = cudaFuncSetAttribute(
+          gather_rows_pipelined_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       static cudaError_t attr4 = cudaFuncSetAttribute(
-          gather_rows_pipelined_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+          gather_rows_pipelined_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       static cudaError_t attr6 = cudaFuncSetAttribute(
-          gather_rows_pipelined_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (attr4 != cudaSuccess || attr6 != cudaSuccess) return POETX_ERR_CUDA;
+          gather_rows_pipelined_kernel<6, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (attr1 != cudaSuccess || attr4 != cudaSuccess || attr6 != cudaSuccess) return POETX_ERR_CUDA;
       const int64_t nblocks = (rows + rb - 1) / rb;
       const int grid = static_cast<int>(std::min<int64_t>(nblocks, launch_sms() * 3));
       return launch_dep(kern, grid, 256, psmem, st, rows * d * 2, reinterpret_cast<const uint16_t*>(in),

@@ -256,8 +256,11 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const T* __restrict__ 
 // coalesced stores), block k + 1 is landing in the other.  Thread t always
 // produces the 16-byte output chunks t, t + 256, ... of a row, so it keeps
 // their indices in registers when a row has at most KREG * 256 chunks.
+// NARROW (rows of fewer than 256 chunks that divide 256: d = 8, 16, ...,
+// 1024; KREG = 1) takes 256 / vpr rows at a time: thread t produces chunk
+// t % vpr of rows t / vpr, t / vpr + 256 / vpr, ... of the block.
 // Waits are bounded; on a timeout the CTA records it and returns.
-template <int KREG>
+template <int KREG, bool NARROW>
 __global__ void __launch_bounds__(256, 3) gather_rows_pipelined_kernel(const uint16_t* __restrict__ in,
                                                                     uint4* __restrict__ out,
                                                                     const int32_t* __restrict__ idx,
@@ -293,12 +296,14 @@ __global__ void __launch_bounds__(256, 3) gather_rows_pipelined_kernel(const uin
     issue(0, 0);
     issue(1, 1);
   }
-  // this thread's chunk indices
-  const bool in_regs = vpr <= KREG * 256;
+  // rows per pass (narrow rows) and this thread's chunk indices
+  static_assert(!NARROW || KREG == 1, "narrow rows: one chunk per thread");
+  const int rpp = NARROW ? 256 / vpr : 1;
+  const bool in_regs = NARROW || vpr <= KREG * 256;
   int4 ia[KREG], ib[KREG];
 #pragma unroll
   for (int q = 0; q < KREG; ++q) {
-    const int c = tid + 256 * q;
+    const int c = NARROW ? tid % vpr : tid + 256 * q;
     if (in_regs && c < vpr) {
       ia[q] = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c);
       ib[q] = __ldg(reinterpret_cast<const int4*>(idx) + 2 * c + 1);
@@ -318,7 +323,19 @@ __global__ void __launch_bounds__(256, 3) gather_rows_pipelined_kernel(const uin
     }
     const int nr = static_cast<int>(min(static_cast<int64_t>(rb), rows - b * rb));
     const uint16_t* buf = reinterpret_cast<const uint16_t*>(gsm + s * buf_bytes);
-    for (int r = 0; r < nr; ++r) {
+    if constexpr (NARROW) {
+      const int c = tid % vpr;
+      const int4 i0 = ia[0], i1 = ib[0];
+      for (int r = tid / vpr; r < nr; r += rpp) {
+        const uint16_t* row = buf + static_cast<size_t>(r) * d;
+        out[(b * rb + r) * static_cast<int64_t>(vpr) + c] =
+            make_uint4(row[i0.x] | (static_cast<uint32_t>(row[i0.y]) << 16),
+                       row[i0.z] | (static_cast<uint32_t>(row[i0.w]) << 16),
+                       row[i1.x] | (static_cast<uint32_t>(row[i1.y]) << 16),
+                       row[i1.z] | (static_cast<uint32_t>(row[i1.w]) << 16));
+      }
+    }
+    for (int r = 0; r < (NARROW ? 0 : nr); ++r) {
       const uint16_t* row = buf + static_cast<size_t>(r) * d;
       uint4* orow = out + (b * rb + r) * static_cast<int64_t>(vpr);
       if (in_regs) {
