@@ -20,6 +20,8 @@ sample on this host's cores.
 from __future__ import annotations
 
 import argparse
+import atexit
+import datetime
 import hashlib
 import json
 import tempfile
@@ -235,9 +237,12 @@ def measured_traffic(kind: str, workload: str, b: int):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi sampling every 20 ms, started ahead of the timed region (so
+    its start-up falls outside it); the summary keeps the samples whose
+    timestamps fall inside the region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int, log_path=None):
         """log_path: keep the raw samples there; default a temporary file,
@@ -257,12 +262,20 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            atexit.register(self._end)  # never outlive this process
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def _end(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
+
+    def stop(self, t0=None, t1=None):
+        """Ends sampling; summarises the samples taken between host times t0
+        and t1 (seconds since the epoch), widened by 0.1 s on each side when
+        the region is shorter than the sampling interval."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -272,7 +285,12 @@ class ClockSampler:
             self.proc.kill()
         self.fh.close()
         with open(self.path) as f:
-            summary = summarise_clock_samples(f)
+            lines = f.readlines()
+        summary = summarise_clock_samples(lines, t0, t1)
+        if summary is None and t0 is not None:
+            summary = summarise_clock_samples(lines, t0 - 0.1, t1 + 0.1)
+            if summary is not None:
+                summary["window"] = "timed region +- 0.1 s (shorter than the sampling interval)"
         if not self.keep:
             try:
                 os.remove(self.path)
@@ -281,12 +299,22 @@ class ClockSampler:
         return summary
 
 
-def summarise_clock_samples(lines):
+def sample_time(stamp: str):
+    """Seconds since the epoch of an nvidia-smi timestamp
+    ('YYYY/MM/DD HH:MM:SS.mmm', local time), or None."""
+    try:
+        return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return None
+
+
+def summarise_clock_samples(lines, t0=None, t1=None):
     """Median SM clock, maximum clock, sample count and the throttle reasons
     seen active, from `nvidia-smi --query-gpu=<ClockSampler.FIELDS>
     --format=csv,noheader,nounits` lines; None without a usable sample.
-    Lines that are not complete samples (a partial last line, [N/A] clocks)
-    are skipped."""
+    With t0 and t1 (seconds since the epoch) only samples whose timestamp
+    lies in [t0, t1] count.  Lines that are not complete samples (a partial
+    last line, [N/A] clocks) are skipped."""
     sm, smax, reasons = [], [], set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for line in lines:
@@ -297,6 +325,10 @@ def summarise_clock_samples(lines):
             clk, clk_max = float(parts[0]), float(parts[1])
         except ValueError:
             continue
+        if t0 is not None:
+            ts = sample_time(parts[8]) if len(parts) > 8 else None
+            if ts is None or ts < t0 or ts > t1:
+                continue
         sm.append(clk)
         smax.append(clk_max)
         for nm, v in zip(names, parts[4:8]):
@@ -615,11 +647,18 @@ def main():
         # overlap its builds and forwards); the timed region ends with drain_merges
         step_counter[0] += 1
 
+    # clock sampling starts before the warm-up, so that nvidia-smi's start-up
+    # lies outside the timed region; only samples inside it are summarised
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
+    clocks = ClockSampler(gpu_idx, args.clock_log)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     drain_merges(step_counter[0])
     torch.cuda.synchronize(dev)
     if px.poetx_device_status(reset=True) != px.POETX_OK:
+        clocks.stop()
         raise SystemExit("device status reported a timeout during warm-up")
 
     # (an optimizer step takes its step count from the host, so it stays eager)
@@ -644,13 +683,10 @@ def main():
     # per-launch timing events (about 1% of a d2048 step)
     px.poetx_profile_reset()
     px.poetx_profile_enable(False)
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    gpu_idx = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
-    clocks = ClockSampler(gpu_idx, args.clock_log)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    t_region0 = time.time()
     launches0 = px.poetx_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -662,9 +698,10 @@ def main():
     drain_merges(step_counter[0])   # the last timed step's merges
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    t_region1 = time.time()
     launches = (launches_per_step * args.steps if graph is not None
                 else px.poetx_launch_count() - launches0)
-    clk = clocks.stop()
+    clk = clocks.stop(t_region0, t_region1)
     # per-class device times (roofline) from as many steps with the library's
     # timing events, right after the timed region: replayed from a graph when
     # the timed steps are (the events become graph nodes, so the times hold

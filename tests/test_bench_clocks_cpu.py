@@ -40,3 +40,19 @@ def test_partial_and_unavailable_samples_are_skipped():
 def test_no_samples_gives_none():
     assert bench.summarise_clock_samples([]) is None
     assert bench.summarise_clock_samples(["garbage\n"]) is None
+
+
+def test_only_samples_inside_the_timed_region_count():
+    import datetime
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    def stamped(sm, dt_ms, cap="Not Active"):
+        t = base + datetime.timedelta(milliseconds=dt_ms)
+        return _line(sm, 2032, cap=cap).rstrip("\n") + ", " + t.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3] + "\n"
+    lines = [stamped(2032, 0), stamped(1500, 100, cap="Active"), stamped(1600, 120), stamped(1700, 140),
+             stamped(1000, 400, cap="Active")]
+    t0 = (base + datetime.timedelta(milliseconds=90)).timestamp()
+    t1 = (base + datetime.timedelta(milliseconds=150)).timestamp()
+    s = bench.summarise_clock_samples(lines, t0, t1)
+    # the idle sample before the region and the one after it are left out
+    assert s == {"sm_mhz": 1600.0, "sm_max_mhz": 2032.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    assert bench.summarise_clock_samples(lines, t1 + 1.0, t1 + 2.0) is None
