@@ -43,6 +43,70 @@ struct NeumannSide {
   __nv_bfloat16* BsbT;
 };
 
+// Converts 64 K values of `ROWS` rows of a row-major fp32 matrix (row r at
+// src + r * ld, K contiguous) into K-major 128-byte-swizzled bf16 hi / lo
+// tiles: 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).  Each of
+// the 256 converter threads issues all its loads before it converts any, so
+// the operand chunk costs one L2 round trip.
+template <int ROWS>
+__device__ __forceinline__ void nb_convert_kmajor(const float* src, int64_t ld, uint8_t* hi, uint8_t* lo,
+                                                  int t) {
+  constexpr int U = ROWS / 32;
+  float4 x[U], y[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = t + 256 * u, r = e / 8, c = e % 8;
+    const float* p = src + static_cast<int64_t>(r) * ld + 8 * c;
+    x[u] = __ldcg(reinterpret_cast<const float4*>(p));
+    y[u] = __ldcg(reinterpret_cast<const float4*>(p + 4));
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = t + 256 * u, r = e / 8, c = e % 8;
+    uint32_t h[4], l[4];
+    h[0] = split_bf16x2(x[u].x, x[u].y, l[0]);
+    h[1] = split_bf16x2(x[u].z, x[u].w, l[1]);
+    h[2] = split_bf16x2(y[u].x, y[u].y, l[2]);
+    h[3] = split_bf16x2(y[u].z, y[u].w, l[3]);
+    const int off = r * 128 + ((c ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// Converts 64 K rows of `COLS` consecutive columns of a row-major fp32
+// matrix (K row kk at src + kk * ld) into MN-major 128-byte-swizzled bf16
+// hi / lo tiles: atoms of 64 columns x 8 K rows, column chunk nc at
+// nc * 8 KB, K row kk at kk * 128, 16-byte chunk c at (c ^ (kk % 8)) * 16.
+// All loads of a thread are issued before any conversion, as above.
+template <int COLS>
+__device__ __forceinline__ void nb_convert_mnmajor(const float* src, int64_t ld, uint8_t* hi,
+                                                   uint8_t* lo, int t) {
+  constexpr int U = COLS / 32;
+  float4 x[U], y[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = t + 256 * u;
+    const int c = e % 8, nc = (e / 8) % (COLS / 64), kk = e / (COLS / 8);
+    const float* p = src + static_cast<int64_t>(kk) * ld + nc * 64 + 8 * c;
+    x[u] = __ldcg(reinterpret_cast<const float4*>(p));
+    y[u] = __ldcg(reinterpret_cast<const float4*>(p + 4));
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = t + 256 * u;
+    const int c = e % 8, nc = (e / 8) % (COLS / 64), kk = e / (COLS / 8);
+    uint32_t h[4], l[4];
+    h[0] = split_bf16x2(x[u].x, x[u].y, l[0]);
+    h[1] = split_bf16x2(x[u].z, x[u].w, l[1]);
+    h[2] = split_bf16x2(y[u].x, y[u].y, l[2]);
+    h[3] = split_bf16x2(y[u].z, y[u].w, l[3]);
+    const int off = nc * 8192 + kk * 128 + ((c ^ (kk & 7)) << 4);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
 template <int BS>
 struct NeuCfg {
   static constexpr int NT = BS < 256 ? BS : 256;     // tile columns
@@ -153,42 +217,10 @@ __global__ void __cluster_dims__(NeuCfg<BS>::C, 1, 1) __launch_bounds__(288, 1)
           uint8_t* al = ah + Cfg::A_BOX;
           uint8_t* bh = al + Cfg::A_BOX;
           uint8_t* bl = bh + Cfg::B_BOX;
-          // A = rows [row0, row0 + 128) of Q, K chunk kc: K-major, 16-byte
-          // chunk c of row r at r*128 + ((c ^ (r % 8)) * 16)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = t + 256 * u, r = e / 8, c = e % 8;
-            const float* src = Qk + static_cast<int64_t>(row0 + r) * BS + kc * 64 + 8 * c;
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-            const float4 y = __ldcg(reinterpret_cast<const float4*>(src + 4));
-            uint32_t h[4], l[4];
-            h[0] = split_bf16x2(x.x, x.y, l[0]);
-            h[1] = split_bf16x2(x.z, x.w, l[1]);
-            h[2] = split_bf16x2(y.x, y.y, l[2]);
-            h[3] = split_bf16x2(y.z, y.w, l[3]);
-            const int off = r * 128 + ((c ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(ah + off) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(al + off) = make_uint4(l[0], l[1], l[2], l[3]);
-          }
-          // B(n, kk) = S_s[kc*64 + kk][col0 + n]: MN-major, atoms of 64
-          // columns x 8 k rows; column chunk nc at nc * 8 KB, k row kk at
-          // kk*128, 16-byte chunk c at (c ^ (kk % 8)) * 16
-#pragma unroll
-          for (int u = 0; u < NT / 32; ++u) {
-            const int e = t + 256 * u;
-            const int c = e % 8, nc = (e / 8) % (NT / 64), kk = e / (NT / 8);
-            const float* src = Scur + static_cast<int64_t>(kc * 64 + kk) * BS + col0 + nc * 64 + 8 * c;
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-            const float4 y = __ldcg(reinterpret_cast<const float4*>(src + 4));
-            uint32_t h[4], l[4];
-            h[0] = split_bf16x2(x.x, x.y, l[0]);
-            h[1] = split_bf16x2(x.z, x.w, l[1]);
-            h[2] = split_bf16x2(y.x, y.y, l[2]);
-            h[3] = split_bf16x2(y.z, y.w, l[3]);
-            const int off = nc * 8192 + kk * 128 + ((c ^ (kk & 7)) << 4);
-            *reinterpret_cast<uint4*>(bh + off) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(bl + off) = make_uint4(l[0], l[1], l[2], l[3]);
-          }
+          // A = rows [row0, row0 + 128) of Q, K chunk kc (K-major); B(n, kk) =
+          // S_s[kc*64 + kk][col0 + n] (MN-major)
+          nb_convert_kmajor<128>(Qk + static_cast<int64_t>(row0) * BS + kc * 64, BS, ah, al, t);
+          nb_convert_mnmajor<NT>(Scur + static_cast<int64_t>(kc * 64) * BS + col0, BS, bh, bl, t);
           fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor cores
         }
         mbar_arrive(&cvt_full[buf]);

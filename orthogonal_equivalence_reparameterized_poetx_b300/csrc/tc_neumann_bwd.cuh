@@ -36,54 +36,6 @@ struct NeumannBwdSide {
   float* dGen;
 };
 
-// Converts 64 K values of `rows` rows of a row-major fp32 matrix (row r at
-// src + r * ld, K contiguous) into K-major 128-byte-swizzled bf16 hi / lo
-// tiles: 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16).
-template <int ROWS>
-__device__ __forceinline__ void nb_convert_kmajor(const float* src, int64_t ld, uint8_t* hi, uint8_t* lo,
-                                                  int t) {
-#pragma unroll
-  for (int u = 0; u < ROWS / 32; ++u) {
-    const int e = t + 256 * u, r = e / 8, c = e % 8;
-    const float* p = src + static_cast<int64_t>(r) * ld + 8 * c;
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(p));
-    const float4 y = __ldcg(reinterpret_cast<const float4*>(p + 4));
-    uint32_t h[4], l[4];
-    h[0] = split_bf16x2(x.x, x.y, l[0]);
-    h[1] = split_bf16x2(x.z, x.w, l[1]);
-    h[2] = split_bf16x2(y.x, y.y, l[2]);
-    h[3] = split_bf16x2(y.z, y.w, l[3]);
-    const int off = r * 128 + ((c ^ (r & 7)) << 4);
-    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
-// Converts 64 K rows of `COLS` consecutive columns of a row-major fp32
-// matrix (K row kk at src + kk * ld) into MN-major 128-byte-swizzled bf16
-// hi / lo tiles: atoms of 64 columns x 8 K rows, column chunk nc at
-// nc * 8 KB, K row kk at kk * 128, 16-byte chunk c at (c ^ (kk % 8)) * 16.
-template <int COLS>
-__device__ __forceinline__ void nb_convert_mnmajor(const float* src, int64_t ld, uint8_t* hi,
-                                                   uint8_t* lo, int t) {
-#pragma unroll
-  for (int u = 0; u < COLS / 32; ++u) {
-    const int e = t + 256 * u;
-    const int c = e % 8, nc = (e / 8) % (COLS / 64), kk = e / (COLS / 8);
-    const float* p = src + static_cast<int64_t>(kk) * ld + nc * 64 + 8 * c;
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(p));
-    const float4 y = __ldcg(reinterpret_cast<const float4*>(p + 4));
-    uint32_t h[4], l[4];
-    h[0] = split_bf16x2(x.x, x.y, l[0]);
-    h[1] = split_bf16x2(x.z, x.w, l[1]);
-    h[2] = split_bf16x2(y.x, y.y, l[2]);
-    h[3] = split_bf16x2(y.z, y.w, l[3]);
-    const int off = nc * 8192 + kk * 128 + ((c ^ (kk & 7)) << 4);
-    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
 template <int BS>
 __global__ void __cluster_dims__(NeuCfg<BS>::C, 1, 1) __launch_bounds__(288, 1)
     tc_neumann_bwd_kernel(const NeumannBwdSide first, const NeumannBwdSide second, int k,
