@@ -74,6 +74,9 @@ def parse():
                     help="override the workload's token count (small profiling cases only)")
     ap.add_argument("--clock-log", default=None,
                     help="keep the raw nvidia-smi clock samples of the timed region in this file")
+    ap.add_argument("--fused-gather-max", type=int, default=-1,
+                    help="widest side whose column permutation runs inside its block transform "
+                         "(0, the library's default: separate gather passes)")
     ap.add_argument("--builds-only", action="store_true",
                     help="time only the block builds (poetx_blocks_build) of each linear, "
                          "in isolation, and print one JSON line")
@@ -118,6 +121,17 @@ def r_in_gemm(b: int) -> bool:
 def p_in_dgrad(T: int, n: int, b: int) -> bool:
     pair = n >= 1024 and T >= 256
     return b <= 128 and (not pair or T * n * 2 <= (32 << 20))
+
+
+# Widest bf16 side (b <= 128) whose column permutation runs inside its block
+# transform: the forward X -> u -> v in one kernel and the backward dY -> dz
+# inside the R-side transform + reduction (off by default in the library; the
+# --fused-gather-max flag sets both).
+FUSED_GATHER_MAX = 0
+
+
+def gather_in_transform(wl, d: int, b: int) -> bool:
+    return wl.dtype == "bf16" and b <= 128 and -(-d // 128) <= 148 and 256 <= d <= FUSED_GATHER_MAX
 
 
 def gemm_flops_per_step(wl, kind: str, b: int = 0) -> float:
@@ -170,7 +184,10 @@ def kind_bytes_per_step(wl, b: int, kind: str) -> float:
     dgrad's epilogue; plus u -> v when recomputing.  gradred (sides whose
     reduction is not fused): dz^T h and dv^T u read two operands.  The fused
     kernels are used for b <= 128 and, when their grid fills the GPU, for
-    b = 256 (as the library decides).
+    b = 256 (as the library decides).  Where the permutation runs inside the
+    transform (gather_in_transform), X -> u -> v reads X once and writes u
+    and v (6 B per element instead of 4 + 4), and dY -> dz -> dh reads dY in
+    place of dz (the gather pass disappears).
     """
     T = wl.tokens
     e = 2 if wl.dtype == "bf16" else 4
@@ -191,11 +208,13 @@ def kind_bytes_per_step(wl, b: int, kind: str) -> float:
         fm, fn = fused(m), fused(n)
         pd = wl.dtype == "bf16" and p_in_dgrad(T, n, b)
         rg = wl.dtype == "bf16" and r_in_gemm(b)
+        gn, gm = gather_in_transform(wl, n, b), gather_in_transform(wl, m, b)
         if kind == "gather":
-            by += 2 * T * ((2 + r) * n + 2 * m) * e
+            by += 2 * T * ((1 if gn else 2 + r) * n + (1 if gm else 2) * m) * e
         elif kind == "blockdiag":
             bwd = (3 if fm else 2) * m + (0 if pd else (3 if fn else 2) * n)
-            by += T * (2 * n + (0 if rg else 2 * m) + bwd + 2 * n * r) * e
+            pfwd = 3 if gn else 2
+            by += T * (pfwd * n + (0 if rg else 2 * m) + bwd + pfwd * n * r) * e
         elif kind == "gradred":
             by += T * ((0 if fm else 2) * m + (0 if (fn or pd) else 2) * n) * e
     return float(by)
@@ -468,6 +487,10 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    px.poetx_set_fused_gather_max_features(args.fused_gather_max)
+    if args.fused_gather_max >= 0:
+        global FUSED_GATHER_MAX
+        FUSED_GATHER_MAX = args.fused_gather_max
     if args.builds_only:
         run_builds_only(args, wl, b, px, torch, dev)
         return

@@ -312,6 +312,21 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns);
  * CUDA graph keeps the setting it was captured with). */
 void poetx_set_dependent_launch(int32_t on);
 
+/* Column permutation inside the block transform ("POET-X: Memory-efficient
+ * LLM Training by Scaling Orthogonal Transformation", Methodologie §1-§2:
+ * the permutations are index maps applied to the input).  For bf16 layers
+ * with 128-wide super-blocks (b <= 128) whose permuted side has 256 to
+ * max_features features, the forward gathers X -> u inside the P-side block
+ * transform (one kernel writes u and v) and the backward gathers dY -> dz
+ * inside the R-side transform + token reduction (dz is never written);
+ * other sides run the separate gather pass.  Results are identical either
+ * way (same bf16 values, same fp32 accumulation order).  Off by default (0):
+ * on B300 the separate passes, launched as programmatic dependents from a
+ * CUDA graph, were as fast or faster at every width measured.  A negative
+ * value restores the default.  Applies to launches issued after the call (a
+ * captured graph keeps its setting). */
+void poetx_set_fused_gather_max_features(int32_t max_features);
+
 /* Forward for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers

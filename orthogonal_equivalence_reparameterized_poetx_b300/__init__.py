@@ -28,7 +28,8 @@ __all__ = [
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
     "poetx_linear_step_host", "poetx_linear_step_host_async", "poetx_device_status",
     "poetx_selftest_bounded_wait",
-    "poetx_set_wait_timeout_ns", "poetx_set_dependent_launch", "poetx_profile_enable",
+    "poetx_set_wait_timeout_ns", "poetx_set_dependent_launch",
+    "poetx_set_fused_gather_max_features", "poetx_profile_enable",
     "poetx_profile_reset", "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "KIND_NAMES", "Layer",
     "EXPORTED_SYMBOLS", "poetx_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -46,7 +47,8 @@ EXPORTED_SYMBOLS = [
     "poetx_linear_fwd", "poetx_linear_bwd", "poetx_merge_workspace_size", "poetx_merge",
     "poetx_linear_step_host", "poetx_linear_step_host_async", "poetx_device_status",
     "poetx_selftest_bounded_wait",
-    "poetx_set_wait_timeout_ns", "poetx_set_dependent_launch", "poetx_profile_enable",
+    "poetx_set_wait_timeout_ns", "poetx_set_dependent_launch",
+    "poetx_set_fused_gather_max_features", "poetx_profile_enable",
     "poetx_profile_reset", "poetx_profile_read", "poetx_profile_kind_name", "poetx_launch_count",
     "poetx_linear_fwd_noalloc",
     "poetx_weight_size", "poetx_blocks_build", "poetx_generator_adamw",
@@ -118,6 +120,7 @@ def _load():
         "poetx_selftest_bounded_wait": (I32, [U64, P]),
         "poetx_set_wait_timeout_ns": (V, [U64]),
         "poetx_set_dependent_launch": (V, [I32]),
+        "poetx_set_fused_gather_max_features": (V, [I32]),
         "poetx_profile_enable": (V, [I32]),
         "poetx_profile_reset": (V, []),
         "poetx_profile_read": (I32, [I32, ctypes.POINTER(ctypes.c_int64),
@@ -285,6 +288,12 @@ def poetx_set_wait_timeout_ns(timeout_ns: int):
 def poetx_set_dependent_launch(on: bool = True):
     """Programmatic dependent launch of the pass kernels (on by default)."""
     LIB.poetx_set_dependent_launch(1 if on else 0)
+
+
+def poetx_set_fused_gather_max_features(max_features: int = -1):
+    """Column permutation inside the block transform for bf16 sides of 256
+    to `max_features` features (0: off, the default; negative: the default)."""
+    LIB.poetx_set_fused_gather_max_features(int(max_features))
 
 
 def poetx_profile_enable(on: bool = True):

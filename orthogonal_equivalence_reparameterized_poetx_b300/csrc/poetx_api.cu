@@ -28,6 +28,7 @@
 #include "tc_gemm.cuh"
 #include "tc_bdgr.cuh"
 #include "tc_bdgr256.cuh"
+#include "tc_gbd.cuh"
 #include "tc_merge.cuh"
 #include "tc_f32gemm.cuh"
 #include "tc_gemm2.cuh"
@@ -558,6 +559,23 @@ poetx_status tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
   return r == CUDA_SUCCESS ? POETX_OK : POETX_ERR_CUDA;
 }
 
+// Row-major bf16 matrix [rows][cols] staged as unswizzled boxes of 256
+// columns x box_rows rows (zero fill out of bounds).
+poetx_status tmap_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                            uint32_t box_rows) {
+  PFN_encodeTiled enc = get_encode_fn();
+  if (!enc) return POETX_ERR_CUDA;
+  if (!aligned(base, 16) || (cols * 2) % 16 != 0) return POETX_ERR_MISALIGNED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {256, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? POETX_OK : POETX_ERR_CUDA;
+}
+
 template <int BN, bool A_MN, bool B_MN, TileMode MODE, typename OutT>
 poetx_status launch_tc(cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& tc, TcGemmArgs args) {
@@ -891,6 +909,72 @@ poetx_status tc_bdgr(cudaStream_t st, const SideLayout& S, const void* in, const
   if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
   POETX_TRY(launch_dep(tc_bdgr_kernel, a.nslots * S.nsb, 320, BdgrCfg::SMEM, st, int64_t(a.M) * a.N * 2, ta, tsb, tc, to, a));
   *slots += a.nslots;
+  return POETX_OK;
+}
+
+// Column permutation fused into the block transform (tc_gbd.cuh): sides of
+// 256 to g_gbd_max_cols features, 128-wide super-blocks; off by default.
+// Every CTA of a token tile stages its whole rows to use 128 of their
+// columns, so the staged bytes grow with d while the launch it saves is a
+// fixed cost.  Measured on B300 (20-step means, two runs each, same box):
+// LLaMA-60M-shaped block 0.538 ms per step with the 512-wide sides fused and
+// 0.576 with every side up to 1536 fused, against 0.534 with the separate
+// passes; d1024 block 4.35 against 3.96 ms.  The fused kernels' own time is
+// below that of the two kernels they replace (LLaMA-60M: about 50 us per
+// step less in the library's per-class events), but in the graph-replayed,
+// dependent-launched step the light gather kernels overlap their neighbours
+// and nothing is gained.
+constexpr int kGbdDefaultMaxCols = 0;
+std::atomic<int> g_gbd_max_cols{kGbdDefaultMaxCols};
+
+bool gbd_ok(const SideLayout& S) {
+  return S.sb == 128 && S.nsb <= launch_sms() && S.g.d >= 256 &&
+         S.g.d <= g_gbd_max_cols.load(std::memory_order_relaxed);
+}
+
+// A = src[:, perm]; out = A S^T per super-block; with REDUCE also the partial
+// slots of A^T C (appended at *slots); a_out (may be null) receives A.
+template <bool REDUCE>
+poetx_status tc_gather_bd(cudaStream_t st, const SideLayout& S, const __nv_bfloat16* src,
+                          const int32_t* perm, const void* Ssb, void* out, void* a_out, const void* Cm,
+                          float* partial, int64_t T, int* slots) {
+  if (T <= 0) return POETX_OK;
+  ProfScope prof(POETX_KIND_BLOCKDIAG, st);
+  using Cfg = GbdCfg<REDUCE>;
+  const int d = S.g.d;
+  GbdArgs a{};
+  a.M = static_cast<int>(T);
+  a.N = d;
+  a.nsb = S.nsb;
+  a.nslots = std::max(1, launch_sms() / S.nsb);
+  a.b = S.g.b;
+  // staged chunks: a power of two of rows (so a chunk never straddles two
+  // token tiles), as large as lets two chunks be in flight, and up to four
+  a.nbox = (d + 255) / 256;
+  const int row_bytes = a.nbox * 512;
+  a.chunk_rows = 128;
+  while (a.chunk_rows > 1 && 2 * a.chunk_rows * row_bytes > Cfg::STG_BYTES) a.chunk_rows /= 2;
+  if (2 * a.chunk_rows * row_bytes > Cfg::STG_BYTES || d % 8 != 0) return POETX_ERR_UNSUPPORTED;
+  a.nstg = std::min(Cfg::MAX_SLOTS, Cfg::STG_BYTES / (a.chunk_rows * row_bytes));
+  a.store_a = a_out != nullptr;
+  a.perm = perm;
+  a.partial = partial;
+  a.timeout_ns = g_timeout_ns;
+  CUtensorMap tx, ts, tc, to, ta;
+  POETX_TRY(tmap_bf16_rows(&tx, src, T, d, a.chunk_rows));
+  POETX_TRY(tmap_bf16(&ts, Ssb, static_cast<uint64_t>(S.nsb) * 128, 128, 128, 128));
+  POETX_TRY(tmap_bf16(&tc, REDUCE ? Cm : out, T, d, d, 128));
+  POETX_TRY(tmap_bf16(&to, out, T, d, d, 128));
+  POETX_TRY(tmap_bf16(&ta, a_out ? a_out : out, T, d, d, 128));
+  auto kern = tc_gbd_kernel<REDUCE>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  });
+  if (attr_err != cudaSuccess) return POETX_ERR_CUDA;
+  POETX_TRY(launch_dep(kern, a.nslots * S.nsb, Cfg::THREADS, Cfg::SMEM, st, T * d * 2, tx, ts, tc, to, ta, a));
+  if (REDUCE) *slots += a.nslots;
   return POETX_OK;
 }
 
@@ -1473,8 +1557,13 @@ poetx_status fwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   auto* h = hs ? hs : c.w<__nv_bfloat16>(c.W.off_m1);
   auto* z = c.w<__nv_bfloat16>(c.W.off_m2);
   const SideLayout &R = c.L.R, &P = c.L.P;
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
-  POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
+  if (gbd_ok(P)) {  // u and v from one kernel (u is kept for the backward)
+    POETX_TRY(tc_gather_bd<false>(c.st, P, X, c.piP(), c.p<__nv_bfloat16>(P.off_Bsb), v, u, nullptr,
+                                  nullptr, T, nullptr));
+  } else {
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, u, c.piP(), T, n));
+    POETX_TRY(tc_blockdiag(c.st, u, c.p<__nv_bfloat16>(P.off_Bsb), v, T, n, P.sb, P.nsb));
+  }
   if (r_epilogue(R, T, m)) {
     POETX_TRY(tc_dense_nt_r(c.st, v, W0p, c.p<__nv_bfloat16>(R.off_Bsb), hs, z, T, m, n, R.nsb));
   } else if (pair_r_epilogue(R, T, m)) {
@@ -1703,19 +1792,25 @@ poetx_status bwd_bf16(const Ctx& c, const __nv_bfloat16* W0p, const __nv_bfloat1
   c.slotsR = c.slotsP = 0;
 
   // u (when not kept), and in recompute mode v and h
-  if (!us) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
-  if (recompute) {
-    POETX_TRY(tc_blockdiag(c.st, u, BsbP, v, T, n, P.sb, P.nsb));
-    POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
+  if (!us && recompute && gbd_ok(P)) {  // u and v from one kernel
+    POETX_TRY(tc_gather_bd<false>(c.st, P, X, c.piP(), BsbP, v, ubuf, nullptr, nullptr, T, nullptr));
+  } else {
+    if (!us) POETX_TRY(gather_cols<__nv_bfloat16>(c.st, X, ubuf, c.piP(), T, n));
+    if (recompute) POETX_TRY(tc_blockdiag(c.st, u, BsbP, v, T, n, P.sb, P.nsb));
   }
+  if (recompute) POETX_TRY(tc_dense_nt(c.st, v, W0p, hbuf, T, m, n));
 
   // R side: dz, dh and the dz^T h partials
-  POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
-  if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
+  if (gbd_ok(R)) {  // dz = dY[:, pi_R] gathered inside the fused transform + reduction
+    POETX_TRY(tc_gather_bd<true>(c.st, R, dY, c.piR(), BsbRT, dh, nullptr, h, partR, T, &c.slotsR));
+  } else if (bdgr_ok(R)) {  // dh = dz B_R and the dz^T h partials from one read of dz
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
     POETX_TRY(tc_bdgr(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
   } else if (bdgr256_ok(R)) {
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
     POETX_TRY(tc_bdgr256(c.st, R, dz, BsbRT, dh, h, partR, T, &c.slotsR));
   } else {
+    POETX_TRY(gather_cols<__nv_bfloat16>(c.st, dY, dz, c.piR(), T, m));
     POETX_TRY(tc_blockdiag(c.st, dz, BsbRT, dh, T, m, R.sb, R.nsb));
     POETX_TRY(tc_gradred(c.st, R, dz, h, partR, T, &c.slotsR));
   }
@@ -2324,6 +2419,10 @@ void poetx_set_wait_timeout_ns(uint64_t timeout_ns) {
 
 void poetx_set_dependent_launch(int32_t on) {
   g_dependent_launch.store(on != 0, std::memory_order_relaxed);
+}
+
+void poetx_set_fused_gather_max_features(int32_t max_features) {
+  g_gbd_max_cols.store(max_features < 0 ? kGbdDefaultMaxCols : max_features, std::memory_order_relaxed);
 }
 
 }  // extern "C"

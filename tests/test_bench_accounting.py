@@ -93,6 +93,17 @@ def test_epilogue_placement_follows_the_library():
     sum_n = 6 * 512 + 1376
     sum_m = 4 * 512 + 2 * 1376 + 512
     assert bench.kind_bytes_per_step(wl, 32, "blockdiag") == 2 * t * (2 * sum_n + 3 * sum_m)
+    assert bench.kind_bytes_per_step(wl, 32, "gather") == 8 * t * (sum_n + sum_m)
+    # with the permutations inside the transforms (bound 1536) the forward
+    # X -> u -> v moves 6 B and the R backward gathers dY itself; the gather
+    # class keeps z -> Y and du -> dX
+    old = bench.FUSED_GATHER_MAX
+    try:
+        bench.FUSED_GATHER_MAX = 1536
+        assert bench.kind_bytes_per_step(wl, 32, "blockdiag") == 2 * t * (3 * sum_n + 3 * sum_m)
+        assert bench.kind_bytes_per_step(wl, 32, "gather") == 4 * t * (sum_n + sum_m)
+    finally:
+        bench.FUSED_GATHER_MAX = old
     # and the dgrad class carries the transform and reduction flops, 4 T sum b_P^2
     sq = lambda d: bench.block_square_sum(d, 32)
     extra = 4 * t * (6 * sq(512) + sq(1376))
@@ -113,3 +124,45 @@ def test_unfused_256_sides_are_counted_as_transform_plus_reduction():
     per = lambda nn, mm, fm, fn: T * (2 * nn + 2 * mm + (3 if fm else 2) * mm + (3 if fn else 2) * nn
                                       + 2 * nn) * 2
     assert bd == per(n, m, False, True) + per(m, n, True, False)
+
+
+def test_gather_inside_the_transform_for_narrow_sides():
+    # off by default; with the bound at 1536: bf16 sides of 256 to 1536
+    # features, b <= 128
+    wl = synth.WORKLOADS["d1024_block"]
+    assert not bench.gather_in_transform(wl, 1024, 64)
+    old = bench.FUSED_GATHER_MAX
+    bench.FUSED_GATHER_MAX = 1536
+    try:
+        _check_d1024_fused_accounting(wl)
+    finally:
+        bench.FUSED_GATHER_MAX = old
+
+
+def _check_d1024_fused_accounting(wl):
+    assert bench.gather_in_transform(wl, 1024, 64) and bench.gather_in_transform(wl, 1536, 128)
+    assert not bench.gather_in_transform(wl, 2816, 64)
+    assert not bench.gather_in_transform(wl, 1024, 256)
+    assert not bench.gather_in_transform(synth.WORKLOADS["fp32_256"], 256, 32)
+    assert not bench.gather_in_transform(wl, 200, 64)
+    # d1024 (recompute, T = 32768): P sides of 1024 gather X -> u inside the
+    # forward and the recompute transform (6 B each), down's 2816-wide P side
+    # keeps its passes; R sides of 1024 gather dY inside the backward transform
+    t = wl.tokens
+    n_f = 6 * 1024             # fused P sides (q, k, v, o, gate, up)
+    n_s = 2816                 # separate P side (down)
+    m_f = 4 * 1024 + 1024      # fused R sides (q, k, v, o, down)
+    m_s = 2 * 2816             # separate R sides (gate, up)
+    assert bench.kind_bytes_per_step(wl, 64, "gather") == 4 * t * (n_f + 3 * n_s + m_f + 2 * m_s)
+    pd = lambda n: bench.p_in_dgrad(t, n, 64)
+    assert not pd(1024) and not pd(2816)
+    # blockdiag: fwd P (6 or 4 B), R in the GEMM, bwd R (6 B) and P (6 B), recompute P (6 or 4 B)
+    want = 2 * t * (3 * n_f + 2 * n_s + 3 * (m_f + m_s) + 3 * (n_f + n_s) + 3 * n_f + 2 * n_s)
+    assert bench.kind_bytes_per_step(wl, 64, "blockdiag") == want
+    # with the bound at 0 every side keeps its gather passes
+    old = bench.FUSED_GATHER_MAX
+    try:
+        bench.FUSED_GATHER_MAX = 0
+        assert bench.kind_bytes_per_step(wl, 64, "gather") == 4 * t * (3 * (n_f + n_s) + 2 * (m_f + m_s))
+    finally:
+        bench.FUSED_GATHER_MAX = old
