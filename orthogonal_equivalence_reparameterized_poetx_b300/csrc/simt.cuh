@@ -286,11 +286,9 @@ __global__ void __launch_bounds__(256, 3) gather_rows_pipelined_kernel(const uin
     if (b >= nblocks) return;
     const int nr = static_cast<int>(min(static_cast<int64_t>(rb), rows - b * rb));
     const uint32_t rowb = static_cast<uint32_t>(d) * 2;
+    // the block's rows are contiguous in memory: one copy for all of them
     mbar_arrive_expect_tx(&full[s], rowb * nr);
-    uint8_t* dst = gsm + s * buf_bytes;
-    for (int r = 0; r < nr; ++r)
-      bulk_load(dst + static_cast<size_t>(r) * rowb, in + (b * rb + r) * static_cast<int64_t>(d), rowb,
-                &full[s]);
+    bulk_load(gsm + s * buf_bytes, in + b * rb * static_cast<int64_t>(d), rowb * nr, &full[s]);
   };
   if (tid == 0) {
     issue(0, 0);
