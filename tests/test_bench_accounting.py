@@ -166,3 +166,18 @@ def _check_d1024_fused_accounting(wl):
         assert bench.kind_bytes_per_step(wl, 64, "gather") == 4 * t * (3 * (n_f + n_s) + 2 * (m_f + m_s))
     finally:
         bench.FUSED_GATHER_MAX = old
+
+
+def test_concurrent_groups_follow_the_block_structure():
+    # q, k, v and gate, up read the same block input; o and down stand alone
+    assert bench.concurrent_groups(synth.WORKLOADS["llama60m_block"]) == [[0, 1, 2], [3], [4, 5], [6]]
+    assert bench.concurrent_groups(synth.WORKLOADS["d2048_block"]) == [[0, 1, 2], [3], [4, 5], [6]]
+    assert bench.concurrent_groups(synth.WORKLOADS["d4096_ffn"]) == [[0], [1]]
+    assert bench.concurrent_groups(synth.WORKLOADS["fp32_256"]) == [[0]]
+
+    class A:
+        mode, weight, optimizer, gpus, graph, concurrent = "cayley", "dense", "none", 1, "auto", "on"
+    wl = synth.WORKLOADS["llama60m_block"]
+    assert bench.workload_config(wl, 32, A)["linear_order"] == "q|k|v o gate|up down"
+    A.concurrent = "off"
+    assert bench.workload_config(wl, 32, A)["linear_order"] == "q k v o gate up down"

@@ -35,6 +35,6 @@ def test_reference_arm_prints_one_contract_line():
     wl = synth.WORKLOADS["llama60m_block"]
 
     class A:  # the arguments above, with the defaults of the other options
-        mode, weight, optimizer, gpus, graph = "cayley", "dense", "none", 1, "auto"
+        mode, weight, optimizer, gpus, graph, concurrent = "cayley", "dense", "none", 1, "auto", "on"
     assert line["config"] == bench.workload_config(wl, wl.block_sizes[0], A)
     assert line["config"]["cuda_graph"] is True
