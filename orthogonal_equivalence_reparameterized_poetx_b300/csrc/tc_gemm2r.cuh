@@ -6,21 +6,27 @@
 //                               each of the tile's two super-blocks
 // ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
 // Transformation", Methodologie §1 and §3).  The main loop is the one of
-// tc_gemm_pair_kernel with B K-major and four stages.  Each CTA rounds its
-// 128 accumulator rows of h to bf16 into a 128 x 256 swizzled shared tile,
+// tc_gemm_pair_kernel with B K-major and five stages.  The epilogue runs the
+// tile's two super-blocks in turn: each CTA rounds its 128 accumulator rows
+// of one super-block of h to bf16 into a 128 x 128 swizzled shared tile,
 // which is the TMA-store source of h (when h is kept) and, in both CTAs at
 // the same offset, the A operand of the transform; each CTA also loads its
 // 64-row half of both super-block matrices (the B operand split of an M =
 // 256, N = 128 pair MMA).  The even CTA's epilogue leader issues the
-// transform MMAs into the tile's own accumulator (both CTAs have read h from
-// it by then), so no TMEM beyond the two 256-column accumulators is needed;
-// the accumulator goes back to the main loop once z has been read.
+// super-block's transform MMAs into its own accumulator columns (both CTAs
+// have read h from them by then), so no TMEM beyond the two 256-column
+// accumulators is needed; z goes out through the same shared tile, and the
+// accumulator goes back to the main loop once both halves of z are read.
+// Staging one super-block at a time (32 KB instead of 64) leaves room for
+// the fifth main-loop stage.
 //
 // Warps (both CTAs): 0 TMA producer, 1 TMEM allocator (even CTA: main-loop
 // MMA issuer), 2..9 epilogue.  Barriers beyond the pair GEMM's:
 //   s_full    each CTA's: its super-block halves of the current tile landed
 //   hstaged   even CTA's: both CTAs' h tiles are staged and S halves landed
-//   zdone     each CTA's: the transform MMAs are complete (multicast commit)
+//             (twice per tile, once per super-block)
+//   zdone     each CTA's: a super-block's transform MMAs are complete
+//             (multicast commit; twice per tile)
 //   zdrain    even CTA's: every transform MMA is complete (before TMEM is freed)
 // Every wait is bounded; on a timeout a CTA records it and winds down, and
 // the pair meets at a cluster barrier before freeing TMEM and exiting.
@@ -40,8 +46,8 @@ struct TcPairRArgs {
 struct TcPairRCfg {
   static constexpr int BOX = 128 * 64 * 2;     // 128 rows x 64 bf16 (16 KB)
   static constexpr int STAGE_BYTES = 2 * BOX;  // this CTA's A rows and B columns of one K step
-  static constexpr int STAGES = 4;
-  static constexpr int HZ_BYTES = 4 * BOX;     // 128 rows x 256 features
+  static constexpr int STAGES = 5;
+  static constexpr int HZ_BYTES = 2 * BOX;     // 128 rows x 128 features (one super-block)
   static constexpr int SBOX = 64 * 64 * 2;     // 64 rows x 64 bf16 (8 KB)
   static constexpr int S_BYTES = 4 * SBOX;     // two super-blocks x (64 rows x 128)
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + HZ_BYTES + S_BYTES + 256;
@@ -194,14 +200,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       ++s_loads;
     };
     // fp32 accumulator columns [sl * 128 + half * 64, + 64) of this thread's row
-    // to bf16 into box 2 * sl + half of the swizzled tile
+    // to bf16 into box `half` of the swizzled tile
     auto tmem_to_tile = [&](uint32_t base, int sl) {
       uint32_t r[2][32];
       const uint32_t c = base + sl * 128 + half * 64;
       tmem_ld_32x32b_x32(c, r[0]);
       tmem_ld_32x32b_x32(c + 32, r[1]);
       tmem_ld_wait();
-      uint8_t* box = hz_tile + (2 * sl + half) * Cfg::BOX;
+      uint8_t* box = hz_tile + half * Cfg::BOX;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t* src = r[q >> 2] + (q & 3) * 8;
@@ -213,14 +219,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         *reinterpret_cast<uint4*>(box + row * 128 + ((q ^ (row & 7)) << 4)) = v;
       }
     };
-    auto store_tile = [&](const CUtensorMap* map, int n0, int m0) {
-      if (m0 >= args.M) return;
-#pragma unroll
-      for (int sl = 0; sl < 2; ++sl) {
-        const int x = n0 + sl * 128;
-        if (x < args.N) tma_store_2d(map, hz_tile + (2 * sl) * Cfg::BOX, x, m0);
-        if (x + 64 < args.N) tma_store_2d(map, hz_tile + (2 * sl + 1) * Cfg::BOX, x + 64, m0);
-      }
+    // the staged super-block (features [x, x + 128)) to global memory
+    auto store_tile = [&](const CUtensorMap* map, int x, int m0) {
+      if (m0 >= args.M || x >= args.N) return;
+      tma_store_2d(map, hz_tile, x, m0);
+      if (x + 64 < args.N) tma_store_2d(map, hz_tile + Cfg::BOX, x + 64, m0);
       bulk_commit();
     };
     if (leader && pair < args.num_tiles) load_s(pair);
@@ -235,60 +238,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       if (named_barrier_any(1, 256, !waited)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(g * 32) << 16);
-      if (leader) bulk_wait_read_all();  // the previous tile's z store has read the tile
-      named_barrier(1, 256);
-      tmem_to_tile(taddr, 0);
-      tmem_to_tile(taddr, 1);
-      tc_fence_before();
-      fence_proxy_async_smem();
-      named_barrier(1, 256);
-      bool fail = false;
-      if (leader) {
-        if (args.store_h) store_tile(&tmH, n0, m0);
-        fail = !mbar_wait(s_full, static_cast<uint32_t>(s_landed & 1), tmo, abort_flag);
-        if (!fail) {
-          ++s_landed;
-          mbar_arrive_remote(dsmem_addr(hstaged, 0));
-        }
-        if (!fail && rank == 0) {
-          fail = !mbar_wait(hstaged, static_cast<uint32_t>(it & 1), tmo, abort_flag);
-          if (!fail) {
-            tc_fence_after();
-            constexpr uint32_t idesc_r = idesc_bf16_f32(256, 128, false, false);  // h S^T
-            const uint32_t sa = smem_u32(hz_tile), ss = smem_u32(s_tile);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint32_t d = tmem_base + acc * 256 + j * 128;
+      bool quit = false;
+#pragma unroll 1
+      for (int sl = 0; sl < 2 && !quit; ++sl) {
+        // round sl: super-block sl of the tile (features n0 + 128 sl ...)
+        const int x = n0 + sl * 128;
+        if (leader) bulk_wait_read_all();  // the previous z store has read the tile
+        named_barrier(1, 256);
+        tmem_to_tile(taddr, sl);
+        tc_fence_before();
+        fence_proxy_async_smem();
+        named_barrier(1, 256);
+        bool fail = false;
+        if (leader) {
+          if (args.store_h) store_tile(&tmH, x, m0);
+          if (sl == 0) {
+            fail = !mbar_wait(s_full, static_cast<uint32_t>(s_landed & 1), tmo, abort_flag);
+            if (!fail) ++s_landed;
+          }
+          if (!fail) mbar_arrive_remote(dsmem_addr(hstaged, 0));
+          if (!fail && rank == 0) {
+            // hstaged and zdone complete twice per tile: round sl is phase sl
+            fail = !mbar_wait(hstaged, static_cast<uint32_t>(sl), tmo, abort_flag);
+            if (!fail) {
+              tc_fence_after();
+              constexpr uint32_t idesc_r = idesc_bf16_f32(256, 128, false, false);  // h S^T
+              const uint32_t sa = smem_u32(hz_tile), ss = smem_u32(s_tile);
+              const uint32_t d = tmem_base + acc * 256 + sl * 128;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a_off = (2 * j + (kk >> 2)) * Cfg::BOX + (kk & 3) * 32;
-                const uint32_t b_off = (2 * j + (kk >> 2)) * Cfg::SBOX + (kk & 3) * 32;
+                const uint32_t a_off = (kk >> 2) * Cfg::BOX + (kk & 3) * 32;
+                const uint32_t b_off = (2 * sl + (kk >> 2)) * Cfg::SBOX + (kk & 3) * 32;
                 mma_bf16_f32_pair(d, smem_desc_sw128(sa + a_off, 16, 1024),
                                   smem_desc_sw128(ss + b_off, 16, 1024), idesc_r, kk != 0 ? 1u : 0u);
               }
+              mma_commit_pair(zdone, 0x3);
             }
-            mma_commit_pair(zdone, 0x3);
           }
         }
+        if (named_barrier_any(1, 256, fail)) { quit = true; break; }
+        const bool zok = mbar_wait(zdone, static_cast<uint32_t>(sl), tmo, abort_flag);
+        if (named_barrier_any(1, 256, !zok)) { quit = true; break; }
+        tc_fence_after();
+        if (leader) bulk_wait_read_all();  // the h store has read the tile
+        named_barrier(1, 256);
+        tmem_to_tile(taddr, sl);
+        tc_fence_before();
+        // both halves of z are read: the accumulator is free
+        if (sl == 1) mbar_arrive_remote(dsmem_addr(&tempty[acc], 0));
+        fence_proxy_async_smem();
+        named_barrier(1, 256);
+        if (leader) {
+          store_tile(&tmZ, x, m0);
+          // the tile's transform MMAs are complete: the next tile's S halves may land
+          const int next = tile + npairs;
+          if (sl == 1 && next < args.num_tiles) load_s(next);
+        }
       }
-      if (named_barrier_any(1, 256, fail)) break;
-      const bool zok = mbar_wait(zdone, static_cast<uint32_t>(it & 1), tmo, abort_flag);
-      if (named_barrier_any(1, 256, !zok)) break;
-      tc_fence_after();
-      if (leader) bulk_wait_read_all();  // the h store has read the tile
-      named_barrier(1, 256);
-      tmem_to_tile(taddr, 0);
-      tmem_to_tile(taddr, 1);
-      tc_fence_before();
-      mbar_arrive_remote(dsmem_addr(&tempty[acc], 0));  // z is read: the accumulator is free
-      fence_proxy_async_smem();
-      named_barrier(1, 256);
-      if (leader) {
-        store_tile(&tmZ, n0, m0);
-        // the transform MMAs are complete: the next tile's S halves may land
-        const int next = tile + npairs;
-        if (next < args.num_tiles) load_s(next);
-      }
+      if (quit) break;
     }
     if (leader) {
       bulk_wait_all();
