@@ -181,3 +181,15 @@ def test_concurrent_groups_follow_the_block_structure():
     assert bench.workload_config(wl, 32, A)["linear_order"] == "q|k|v o gate|up down"
     A.concurrent = "off"
     assert bench.workload_config(wl, 32, A)["linear_order"] == "q k v o gate up down"
+
+
+@pytest.mark.parametrize("key", ["llama60m_block", "d1024_block", "d2048_block", "d4096_ffn"])
+@pytest.mark.parametrize("b", [32, 64, 128, 256, 512])
+def test_class_flops_partition_the_step_flops(key, b):
+    # the GEMM classes (with the transforms in their epilogues), the block
+    # transforms and the separate reductions together are the step's
+    # algorithmic flops, whatever the placement rules decide
+    wl = synth.WORKLOADS[key]
+    parts = sum(bench.kind_flops_per_step(wl, b, k)
+                for k in ("gemm_fwd", "gemm_dgrad", "blockdiag", "gradred"))
+    assert parts == pytest.approx(bench.step_flops(wl, b), rel=1e-12)
