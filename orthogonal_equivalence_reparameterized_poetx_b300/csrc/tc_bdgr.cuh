@@ -16,8 +16,11 @@
 // accumulates in TMEM over all its tiles and is written once as partial
 // `slot` of super-block s (layout [slot][s][128][128] fp32).
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 epilogue.
-// Stage: A tile (128 tokens x 128 features), S tile (128 x 128), C tile,
-// each as two 64-column boxes with 128-byte swizzle: 96 KB, two stages.
+// Stage: A tile (128 tokens x 128 features) and C tile, each as two 64-column
+// boxes with 128-byte swizzle: 64 KB, two stages.  The CTA's super-block
+// matrix S_s (128 x 128, 32 KB) is loaded once; the output is staged in two
+// alternating 32 KB tiles, so a tile's store need not finish reading before
+// the next tile is staged.
 #pragma once
 
 #include "ptx.cuh"
@@ -37,10 +40,10 @@ struct BdgrArgs {
 struct BdgrCfg {
   static constexpr int BOX = 128 * 64 * 2;  // 16 KB
   static constexpr int TILE = 2 * BOX;      // 32 KB (128 x 128 bf16)
-  static constexpr int STAGE = 3 * TILE;    // A, S, C
+  static constexpr int STAGE = 2 * TILE;    // A, C
   static constexpr int STAGES = 2;
-  static constexpr int OUT = TILE;          // bf16 output staging
-  static constexpr int SMEM = 1024 + STAGES * STAGE + OUT + 256;
+  static constexpr int OUT = 2 * TILE;      // two bf16 output staging tiles
+  static constexpr int SMEM = 1024 + STAGES * STAGE + TILE /* S */ + OUT + 256;
   static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -54,13 +57,15 @@ __global__ void __launch_bounds__(320, 1)
   // 1024-byte aligned by pointer arithmetic on the shared array, so that the
   // compiler keeps shared-memory instructions for the accesses through it
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* out_stage = smem + STAGES * Cfg::STAGE;
+  uint8_t* s_tile = smem + STAGES * Cfg::STAGE;
+  uint8_t* out_stage = s_tile + Cfg::TILE;
   uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* gdone = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gdone + 1);
+  uint64_t* sfull = gdone + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -82,6 +87,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&tempty[a], 256);
     }
     mbar_init(gdone, 1);
+    mbar_init(sfull, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -102,6 +108,9 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      mbar_arrive_expect_tx(sfull, Cfg::TILE);
+      tma_load_2d(s_tile, &tmS, sfull, 0, f0);
+      tma_load_2d(s_tile + Cfg::BOX, &tmS, sfull, 64, f0);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_phase[STAGES] = {0, 0};
@@ -110,24 +119,21 @@ __global__ void __launch_bounds__(320, 1)
         const int m0 = (slot + i * args.nslots) * 128;
         if (!mbar_wait(&empty[stage], phase ^ 1u, tmo, abort_flag)) break;
         uint8_t* sa = smem + stage * Cfg::STAGE;
-        uint8_t* ss = sa + Cfg::TILE;
-        uint8_t* sc = ss + Cfg::TILE;
+        uint8_t* sc = sa + Cfg::TILE;
         mbar_arrive_expect_tx(&full[stage], Cfg::STAGE);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           tma_load_2d(sa + h * Cfg::BOX, &tmA, &full[stage], f0 + 64 * h, m0);
-          tma_load_2d(ss + h * Cfg::BOX, &tmS, &full[stage], 64 * h, f0);
           tma_load_2d(sc + h * Cfg::BOX, &tmC, &full[stage], f0 + 64 * h, m0);
         }
         issued[stage] = true;
         issued_phase[stage] = phase;
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
+      volatile int never = 0;
       for (int i = 0; i < STAGES; ++i)
-        if (issued[i]) {
-          volatile int never = 0;
-          mbar_wait(&full[i], issued_phase[i], tmo, &never);
-        }
+        if (issued[i]) mbar_wait(&full[i], issued_phase[i], tmo, &never);
+      mbar_wait(sfull, 0, tmo, &never);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -135,9 +141,10 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // A S^T
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, 128, true, true);    // A^T C
       const uint32_t d_g = tmem_base + 256;
+      const uint32_t ss = smem_u32(s_tile);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      bool ok = ntiles == 0 || mbar_wait(sfull, 0, tmo, abort_flag);
       for (int i = 0; i < ntiles && ok; ++i) {
         const int acc = i & 1;
         const uint32_t acc_phase = (i >> 1) & 1;
@@ -145,8 +152,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(&full[stage], phase, tmo, abort_flag)) break;
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE);
-        const uint32_t ss = sa + Cfg::TILE;
-        const uint32_t sc = ss + Cfg::TILE;
+        const uint32_t sc = sa + Cfg::TILE;
         const uint32_t d_t = tmem_base + acc * 128;
         // transform: K = 128 input features, 8 steps of 16 (two 64-wide boxes)
 #pragma unroll
@@ -193,9 +199,11 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (leader) bulk_wait_read_all();
+      // the store from this staging tile, two tiles back, must have read it
+      if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
       named_barrier(1, 256);
-      uint8_t* box = out_stage + half * Cfg::BOX;
+      uint8_t* ostage = out_stage + (i & 1) * Cfg::TILE;
+      uint8_t* box = ostage + half * Cfg::BOX;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t* src = r[q >> 2] + (q & 3) * 8;
@@ -209,8 +217,8 @@ __global__ void __launch_bounds__(320, 1)
       fence_proxy_async_smem();
       named_barrier(1, 256);
       if (leader) {
-        tma_store_2d(&tmOut, out_stage, f0, m0);
-        if (f0 + 64 < args.N) tma_store_2d(&tmOut, out_stage + Cfg::BOX, f0 + 64, m0);
+        tma_store_2d(&tmOut, ostage, f0, m0);
+        if (f0 + 64 < args.N) tma_store_2d(&tmOut, ostage + Cfg::BOX, f0 + 64, m0);
         bulk_commit();
       }
     }
